@@ -1,0 +1,185 @@
+"""GB300 (sm_103a) Multi-Head Latent Attention prolog.
+
+Thin Python binding over the C ABI of ``include/mla_prolog.h``: the functions below
+have the C names and only marshal arguments (torch tensors -> ``mla_tensor``
+descriptors).  Every step of the prolog runs in the CUDA kernels of
+``libmla_prolog.so``; there is no CPU path.  If the library is missing, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+__all__ = [
+    "MlaError", "TENSOR_ARGS", "lib", "mla_prolog_workspace_size", "mla_prolog",
+    "mla_prolog_device_status", "mla_prolog_status_string", "STATUS", "DEV_CACHE_INDEX_RANGE",
+    "DEV_WAIT_TIMEOUT", "library_path", "mla_prolog_timing_enable", "mla_prolog_timing_read",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libmla_prolog.so")
+
+STATUS = {0: "MLA_OK", 161001: "MLA_ERR_PARAM_NULLPTR", 161002: "MLA_ERR_PARAM_INVALID",
+          361001: "MLA_ERR_RUNTIME", 561002: "MLA_ERR_TILING"}
+DEV_CACHE_INDEX_RANGE = 0x1
+DEV_WAIT_TIMEOUT = 0x2
+
+# Positional order of the tensor arguments of the C entry points (before the scalars).
+TENSOR_ARGS = ("x", "w_dq", "w_uqqr", "w_uk", "w_dkvkr", "gamma_cq", "gamma_ckv", "rope_sin", "rope_cos",
+               "cache_index", "kv_cache", "kr_cache", "dequant_scale_x", "dequant_scale_w_dq",
+               "dequant_scale_w_uqqr", "dequant_scale_w_dkvkr", "quant_scale_ckv", "quant_scale_ckr",
+               "smooth_scales_cq")
+OUTPUT_ARGS = ("q_out", "q_rope_out", "dequant_scale_q_nope_out")
+
+
+class MlaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+class MlaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4)]
+
+
+class MlaKernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("ms", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libmla_prolog.so (fails loudly when it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"{library_path} is missing: build it with attention_pre_processing_gb300.build.build()")
+        L = ctypes.CDLL(library_path)
+        P = ctypes.POINTER(MlaTensor)
+        tens = [P] * len(TENSOR_ARGS)
+        scal = [ctypes.c_double, ctypes.c_double, ctypes.c_char_p]
+        outs = [P] * len(OUTPUT_ARGS)
+        L.mla_prolog_workspace_size.argtypes = tens + scal + outs + [ctypes.POINTER(ctypes.c_uint64)]
+        L.mla_prolog_workspace_size.restype = ctypes.c_int
+        L.mla_prolog.argtypes = tens + scal + outs + [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
+        L.mla_prolog.restype = ctypes.c_int
+        L.mla_prolog_device_status.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
+                                               ctypes.POINTER(ctypes.c_uint32)]
+        L.mla_prolog_device_status.restype = ctypes.c_int
+        L.mla_prolog_timing_enable.argtypes = [ctypes.c_int]
+        L.mla_prolog_timing_enable.restype = ctypes.c_int
+        L.mla_prolog_timing_read.argtypes = [ctypes.POINTER(MlaKernelTime), ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+        L.mla_prolog_timing_read.restype = ctypes.c_int
+        L.mla_prolog_status_string.argtypes = [ctypes.c_int]
+        L.mla_prolog_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.bfloat16: 0, torch.int8: 1, torch.float32: 2, torch.int64: 3}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def describe(t) -> Optional[MlaTensor]:
+    """torch tensor -> mla_tensor descriptor (no copy; the tensor must stay alive)."""
+    if t is None:
+        return None
+    if isinstance(t, MlaTensor):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    if t.dim() < 1 or t.dim() > 4:
+        raise ValueError("tensors have 1 to 4 dimensions")
+    d = MlaTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _dtype_code(t)
+    d.ndim = t.dim()
+    for i, s in enumerate(t.shape):
+        d.shape[i] = int(s)
+    return d
+
+
+def _marshal(tensors: Dict, eps_cq: float, eps_ckv: float, cache_mode: Optional[str]):
+    descs = [describe(tensors.get(k)) for k in TENSOR_ARGS]
+    outs = [describe(tensors.get(k)) for k in OUTPUT_ARGS]
+    ptrs = [ctypes.byref(d) if d is not None else None for d in descs]
+    optrs = [ctypes.byref(d) if d is not None else None for d in outs]
+    cm = None if cache_mode is None else cache_mode.encode()
+    return ptrs + [float(eps_cq), float(eps_ckv), cm] + optrs, (descs, outs)
+
+
+def mla_prolog_workspace_size(tensors: Dict, eps_cq: float, eps_ckv: float,
+                              cache_mode: Optional[str] = "PA_BSND") -> int:
+    """Phase 1: bytes of device workspace for these arguments (raises MlaError on a bad argument)."""
+    args, _keep = _marshal(tensors, eps_cq, eps_ckv, cache_mode)
+    out = ctypes.c_uint64(0)
+    rc = lib().mla_prolog_workspace_size(*args, ctypes.byref(out))
+    if rc != 0:
+        raise MlaError(rc, "mla_prolog_workspace_size")
+    return int(out.value)
+
+
+def _ptr(x) -> int:
+    return x if isinstance(x, int) else x.data_ptr()
+
+
+def mla_prolog(tensors: Dict, eps_cq: float, eps_ckv: float, workspace, workspace_bytes: Optional[int] = None,
+               stream=None, cache_mode: Optional[str] = "PA_BSND", check: bool = True) -> int:
+    """Phase 2: enqueue the prolog on ``stream`` (a torch.cuda.Stream, a raw handle, or None for
+    torch's current stream).  ``workspace`` is a device tensor or address."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    args, _keep = _marshal(tensors, eps_cq, eps_ckv, cache_mode)
+    rc = lib().mla_prolog(*args, ctypes.c_void_p(_ptr(workspace)), ctypes.c_uint64(workspace_bytes),
+                          ctypes.c_void_p(stream))
+    if check and rc != 0:
+        raise MlaError(rc, "mla_prolog")
+    return rc
+
+
+def mla_prolog_device_status(workspace, workspace_bytes: Optional[int] = None, stream=None) -> int:
+    """Wait for the stream and return the device status bits of the last call on ``workspace``."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    bits = ctypes.c_uint32(0)
+    rc = lib().mla_prolog_device_status(ctypes.c_void_p(_ptr(workspace)), ctypes.c_uint64(workspace_bytes),
+                                        ctypes.c_void_p(stream), ctypes.byref(bits))
+    if rc != 0:
+        raise MlaError(rc, "mla_prolog_device_status")
+    return int(bits.value)
+
+
+def mla_prolog_timing_enable(enable: bool) -> None:
+    lib().mla_prolog_timing_enable(1 if enable else 0)
+
+
+def mla_prolog_timing_read():
+    """[(kernel name, ms), ...] of the most recent call made while timing was enabled."""
+    buf = (MlaKernelTime * 16)()
+    n = ctypes.c_int(0)
+    rc = lib().mla_prolog_timing_read(buf, 16, ctypes.byref(n))
+    if rc != 0:
+        raise MlaError(rc, "mla_prolog_timing_read")
+    return [(buf[i].name.decode(), float(buf[i].ms)) for i in range(min(n.value, 16))]
+
+
+def mla_prolog_status_string(code: int) -> str:
+    return lib().mla_prolog_status_string(int(code)).decode()

@@ -1,0 +1,741 @@
+// C ABI of the MLA prolog: argument validation, tile planning, workspace layout, TMA
+// descriptors and kernel launches.  Declarations and argument documentation: mla_prolog.h.
+//
+// Pipeline of one call (all kernels on the caller's stream, chained with programmatic
+// dependent launch so each grid's prologue overlaps the previous grid's tail):
+//   [int8 operands only] widen int8 tokenX / weights to bf16 in the workspace
+//   K1  x . [W^DQ | W^DKV | W^KR]        -> fp32 partials (decode) or fp32 rows (prefill)
+//   F1  sum partials, RmsNorm, RoPE(k^R), kv/kr cache writes, c^Q (bf16 or int8 codes)
+//   K2  c^Q . W^UqQr                      -> fp32 partials + F2 (decode), or fused RoPE epilogue
+//   K3  q^C[:, n, :] . W^UK[n] per head   -> queryOut bf16, or int8 + dequantScaleQNope
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mla_prolog.h"
+#include "finalize.cuh"
+#include "gemm_tc.cuh"
+
+using namespace mla;
+
+namespace {
+
+// ---------------------------------------------------------------- validation
+
+struct Dims {
+    int64_t T, He, Hcq, N, D, Dr, Hckv, block_num, block_size;
+};
+
+struct Scenario {
+    bool x_i8;      // int8 tokenX, weightDq, weightDkvKr
+    bool uqqr_i8;   // int8 weightUqQr
+    bool kv_i8;
+    bool kr_i8;
+    bool q_i8;      // queryOut int8: dynamic quantisation of q^N
+};
+
+struct Args {
+    const mla_tensor *x, *wdq, *wuqqr, *wuk, *wdkvkr, *gcq, *gckv, *sin, *cos, *idx, *kv, *kr;
+    const mla_tensor *sx, *swdq, *swuqqr, *swdkvkr, *qckv, *qckr, *smooth;
+    double eps_cq, eps_ckv;
+    const char* cache_mode;
+    const mla_tensor *qout, *qrope, *qscale;
+};
+
+int64_t numel(const mla_tensor* t) {
+    int64_t n = 1;
+    for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+    return n;
+}
+
+bool shape_is(const mla_tensor* t, std::initializer_list<int64_t> s) {
+    if (t->ndim != (int)s.size()) return false;
+    int i = 0;
+    for (int64_t v : s)
+        if (t->shape[i++] != v) return false;
+    return true;
+}
+
+bool aligned16(const mla_tensor* t) {
+    return t->data == nullptr || (reinterpret_cast<uintptr_t>(t->data) & 15u) == 0;
+}
+
+// A per-token tensor: (T, rest...) or (B, S, rest...).  Returns T or -1.
+int64_t tokens_of(const mla_tensor* t, int rest_dims) {
+    const int lead = t->ndim - rest_dims;
+    if (lead != 1 && lead != 2) return -1;
+    int64_t T = t->shape[0];
+    if (lead == 2) T *= t->shape[1];
+    return T;
+}
+
+bool rest_is(const mla_tensor* t, int rest_dims, std::initializer_list<int64_t> s) {
+    if ((int)s.size() != rest_dims) return false;
+    int i = t->ndim - rest_dims;
+    for (int64_t v : s)
+        if (t->shape[i++] != v) return false;
+    return true;
+}
+
+// A (1, n) or (n) fp32 vector.
+bool vec_f32(const mla_tensor* t, int64_t n) {
+    if (t->dtype != MLA_DT_FP32) return false;
+    return shape_is(t, {n}) || shape_is(t, {1, n});
+}
+
+mla_status validate(const Args& a, Dims& d, Scenario& sc) {
+    const mla_tensor* req[] = {a.x, a.wdq, a.wuqqr, a.wuk, a.wdkvkr, a.gcq, a.gckv, a.sin, a.cos,
+                               a.idx, a.kv, a.kr, a.qout, a.qrope};
+    for (const mla_tensor* t : req)
+        if (t == nullptr) return MLA_ERR_PARAM_NULLPTR;
+    const mla_tensor* all[] = {a.x, a.wdq, a.wuqqr, a.wuk, a.wdkvkr, a.gcq, a.gckv, a.sin, a.cos, a.idx, a.kv,
+                               a.kr, a.qout, a.qrope, a.sx, a.swdq, a.swuqqr, a.swdkvkr, a.qckv, a.qckr,
+                               a.smooth, a.qscale};
+    for (const mla_tensor* t : all) {
+        if (t == nullptr) continue;
+        if (t->ndim < 1 || t->ndim > 4) return MLA_ERR_PARAM_INVALID;
+        for (int i = 0; i < t->ndim; ++i)
+            if (t->shape[i] < 0) return MLA_ERR_PARAM_INVALID;
+        if (t->data == nullptr && numel(t) > 0) return MLA_ERR_PARAM_NULLPTR;
+        if (!aligned16(t)) return MLA_ERR_PARAM_INVALID;
+    }
+
+    // tokenX (T, He) or (B, S, He)
+    if (a.x->dtype != MLA_DT_BF16 && a.x->dtype != MLA_DT_INT8) return MLA_ERR_PARAM_INVALID;
+    d.T = tokens_of(a.x, 1);
+    if (d.T < 0) return MLA_ERR_PARAM_INVALID;
+    d.He = a.x->shape[a.x->ndim - 1];
+    sc.x_i8 = a.x->dtype == MLA_DT_INT8;
+    // weightUk (N, D, Hckv)
+    if (a.wuk->dtype != MLA_DT_BF16 || a.wuk->ndim != 3) return MLA_ERR_PARAM_INVALID;
+    d.N = a.wuk->shape[0];
+    d.D = a.wuk->shape[1];
+    d.Hckv = a.wuk->shape[2];
+    // weightDq (He, Hcq)
+    if (a.wdq->ndim != 2 || a.wdq->shape[0] != d.He) return MLA_ERR_PARAM_INVALID;
+    d.Hcq = a.wdq->shape[1];
+    // weightUqQr (Hcq, N*(D+Dr))
+    if (a.wuqqr->ndim != 2 || a.wuqqr->shape[0] != d.Hcq || d.N <= 0) return MLA_ERR_PARAM_INVALID;
+    if (a.wuqqr->shape[1] % d.N != 0) return MLA_ERR_PARAM_INVALID;
+    d.Dr = a.wuqqr->shape[1] / d.N - d.D;
+    if (d.He <= 0 || d.Hcq <= 0 || d.D <= 0 || d.Dr <= 0 || d.Hckv <= 0) return MLA_ERR_PARAM_INVALID;
+    // weightDkvKr (He, Hckv + Dr)
+    if (!shape_is(a.wdkvkr, {d.He, d.Hckv + d.Dr})) return MLA_ERR_PARAM_INVALID;
+    // dtype pattern of the weights
+    sc.uqqr_i8 = a.wuqqr->dtype == MLA_DT_INT8;
+    if (a.wuqqr->dtype != MLA_DT_BF16 && !sc.uqqr_i8) return MLA_ERR_PARAM_INVALID;
+    const int32_t xdt = a.x->dtype;
+    if (a.wdq->dtype != xdt || a.wdkvkr->dtype != xdt) return MLA_ERR_PARAM_INVALID;
+    if (sc.x_i8 && !sc.uqqr_i8) return MLA_ERR_PARAM_INVALID;
+    // gammas
+    if (a.gcq->dtype != MLA_DT_BF16 || !(shape_is(a.gcq, {d.Hcq}) || shape_is(a.gcq, {1, d.Hcq})))
+        return MLA_ERR_PARAM_INVALID;
+    if (a.gckv->dtype != MLA_DT_BF16 || !(shape_is(a.gckv, {d.Hckv}) || shape_is(a.gckv, {1, d.Hckv})))
+        return MLA_ERR_PARAM_INVALID;
+    // rope tables, cacheIndex
+    for (const mla_tensor* t : {a.sin, a.cos}) {
+        if (t->dtype != MLA_DT_BF16 || tokens_of(t, 1) != d.T || !rest_is(t, 1, {d.Dr})) return MLA_ERR_PARAM_INVALID;
+        if (t->ndim == 3 && (t->shape[0] != a.x->shape[0] || a.x->ndim != 3)) return MLA_ERR_PARAM_INVALID;
+    }
+    if (a.idx->dtype != MLA_DT_INT64 || tokens_of(a.idx, 0) != d.T) return MLA_ERR_PARAM_INVALID;
+    // caches (BlockNum, BlockSize, Nkv = 1, H)
+    if (a.kv->ndim != 4 || a.kr->ndim != 4) return MLA_ERR_PARAM_INVALID;
+    d.block_num = a.kv->shape[0];
+    d.block_size = a.kv->shape[1];
+    if (!shape_is(a.kv, {d.block_num, d.block_size, 1, d.Hckv})) return MLA_ERR_PARAM_INVALID;
+    if (!shape_is(a.kr, {d.block_num, d.block_size, 1, d.Dr})) return MLA_ERR_PARAM_INVALID;
+    sc.kv_i8 = a.kv->dtype == MLA_DT_INT8;
+    sc.kr_i8 = a.kr->dtype == MLA_DT_INT8;
+    if (a.kv->dtype != MLA_DT_BF16 && !sc.kv_i8) return MLA_ERR_PARAM_INVALID;
+    if (a.kr->dtype != MLA_DT_BF16 && !sc.kr_i8) return MLA_ERR_PARAM_INVALID;
+    // outputs
+    if (a.qout->dtype != MLA_DT_BF16 && a.qout->dtype != MLA_DT_INT8) return MLA_ERR_PARAM_INVALID;
+    if (tokens_of(a.qout, 2) != d.T || !rest_is(a.qout, 2, {d.N, d.Hckv})) return MLA_ERR_PARAM_INVALID;
+    if (a.qrope->dtype != MLA_DT_BF16 || tokens_of(a.qrope, 2) != d.T || !rest_is(a.qrope, 2, {d.N, d.Dr}))
+        return MLA_ERR_PARAM_INVALID;
+    sc.q_i8 = a.qout->dtype == MLA_DT_INT8;
+    if (sc.q_i8) {
+        if (a.qscale == nullptr) return MLA_ERR_PARAM_NULLPTR;
+        if (a.qscale->dtype != MLA_DT_FP32) return MLA_ERR_PARAM_INVALID;
+        const bool ok = (a.qscale->ndim == 3 && a.qscale->shape[0] == d.T && a.qscale->shape[1] == d.N &&
+                         a.qscale->shape[2] == 1) ||
+                        (a.qscale->ndim == 2 && a.qscale->shape[0] == d.T && a.qscale->shape[1] == d.N);
+        if (!ok) return MLA_ERR_PARAM_INVALID;
+    } else if (a.qscale != nullptr && numel(a.qscale) > 1) {
+        return MLA_ERR_PARAM_INVALID;
+    }
+
+    // optional-argument pattern of each scenario (page: scenario / dtype table)
+    const int64_t W = d.N * (d.D + d.Dr);
+    if (sc.x_i8) {
+        if (!a.sx || !a.swdq || !a.swuqqr || !a.swdkvkr) return MLA_ERR_PARAM_NULLPTR;
+        if (a.sx->dtype != MLA_DT_FP32 || !(shape_is(a.sx, {d.T, 1}) || shape_is(a.sx, {d.T})))
+            return MLA_ERR_PARAM_INVALID;
+        if (!vec_f32(a.swdq, d.Hcq) || !vec_f32(a.swdkvkr, d.Hckv + d.Dr)) return MLA_ERR_PARAM_INVALID;
+        if (sc.kr_i8 || a.qckr) return MLA_ERR_PARAM_INVALID;  // krCache stays bf16 in full quantisation
+    } else {
+        if (a.sx || a.swdq || a.swdkvkr) return MLA_ERR_PARAM_INVALID;
+    }
+    if (sc.uqqr_i8) {
+        if (!a.swuqqr) return MLA_ERR_PARAM_NULLPTR;
+        if (!vec_f32(a.swuqqr, W)) return MLA_ERR_PARAM_INVALID;
+        if (a.smooth && !vec_f32(a.smooth, d.Hcq)) return MLA_ERR_PARAM_INVALID;
+    } else {
+        if (a.swuqqr || a.smooth) return MLA_ERR_PARAM_INVALID;
+    }
+    if (sc.kv_i8) {
+        if (!sc.uqqr_i8) return MLA_ERR_PARAM_INVALID;   // a quantised cache needs a quantised scenario
+        if (!a.qckv) return MLA_ERR_PARAM_NULLPTR;
+        if (!vec_f32(a.qckv, d.Hckv)) return MLA_ERR_PARAM_INVALID;
+        if (!sc.x_i8) {
+            // partial quantisation with quantised caches: both caches are int8
+            if (!sc.kr_i8) return MLA_ERR_PARAM_INVALID;
+            if (!a.qckr) return MLA_ERR_PARAM_NULLPTR;
+            if (!vec_f32(a.qckr, d.Dr)) return MLA_ERR_PARAM_INVALID;
+        }
+    } else {
+        if (a.qckv || a.qckr || sc.kr_i8) return MLA_ERR_PARAM_INVALID;
+    }
+    if (!std::isfinite(a.eps_cq) || !std::isfinite(a.eps_ckv) || a.eps_cq < 0 || a.eps_ckv < 0)
+        return MLA_ERR_PARAM_INVALID;
+    if (a.cache_mode != nullptr && std::strcmp(a.cache_mode, "PA_BSND") != 0) return MLA_ERR_PARAM_INVALID;
+
+    // tiling rules of the kernels
+    if (d.He % 8 || d.Hcq % 64 || d.D % 8 || (d.Dr & 1) || W % 8 || (d.Hckv + d.Dr) % 8 || d.Hckv % 8)
+        return MLA_ERR_TILING;
+    if (sc.q_i8 && d.Hckv > 512) return MLA_ERR_TILING;
+    if (d.T > (int64_t)INT32_MAX || d.He > (int64_t)INT32_MAX || W > (int64_t)INT32_MAX) return MLA_ERR_TILING;
+    return MLA_OK;
+}
+
+// ---------------------------------------------------------------------- plan
+
+constexpr int kBN12 = 192;   // column tile of the two weight-streaming GEMMs (one head of 128+64)
+
+struct GemmPlan {
+    int split = 0, msub = 1, grid = 0, m_tiles = 1, n_tiles = 0, kblocks = 0, bn = kBN12;
+    long long total = 0;
+};
+
+struct Plan {
+    GemmPlan g1, g2, g3;
+    bool g2_fused = false;   // K2 epilogue does RoPE and q^C (no F2)
+    int64_t ncols1 = 0, ncols2 = 0;
+    size_t off_cq = 0, off_cqs = 0, off_qc = 0, off_p1 = 0, off_p2 = 0, off_xb = 0, off_wdq = 0, off_wdkvkr = 0,
+           off_wuqqr = 0, bytes = 0;
+};
+
+constexpr size_t kStatusBytes = 1024;
+
+size_t up1024(size_t v) { return (v + 1023) & ~size_t(1023); }
+
+int device_sms(int* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return -1;
+    *out = sms;
+    return 0;
+}
+
+void plan_split_or_tile(GemmPlan& g, int64_t T, int64_t ncols, int64_t K, int sms) {
+    g.kblocks = (int)((K + kBK - 1) / kBK);
+    g.n_tiles = (int)((ncols + g.bn - 1) / g.bn);
+    if (T <= 256 && g.n_tiles <= sms) {
+        g.split = 1;
+        g.msub = T <= 128 ? 1 : 2;
+        g.m_tiles = 1;
+        g.total = (long long)g.n_tiles * g.kblocks;
+        g.grid = (int)(g.total < sms ? g.total : sms);
+    } else {
+        g.split = 0;
+        g.msub = 2;
+        g.m_tiles = (int)((T + 255) / 256);
+        const long long tiles = (long long)g.m_tiles * g.n_tiles;
+        g.grid = (int)(tiles < sms ? tiles : sms);
+    }
+}
+
+Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
+    Plan p;
+    const int64_t T = d.T;
+    p.ncols1 = d.Hcq + d.Hckv + d.Dr;
+    p.ncols2 = d.N * (d.D + d.Dr);
+    plan_split_or_tile(p.g1, T, p.ncols1, d.He, sms);
+    plan_split_or_tile(p.g2, T, p.ncols2, d.Hcq, sms);
+    p.g2_fused = !p.g2.split && d.D == 128 && d.Dr == 64;
+    // K3: per head, 128-row tiles; an int8 output needs the whole Hckv row in one tile.
+    p.g3.bn = sc.q_i8 ? 512 : 256;
+    p.g3.kblocks = (int)((d.D + kBK - 1) / kBK);
+    const int tph = (int)((d.Hckv + p.g3.bn - 1) / p.g3.bn);
+    p.g3.n_tiles = (int)(d.N * tph);
+    p.g3.m_tiles = (int)((T + 127) / 128);
+    p.g3.msub = 1;
+    {
+        const long long tiles = (long long)p.g3.m_tiles * p.g3.n_tiles;
+        p.g3.grid = (int)(tiles < sms ? tiles : sms);
+    }
+
+    size_t off = kStatusBytes;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = up1024(off + bytes);
+        return o;
+    };
+    p.off_cq = take((size_t)T * d.Hcq * 2);
+    p.off_cqs = take((size_t)T * 4);
+    p.off_qc = take((size_t)T * d.N * d.D * 2);
+    p.off_p1 = take(p.g1.split ? (size_t)2 * p.g1.grid * T * p.g1.bn * 4 : (size_t)T * p.ncols1 * 4);
+    if (p.g2.split)
+        p.off_p2 = take((size_t)2 * p.g2.grid * T * p.g2.bn * 4);
+    else if (!p.g2_fused)
+        p.off_p2 = take((size_t)T * p.ncols2 * 4);
+    if (sc.x_i8) {
+        p.off_xb = take((size_t)T * d.He * 2);
+        p.off_wdq = take((size_t)d.He * d.Hcq * 2);
+        p.off_wdkvkr = take((size_t)d.He * (d.Hckv + d.Dr) * 2);
+    }
+    if (sc.uqqr_i8) p.off_wuqqr = take((size_t)d.Hcq * p.ncols2 * 2);
+    p.bytes = off;
+    return p;
+}
+
+// --------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// bf16 map with a 64-element (128-byte) inner box and 128-byte swizzle.
+bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                const uint32_t* box) {
+    cuuint64_t gd[3];
+    cuuint64_t gs[2];
+    cuuint32_t bx[3];
+    cuuint32_t es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs,
+                                bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Row-major (rows, cols) bf16 matrix.  Activations use a 128-row box, weights a 64-row box.
+bool map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    const uint64_t dims[2] = {cols, rows};
+    const uint64_t strides[1] = {cols * 2};
+    const uint32_t box[2] = {64, box_rows};
+    return encode_map(m, base, 2, dims, strides, box);
+}
+
+// --------------------------------------------------------------------- timing
+
+struct Timing {
+    bool enabled = false;
+    bool have = false;
+    int n = 0;                        // kernels recorded in the last timed call
+    cudaEvent_t ev[16] = {};
+    const char* name[16] = {};
+};
+Timing g_timing;
+std::mutex g_timing_mu;
+
+// Records the event that closes the interval of the kernel just launched.
+void timing_mark(cudaStream_t st, const char* name) {
+    if (!g_timing.enabled || g_timing.n >= 15) return;
+    if (!g_timing.ev[g_timing.n + 1] && cudaEventCreate(&g_timing.ev[g_timing.n + 1]) != cudaSuccess) return;
+    g_timing.name[g_timing.n] = name;
+    cudaEventRecord(g_timing.ev[g_timing.n + 1], st);
+    ++g_timing.n;
+}
+
+void timing_begin(cudaStream_t st) {
+    if (!g_timing.enabled) return;
+    g_timing.n = 0;
+    g_timing.have = false;
+    if (!g_timing.ev[0] && cudaEventCreate(&g_timing.ev[0]) != cudaSuccess) return;
+    cudaEventRecord(g_timing.ev[0], st);
+}
+
+// --------------------------------------------------------------------- launch
+
+template <typename Kernel, typename... ArgsT>
+cudaError_t launch(Kernel k, int grid, int block, size_t smem, cudaStream_t st, ArgsT... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_timing.enabled ? 0 : 1;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
+template <int BN, int MSUB, int STAGES, int EPI>
+cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                        const GemmArgs& args) {
+    using C = GemmCfg<BN, MSUB, STAGES>;
+    auto k = gemm_tc_kernel<BN, MSUB, STAGES, EPI>;
+    // The attribute is per function; setting it on every call is cheap and device-safe.
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    return launch(k, grid, kGemmThreads, C::kSmem, st, a, b0, b1, args);
+}
+
+struct Launched {
+    const Args* a;
+    Dims d;
+    Scenario sc;
+    Plan p;
+    uint8_t* ws;
+    cudaStream_t st;
+    int sms;
+};
+
+int sms_of(const Launched& L) { return L.sms; }
+
+mla_status run(const Launched& L) {
+    const Args& a = *L.a;
+    const Dims& d = L.d;
+    const Scenario& sc = L.sc;
+    const Plan& p = L.p;
+    uint8_t* ws = L.ws;
+    cudaStream_t st = L.st;
+    uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+    const int T = (int)d.T;
+    if (!get_encoder()) return MLA_ERR_RUNTIME;
+
+    // int8 operands are widened to bf16 (exact) for the bf16 tensor-core path.
+    const void* x_bf = a.x->data;
+    const void* wdq_bf = a.wdq->data;
+    const void* wdkvkr_bf = a.wdkvkr->data;
+    const void* wuqqr_bf = a.wuqqr->data;
+    auto widen = [&](const void* src, size_t off, long long n) -> cudaError_t {
+        const long long blocks = (n / 16 + 255) / 256;
+        const int grid = (int)(blocks < 4096 ? (blocks > 0 ? blocks : 1) : 4096);
+        return launch(convert_i8_to_bf16_kernel, grid, 256, 0, st, reinterpret_cast<const int8_t*>(src),
+                      reinterpret_cast<__nv_bfloat16*>(ws + off), n);
+    };
+    if (sc.x_i8) {
+        if (widen(a.x->data, p.off_xb, (long long)d.T * d.He) != cudaSuccess) return MLA_ERR_RUNTIME;
+        timing_mark(st, "widen_x");
+        if (widen(a.wdq->data, p.off_wdq, (long long)d.He * d.Hcq) != cudaSuccess) return MLA_ERR_RUNTIME;
+        timing_mark(st, "widen_w_dq");
+        if (widen(a.wdkvkr->data, p.off_wdkvkr, (long long)d.He * (d.Hckv + d.Dr)) != cudaSuccess)
+            return MLA_ERR_RUNTIME;
+        timing_mark(st, "widen_w_dkvkr");
+        x_bf = ws + p.off_xb;
+        wdq_bf = ws + p.off_wdq;
+        wdkvkr_bf = ws + p.off_wdkvkr;
+    }
+    if (sc.uqqr_i8) {
+        if (widen(a.wuqqr->data, p.off_wuqqr, (long long)d.Hcq * p.ncols2) != cudaSuccess) return MLA_ERR_RUNTIME;
+        timing_mark(st, "widen_w_uqqr");
+        wuqqr_bf = ws + p.off_wuqqr;
+    }
+
+    // ---- K1: down-projection
+    CUtensorMap mA1, mB1a, mB1b;
+    if (!map_2d(&mA1, x_bf, d.T, d.He, 128) || !map_2d(&mB1a, wdq_bf, d.He, d.Hcq, 64) ||
+        !map_2d(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64))
+        return MLA_ERR_RUNTIME;
+    float* p1 = reinterpret_cast<float*>(ws + p.off_p1);
+    GemmArgs g1 = {};
+    g1.T = T;
+    g1.kblocks = p.g1.kblocks;
+    g1.ncols = (int)p.ncols1;
+    g1.n_tiles = p.g1.n_tiles;
+    g1.m_tiles = p.g1.m_tiles;
+    g1.split = p.g1.split;
+    g1.total = p.g1.total;
+    g1.b_split_col = (int)d.Hcq;
+    g1.clear_status = 1;
+    g1.out_f32 = p1;
+    g1.status = status;
+    cudaError_t e = (p.g1.msub == 1) ? launch_gemm<kBN12, 1, 5, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
+                                     : launch_gemm<kBN12, 2, 3, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+    if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+    timing_mark(st, "k1_down_proj");
+
+    // ---- F1: partial sums, RmsNorm, RoPE(k^R), cache writes, c^Q
+    DownArgs f1 = {};
+    f1.T = T;
+    f1.Hcq = (int)d.Hcq;
+    f1.Hckv = (int)d.Hckv;
+    f1.Dr = (int)d.Dr;
+    f1.src = {p1, p.g1.split, p.g1.total, p.g1.grid, p.g1.kblocks, p.g1.bn, T, (int)p.ncols1};
+    if (sc.x_i8) {
+        f1.scale_x = static_cast<const float*>(a.sx->data);
+        f1.scale_w_dq = static_cast<const float*>(a.swdq->data);
+        f1.scale_w_dkvkr = static_cast<const float*>(a.swdkvkr->data);
+    }
+    f1.gamma_cq = static_cast<const __nv_bfloat16*>(a.gcq->data);
+    f1.gamma_ckv = static_cast<const __nv_bfloat16*>(a.gckv->data);
+    f1.eps_cq = (float)a.eps_cq;
+    f1.eps_ckv = (float)a.eps_ckv;
+    f1.rope_cos = static_cast<const __nv_bfloat16*>(a.cos->data);
+    f1.rope_sin = static_cast<const __nv_bfloat16*>(a.sin->data);
+    f1.cache_index = static_cast<const long long*>(a.idx->data);
+    f1.nslots = d.block_num * d.block_size;
+    f1.kv_cache = a.kv->data;
+    f1.kv_int8 = sc.kv_i8;
+    f1.quant_scale_ckv = a.qckv ? static_cast<const float*>(a.qckv->data) : nullptr;
+    f1.kr_cache = a.kr->data;
+    f1.kr_int8 = sc.kr_i8;
+    f1.quant_scale_ckr = a.qckr ? static_cast<const float*>(a.qckr->data) : nullptr;
+    f1.c_q = reinterpret_cast<__nv_bfloat16*>(ws + p.off_cq);
+    f1.cq_quant = sc.uqqr_i8;
+    f1.smooth_cq = a.smooth ? static_cast<const float*>(a.smooth->data) : nullptr;
+    f1.c_q_scale = reinterpret_cast<float*>(ws + p.off_cqs);
+    f1.status = status;
+    {
+        const int grid = T < 16 * sms_of(L) ? T : 16 * sms_of(L);
+        e = launch(finalize_down_kernel, grid, kRowThreads, (size_t)p.ncols1 * 4, st, f1);
+        if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+        timing_mark(st, "f1_norm_rope_cache");
+    }
+
+    // ---- K2: up-projection
+    CUtensorMap mA2, mB2;
+    if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, 128) || !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64))
+        return MLA_ERR_RUNTIME;
+    const float* row_scale = sc.uqqr_i8 ? reinterpret_cast<const float*>(ws + p.off_cqs) : nullptr;
+    const float* col_scale = sc.uqqr_i8 ? static_cast<const float*>(a.swuqqr->data) : nullptr;
+    __nv_bfloat16* qc = reinterpret_cast<__nv_bfloat16*>(ws + p.off_qc);
+    GemmArgs g2 = {};
+    g2.T = T;
+    g2.kblocks = p.g2.kblocks;
+    g2.ncols = (int)p.ncols2;
+    g2.n_tiles = p.g2.n_tiles;
+    g2.m_tiles = p.g2.m_tiles;
+    g2.split = p.g2.split;
+    g2.total = p.g2.total;
+    g2.b_split_col = INT32_MAX;   // one weight map
+    g2.status = status;
+    if (p.g2_fused) {
+        g2.N = (int)d.N;
+        g2.q_c = qc;
+        g2.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
+        g2.rope_cos = f1.rope_cos;
+        g2.rope_sin = f1.rope_sin;
+        g2.row_scale = row_scale;
+        g2.col_scale = col_scale;
+        e = launch_gemm<kBN12, 2, 3, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2);
+    } else {
+        g2.out_f32 = reinterpret_cast<float*>(ws + p.off_p2);
+        e = (p.g2.msub == 1) ? launch_gemm<kBN12, 1, 5, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2)
+                             : launch_gemm<kBN12, 2, 3, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2);
+    }
+    if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+    timing_mark(st, "k2_up_proj");
+    if (!p.g2_fused) {
+        UpArgs f2 = {};
+        f2.T = T;
+        f2.N = (int)d.N;
+        f2.D = (int)d.D;
+        f2.Dr = (int)d.Dr;
+        f2.src = {reinterpret_cast<const float*>(ws + p.off_p2), p.g2.split, p.g2.total, p.g2.grid, p.g2.kblocks,
+                  p.g2.bn, T, (int)p.ncols2};
+        f2.row_scale = row_scale;
+        f2.col_scale = col_scale;
+        f2.rope_cos = f1.rope_cos;
+        f2.rope_sin = f1.rope_sin;
+        f2.q_c = qc;
+        f2.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
+        const int grid = T < 16 * sms_of(L) ? T : 16 * sms_of(L);
+        e = launch(finalize_up_kernel, grid, kRowThreads, 0, st, f2);
+        if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+        timing_mark(st, "f2_rope_qc");
+    }
+
+    // ---- K3: per-head W^UK contraction
+    CUtensorMap mA3, mB3;
+    {
+        const uint64_t dims[3] = {(uint64_t)d.D, (uint64_t)d.N, (uint64_t)d.T};
+        const uint64_t strides[2] = {(uint64_t)d.D * 2, (uint64_t)d.N * d.D * 2};
+        const uint32_t box[3] = {64, 1, 128};
+        if (!encode_map(&mA3, qc, 3, dims, strides, box)) return MLA_ERR_RUNTIME;
+        const uint64_t dimsb[3] = {(uint64_t)d.Hckv, (uint64_t)d.D, (uint64_t)d.N};
+        const uint64_t stridesb[2] = {(uint64_t)d.Hckv * 2, (uint64_t)d.D * d.Hckv * 2};
+        const uint32_t boxb[3] = {64, 64, 1};
+        if (!encode_map(&mB3, a.wuk->data, 3, dimsb, stridesb, boxb)) return MLA_ERR_RUNTIME;
+    }
+    GemmArgs g3 = {};
+    g3.T = T;
+    g3.kblocks = p.g3.kblocks;
+    g3.ncols = (int)d.Hckv;
+    g3.n_tiles = p.g3.n_tiles;
+    g3.m_tiles = p.g3.m_tiles;
+    g3.split = 0;
+    g3.b_split_col = INT32_MAX;
+    g3.head_mode = 1;
+    g3.tiles_per_head = p.g3.n_tiles / (int)d.N;
+    g3.N = (int)d.N;
+    g3.Hckv = (int)d.Hckv;
+    g3.status = status;
+    if (sc.q_i8) {
+        g3.q_out_i8 = static_cast<int8_t*>(a.qout->data);
+        g3.q_scale = static_cast<float*>(a.qscale->data);
+        e = launch_gemm<512, 1, 2, EPI_QN>(p.g3.grid, st, mA3, mB3, mB3, g3);
+    } else {
+        g3.q_out_bf16 = static_cast<__nv_bfloat16*>(a.qout->data);
+        e = launch_gemm<256, 1, 4, EPI_QN>(p.g3.grid, st, mA3, mB3, mB3, g3);
+    }
+    if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+    timing_mark(st, "k3_absorb_uk");
+    if (g_timing.enabled) g_timing.have = true;
+    return MLA_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+#define MLA_TENSOR_PARAMS                                                                                      \
+    const mla_tensor *tokenX, const mla_tensor *weightDq, const mla_tensor *weightUqQr,                        \
+        const mla_tensor *weightUk, const mla_tensor *weightDkvKr, const mla_tensor *rmsnormGammaCq,          \
+        const mla_tensor *rmsnormGammaCkv, const mla_tensor *ropeSin, const mla_tensor *ropeCos,              \
+        const mla_tensor *cacheIndex, const mla_tensor *kvCache, const mla_tensor *krCache,                   \
+        const mla_tensor *dequantScaleX, const mla_tensor *dequantScaleWDq,                                   \
+        const mla_tensor *dequantScaleWUqQr, const mla_tensor *dequantScaleWDkvKr,                            \
+        const mla_tensor *quantScaleCkv, const mla_tensor *quantScaleCkr, const mla_tensor *smoothScalesCq,   \
+        double rmsnormEpsilonCq, double rmsnormEpsilonCkv, const char *cacheMode, const mla_tensor *queryOut, \
+        const mla_tensor *queryRopeOut, const mla_tensor *dequantScaleQNopeOut
+
+static Args pack_args(MLA_TENSOR_PARAMS) {
+    Args a;
+    a.x = tokenX;
+    a.wdq = weightDq;
+    a.wuqqr = weightUqQr;
+    a.wuk = weightUk;
+    a.wdkvkr = weightDkvKr;
+    a.gcq = rmsnormGammaCq;
+    a.gckv = rmsnormGammaCkv;
+    a.sin = ropeSin;
+    a.cos = ropeCos;
+    a.idx = cacheIndex;
+    a.kv = kvCache;
+    a.kr = krCache;
+    a.sx = dequantScaleX;
+    a.swdq = dequantScaleWDq;
+    a.swuqqr = dequantScaleWUqQr;
+    a.swdkvkr = dequantScaleWDkvKr;
+    a.qckv = quantScaleCkv;
+    a.qckr = quantScaleCkr;
+    a.smooth = smoothScalesCq;
+    a.eps_cq = rmsnormEpsilonCq;
+    a.eps_ckv = rmsnormEpsilonCkv;
+    a.cache_mode = cacheMode;
+    a.qout = queryOut;
+    a.qrope = queryRopeOut;
+    a.qscale = dequantScaleQNopeOut;
+    return a;
+}
+
+#define MLA_TENSOR_ARGS                                                                                          \
+    tokenX, weightDq, weightUqQr, weightUk, weightDkvKr, rmsnormGammaCq, rmsnormGammaCkv, ropeSin, ropeCos,     \
+        cacheIndex, kvCache, krCache, dequantScaleX, dequantScaleWDq, dequantScaleWUqQr, dequantScaleWDkvKr,    \
+        quantScaleCkv, quantScaleCkr, smoothScalesCq, rmsnormEpsilonCq, rmsnormEpsilonCkv, cacheMode, queryOut, \
+        queryRopeOut, dequantScaleQNopeOut
+
+extern "C" mla_status mla_prolog_workspace_size(MLA_TENSOR_PARAMS, uint64_t* workspaceSize) {
+    if (workspaceSize == nullptr) return MLA_ERR_PARAM_NULLPTR;
+    const Args a = pack_args(MLA_TENSOR_ARGS);
+    Dims d;
+    Scenario sc;
+    const mla_status s = validate(a, d, sc);
+    if (s != MLA_OK) return s;
+    if (d.T == 0) {
+        *workspaceSize = kStatusBytes;
+        return MLA_OK;
+    }
+    int sms = 0;
+    if (device_sms(&sms) != 0) return MLA_ERR_RUNTIME;
+    *workspaceSize = make_plan(d, sc, sms).bytes;
+    return MLA_OK;
+}
+
+extern "C" mla_status mla_prolog(MLA_TENSOR_PARAMS, void* workspace, uint64_t workspaceSize, void* stream) {
+    const Args a = pack_args(MLA_TENSOR_ARGS);
+    Dims d;
+    Scenario sc;
+    const mla_status s = validate(a, d, sc);
+    if (s != MLA_OK) return s;
+    if (d.T == 0) return MLA_OK;
+    if (workspace == nullptr) return MLA_ERR_PARAM_NULLPTR;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return MLA_ERR_PARAM_INVALID;
+    int sms = 0;
+    if (device_sms(&sms) != 0) return MLA_ERR_RUNTIME;
+    Launched L{&a, d, sc, make_plan(d, sc, sms), static_cast<uint8_t*>(workspace),
+               static_cast<cudaStream_t>(stream), sms};
+    if (workspaceSize < L.p.bytes) return MLA_ERR_PARAM_INVALID;
+    timing_begin(L.st);
+    return run(L);
+}
+
+extern "C" mla_status mla_prolog_device_status(const void* workspace, uint64_t workspaceSize, void* stream,
+                                               uint32_t* bits) {
+    if (workspace == nullptr || bits == nullptr) return MLA_ERR_PARAM_NULLPTR;
+    if (workspaceSize < sizeof(uint32_t)) return MLA_ERR_PARAM_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_RUNTIME;
+    if (cudaMemcpy(bits, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_RUNTIME;
+    return MLA_OK;
+}
+
+extern "C" mla_status mla_prolog_timing_enable(int enable) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    g_timing.enabled = enable != 0;
+    g_timing.have = false;
+    return MLA_OK;
+}
+
+extern "C" mla_status mla_prolog_timing_read(mla_kernel_time* out, int capacity, int* count) {
+    if (out == nullptr || count == nullptr) return MLA_ERR_PARAM_NULLPTR;
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    if (!g_timing.have || g_timing.n == 0) return MLA_ERR_PARAM_INVALID;
+    if (cudaEventSynchronize(g_timing.ev[g_timing.n]) != cudaSuccess) return MLA_ERR_RUNTIME;
+    *count = g_timing.n;
+    for (int i = 0; i < g_timing.n && i < capacity; ++i) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, g_timing.ev[i], g_timing.ev[i + 1]) != cudaSuccess) return MLA_ERR_RUNTIME;
+        std::memset(out[i].name, 0, sizeof out[i].name);
+        std::strncpy(out[i].name, g_timing.name[i], sizeof out[i].name - 1);
+        out[i].ms = ms;
+    }
+    return MLA_OK;
+}
+
+extern "C" const char* mla_prolog_status_string(mla_status status) {
+    switch (status) {
+        case MLA_OK: return "MLA_OK";
+        case MLA_ERR_PARAM_NULLPTR: return "MLA_ERR_PARAM_NULLPTR (161001): a required pointer is NULL";
+        case MLA_ERR_PARAM_INVALID: return "MLA_ERR_PARAM_INVALID (161002): shape, dtype or scenario not accepted";
+        case MLA_ERR_RUNTIME: return "MLA_ERR_RUNTIME (361001): a CUDA runtime call failed";
+        case MLA_ERR_TILING: return "MLA_ERR_TILING (561002): shapes outside the kernels' tiling rules";
+    }
+    return "unknown mla_status";
+}

@@ -56,7 +56,10 @@ class MlaConfig:
     theta: float = 1e4
     # scenario switches (aclnnMlaPrologV2WeightNz, Constraints: scenario table)
     x_int8: bool = False          # int8 full quantisation of tokenX and the three weights
+    uqqr_int8: bool = False       # partial quantisation: weightUqQr alone is int8
     kv_int8: bool = False         # kv cache quantised with quantScaleCkv
+    kr_int8: bool = False         # kr cache quantised with quantScaleCkr (partial quantisation)
+    smooth: bool = False          # pass smoothScalesCq ~ U(0.5, 1.5)
     q_int8: bool = False          # q^N dynamically quantised to int8 ("fifth path")
     outlier_frac: float = 0.0     # fraction of x elements multiplied by outlier_mult
     outlier_mult: float = 1.0
@@ -78,6 +81,8 @@ class MlaConfig:
         q = []
         if self.x_int8:
             q.append("int8-in")
+        elif self.uqqr_int8:
+            q.append("uqqr-int8")
         if self.kv_int8:
             q.append("kv-int8")
         if self.q_int8:
@@ -180,7 +185,10 @@ def make_inputs(cfg: MlaConfig, seed: Optional[int] = None) -> Dict[str, Optiona
         return (torch.randn(shape, generator=gen, dtype=torch.float32) * std).to(torch.bfloat16)
 
     out["w_dq"] = wmat((He, Hcq), cfg.w_std)
-    out["w_uqqr"] = wmat((Hcq, N * (D + Dr)), cfg.w_std)
+    if cfg.uqqr_int8 and not cfg.x_int8:
+        out["w_uqqr"] = _randint8(gen, (Hcq, N * (D + Dr)))
+    else:
+        out["w_uqqr"] = wmat((Hcq, N * (D + Dr)), cfg.w_std)
     uk_std = cfg.w_uk_std if cfg.w_uk_std is not None else cfg.w_std
     out["w_uk"] = (torch.randn((N, D, Hckv), generator=gen, dtype=torch.float32) * uk_std).to(torch.bfloat16)
     out["w_dkvkr"] = wmat((He, Hckv + Dr), cfg.w_std)
@@ -221,7 +229,8 @@ def make_inputs(cfg: MlaConfig, seed: Optional[int] = None) -> Dict[str, Optiona
     # caches pre-filled with random bits (the sentinel)
     kv_dtype = torch.int8 if cfg.kv_int8 else torch.bfloat16
     out["kv_cache"] = _random_bits(gen, (s.block_num, s.block_size, 1, Hckv), kv_dtype)
-    out["kr_cache"] = _random_bits(gen, (s.block_num, s.block_size, 1, Dr), torch.bfloat16)
+    kr_dtype = torch.int8 if cfg.kr_int8 else torch.bfloat16
+    out["kr_cache"] = _random_bits(gen, (s.block_num, s.block_size, 1, Dr), kr_dtype)
 
     # scales (aclnnMlaPrologV2WeightNz, Constraints: scenario table)
     for k in ("dequant_scale_x", "dequant_scale_w_dq", "dequant_scale_w_uqqr",
@@ -232,11 +241,20 @@ def make_inputs(cfg: MlaConfig, seed: Optional[int] = None) -> Dict[str, Optiona
         out["dequant_scale_w_dq"] = _uniform(gen, (1, Hcq), cfg.sw_lo, cfg.sw_hi).to(torch.float32)
         out["dequant_scale_w_uqqr"] = _uniform(gen, (1, N * (D + Dr)), cfg.sw_lo, cfg.sw_hi).to(torch.float32)
         out["dequant_scale_w_dkvkr"] = _uniform(gen, (1, Hckv + Dr), cfg.sw_lo, cfg.sw_hi).to(torch.float32)
+    elif cfg.uqqr_int8:
+        out["dequant_scale_w_uqqr"] = _uniform(gen, (1, N * (D + Dr)), cfg.sw_lo, cfg.sw_hi).to(torch.float32)
     if cfg.kv_int8:
         qs = _uniform(gen, (1, Hckv), cfg.ckv_lo, cfg.ckv_hi)
         if cfg.ckv_reciprocal:
             qs = 1.0 / qs
         out["quant_scale_ckv"] = qs.to(torch.float32)
+    if cfg.kr_int8:
+        qs = _uniform(gen, (1, Dr), cfg.ckv_lo, cfg.ckv_hi)
+        if cfg.ckv_reciprocal:
+            qs = 1.0 / qs
+        out["quant_scale_ckr"] = qs.to(torch.float32)
+    if cfg.smooth and (cfg.x_int8 or cfg.uqqr_int8):
+        out["smooth_scales_cq"] = _uniform(gen, (1, Hcq), 0.5, 1.5).to(torch.float32)
     return out
 
 

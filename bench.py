@@ -1,0 +1,410 @@
+"""Benchmark of the MLA prolog on one GB300 (or N independent replicas).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {cuda,reference}]
+
+One step = one mla_prolog() call (all kernels of the prolog) over one batch of synthetic
+DeepSeek-V3-shaped input: T = 32 decode tokens (the headline workload).  The L2 cache is
+flushed (a 2 x L2-size buffer is rewritten) before every timed step, outside the timed
+events.  Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (fp64 C, OpenMP) on the host cores instead, on a
+bounded sample of tokens of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "decode_t32"
+PREFILL = "prefill_t8192"
+METRIC = "MLA prolog tokens/s & µs/call (T=32 decode, T=8192) + % HBM/tensor roofline"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ byte / flop model
+
+def step_bytes(s, q_int8=False):
+    """Algorithmic bytes of one call: every input read once, every output and cache row written once."""
+    W = s.He * (s.Hcq + s.Hckv + s.Dr) + s.Hcq * s.N * (s.D + s.Dr) + s.N * s.D * s.Hckv
+    per_tok = (s.He * 2 + 2 * s.Dr * 2 + 8 + s.N * s.Hckv * (1 if q_int8 else 2) + s.N * s.Dr * 2
+               + s.Hckv * 2 + s.Dr * 2 + (s.N * 4 if q_int8 else 0))
+    return W * 2 + (s.Hcq + s.Hckv) * 2 + s.T * per_tok
+
+
+def k2_bytes(s):
+    """Up-projection c^Q . W^UqQr: the weight, c^Q in, q^C and q^R out (bf16)."""
+    return s.Hcq * s.N * (s.D + s.Dr) * 2 + s.T * s.Hcq * 2 + s.T * s.N * (s.D + s.Dr) * 2
+
+
+def k2_flops(s):
+    return 2 * s.T * s.Hcq * s.N * (s.D + s.Dr)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_cuda(args, rank, world):
+    import torch
+    from attention_pre_processing_gb300 import build as cuda_build
+    from attention_pre_processing_gb300 import workloads, mla_prolog, mla_prolog_timing_enable, mla_prolog_timing_read
+    from attention_pre_processing_gb300.runner import PrologCall
+
+    cuda_build.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    peaks = _peaks()
+    cfg = workloads.config(HEADLINE)
+    s = cfg.shape
+    inp = workloads.make_inputs(cfg)
+    call = PrologCall(cfg, inp, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def flush_l2():
+        flush.fill_(1)
+
+    # warm-up
+    for _ in range(args.warmup):
+        flush_l2()
+        call(stream)
+    torch.cuda.synchronize(dev)
+    if call.status(stream) != 0:
+        raise RuntimeError("device status bits set during warm-up")
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            flush_l2()
+            starts[i].record(stream)
+            call(stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        t_wall = time.perf_counter() - t_wall0
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    if call.status(stream) != 0:
+        raise RuntimeError("device status bits set during the timed region")
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    tokens = s.T * K * world
+    value = tokens / (total_ms / 1e3)
+    kernels_per_step = 5 if not cfg.x_int8 else 9
+
+    # per-kernel durations (each kernel alone, events between kernels) for the roofline
+    mla_prolog_timing_enable(True)
+    per_kernel = {}
+    for i in range(max(K, 10)):
+        flush_l2()
+        call(stream)
+        for name, ms in mla_prolog_timing_read():
+            per_kernel.setdefault(name, []).append(ms)
+    mla_prolog_timing_enable(False)
+    kern_ms = {k: statistics.mean(v) for k, v in per_kernel.items()}
+    k2_ms = kern_ms.get("k2_up_proj")
+    dom_bytes = k2_bytes(s)
+    achieved = dom_bytes / (k2_ms / 1e3) / 1e9 if k2_ms else None
+    traffic = _read_traffic("k2_up_proj", HEADLINE)
+    roofline = {"kernel": "k2_up_proj", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": (achieved / peaks["hbm_gbs"]) if achieved else None,
+                "traffic": traffic, "peak_source": peaks["source"] + " (HBM copy, burst)",
+                "algorithmic_bytes": dom_bytes}
+
+    # end to end: host inputs -> device, call, results -> host, every step
+    e2e = _e2e(call, cfg, stream, dev, K, flush_l2)
+
+    # whole-call roofline (bytes / measured HBM)
+    sbytes = step_bytes(s)
+    step_roof = {"bytes": sbytes, "achieved_gbs": sbytes / (ms_per_step / 1e3) / 1e9,
+                 "frac_of_measured_hbm": sbytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+                 "frac_of_nominal_8tbs": sbytes / (ms_per_step / 1e3) / 1e9 / 8000.0}
+
+    prefill = None
+    if not args.skip_prefill:
+        prefill = _prefill(dev, stream, flush_l2, peaks, max(3, min(K, 10)))
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        cpu = cpu_baseline(cfg, inp, budget_s=args.cpu_budget)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_call": ms_per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded, DeepSeek-V3-shaped random weights)",
+            "config": {"workload": cfg.workload, "T": s.T, "He": s.He, "Hcq": s.Hcq, "N": s.N, "D": s.D,
+                       "Dr": s.Dr, "Hckv": s.Hckv, "kv_cache": f"{s.block_num}x{s.block_size}",
+                       "global_batch": s.T * world, "parallelism": f"replicas x{world}",
+                       "l2": "flushed before every step (2 x L2 bytes rewritten, outside the timed events)",
+                       "timing": "CUDA events around each mla_prolog call on its stream"},
+            "roofline": roofline, "step_roofline": step_roof, "kernels_ms": kern_ms,
+            "gpu_launches": kernels_per_step * K,
+            "clocks": clk.summary(), "e2e": e2e, "wall_s_timed": t_wall,
+            "cpu_baseline": cpu, "prefill": prefill,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _read_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, when one exists for this kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return j.get(workload, {}).get(kernel)
+    except Exception:
+        return None
+
+
+def _e2e(call, cfg, stream, dev, K, flush_l2):
+    import torch
+    s = cfg.shape
+    host_in = {k: call.t[k].cpu().pin_memory() for k in ("x", "rope_sin", "rope_cos", "cache_index")}
+    host_out = {k: torch.empty(call.t[k].shape, dtype=call.t[k].dtype, pin_memory=True) for k in ("q_out", "q_rope_out")}
+    bi = sum(v.numel() * v.element_size() for v in host_in.values())
+    bo = sum(v.numel() * v.element_size() for v in host_out.values())
+    for _ in range(3):
+        for k, v in host_in.items():
+            call.t[k].copy_(v, non_blocking=True)
+        call(stream)
+        for k, v in host_out.items():
+            v.copy_(call.t[k], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush_l2()
+        starts[i].record(stream)
+        for k, v in host_in.items():
+            call.t[k].copy_(v, non_blocking=True)
+        call(stream)
+        for k, v in host_out.items():
+            v.copy_(call.t[k], non_blocking=True)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / K
+    return {"value": s.T / (ms / 1e3), "unit": "tokens/s", "us_per_call": ms * 1e3,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "path": "pinned host -> device copies, mla_prolog (C ABI), device -> pinned host copies"}
+
+
+def _prefill(dev, stream, flush_l2, peaks, K):
+    """T = 8192 prefill, reported beside the headline (tensor-core bound)."""
+    import torch
+    from attention_pre_processing_gb300 import workloads, mla_prolog_timing_enable, mla_prolog_timing_read
+    from attention_pre_processing_gb300.runner import PrologCall
+    cfg = workloads.config(PREFILL)
+    s = cfg.shape
+    inp = workloads.make_inputs(cfg)
+    call = PrologCall(cfg, inp, device=dev)
+    for _ in range(3):
+        call(stream)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush_l2()
+        starts[i].record(stream)
+        call(stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / K
+    mla_prolog_timing_enable(True)
+    per = {}
+    for _ in range(K):
+        flush_l2()
+        call(stream)
+        for name, t in mla_prolog_timing_read():
+            per.setdefault(name, []).append(t)
+    mla_prolog_timing_enable(False)
+    kern = {k: statistics.mean(v) for k, v in per.items()}
+    flops = workloads.flops_per_token(s) * s.T
+    k2 = kern.get("k2_up_proj")
+    k2_tf = k2_flops(s) / (k2 / 1e3) / 1e12 if k2 else None
+    ok = call.status(stream) == 0
+    del call
+    torch.cuda.empty_cache()
+    return {"workload": cfg.workload, "us_per_call": ms * 1e3, "tokens_per_s": s.T / (ms / 1e3),
+            "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+            "roofline_k2": {"bound": "tensor", "achieved": k2_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": (k2_tf / peaks["bf16_tflops"]) if k2_tf else None},
+            "kernels_ms": kern, "status_clean": ok}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def cpu_baseline(cfg, inp, budget_s=12.0, steps=None):
+    """Times the oracle on growing token samples until ~budget_s of CPU work."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from attention_pre_processing_gb300 import workloads
+
+    class Dims:
+        pass
+
+    d = Dims()
+    for k in ("T", "He", "Hcq", "N", "D", "Dr", "Hckv", "block_num", "block_size"):
+        setattr(d, k, getattr(cfg.shape, k))
+    oracle.build()
+    threads = oracle.max_threads()
+    done, elapsed, n = 0, 0.0, max(1, threads)
+    while elapsed < budget_s and done < cfg.shape.T * 8:
+        tok = (workloads.sample_tokens(cfg.shape.T, n, seed=done + 1) if n < cfg.shape.T
+               else list(range(cfg.shape.T)))
+        t0 = time.perf_counter()
+        oracle.prolog(inp, dims=d, eps_cq=cfg.eps_cq, eps_ckv=cfg.eps_ckv, x_int8=cfg.x_int8,
+                      kv_int8=cfg.kv_int8, q_int8=cfg.q_int8, tokens=tok, with_intermediates=False)
+        elapsed += time.perf_counter() - t0
+        done += len(tok)
+        n = min(n * 2, cfg.shape.T)
+    return {"value": done / elapsed, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} tokens of {cfg.workload} in {elapsed:.1f} s (fp64 C, OpenMP over tokens)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from attention_pre_processing_gb300 import workloads
+    cfg = workloads.config(HEADLINE)
+    inp = workloads.make_inputs(cfg)
+    budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(cfg, inp, budget_s=0.5)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(cfg, inp, budget_s=budget))
+    wall = time.perf_counter() - t0
+    tok = sum(float(v["sample"].split()[0]) for v in vals)
+    value = tok / sum(float(v["sample"].split(" in ")[1].split()[0]) for v in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, DeepSeek-V3-shaped random weights)",
+            "config": {"workload": cfg.workload, "T": cfg.shape.T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": vals[0]["cores"], "kind": "oracle",
+                             "sample": f"{int(tok)} tokens over {args.steps} steps"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_cuda(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -32,7 +32,8 @@ def oracle_for(cfg, inp, tokens=None, num_threads=0, with_intermediates=True):
     """Run the oracle on a workload config's inputs."""
     import oracle
     return oracle.prolog(inp, dims=_Dims(cfg.shape), eps_cq=cfg.eps_cq, eps_ckv=cfg.eps_ckv,
-                         x_int8=cfg.x_int8, kv_int8=cfg.kv_int8, q_int8=cfg.q_int8,
+                         x_int8=cfg.x_int8, uqqr_int8=cfg.x_int8 or cfg.uqqr_int8, kv_int8=cfg.kv_int8,
+                         kr_int8=cfg.kr_int8, q_int8=cfg.q_int8,
                          tokens=tokens, num_threads=num_threads, with_intermediates=with_intermediates)
 
 

@@ -1,0 +1,160 @@
+"""Host-side checks of the C ABI library: it loads, exports every entry point the header
+declares, and validates arguments with the pages' return codes before touching the GPU.
+No GPU needed: the pointers below are never dereferenced on the host, and every case is
+rejected before the first CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_pre_processing_gb300 as mla
+from attention_pre_processing_gb300 import build as _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return mla.lib()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^MLA_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)
+    return names
+
+
+def test_exports_every_declared_entry_point(lib):
+    names = declared_functions()
+    assert {"mla_prolog_workspace_size", "mla_prolog", "mla_prolog_device_status"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert mla.mla_prolog_status_string(0) == "MLA_OK"
+    assert "161001" in mla.mla_prolog_status_string(161001)
+    assert "561002" in mla.mla_prolog_status_string(561002)
+
+
+# ---------------------------------------------------------- descriptors
+
+BF16, I8, F32, I64 = 0, 1, 2, 3
+_addr = [0x100000]
+
+
+def T(dtype, *shape):
+    d = mla.MlaTensor()
+    _addr[0] += 0x1000
+    d.data = _addr[0]
+    d.dtype = dtype
+    d.ndim = len(shape)
+    for i, s in enumerate(shape):
+        d.shape[i] = s
+    return d
+
+
+def dsv3(Tk=32, **kw):
+    He, Hcq, N, D, Dr, Hckv = 7168, 1536, 128, 128, 64, 512
+    t = dict(x=T(BF16, Tk, He), w_dq=T(BF16, He, Hcq), w_uqqr=T(BF16, Hcq, N * (D + Dr)), w_uk=T(BF16, N, D, Hckv),
+             w_dkvkr=T(BF16, He, Hckv + Dr), gamma_cq=T(BF16, Hcq), gamma_ckv=T(BF16, Hckv),
+             rope_sin=T(BF16, Tk, Dr), rope_cos=T(BF16, Tk, Dr), cache_index=T(I64, Tk),
+             kv_cache=T(BF16, 16, 128, 1, Hckv), kr_cache=T(BF16, 16, 128, 1, Dr),
+             q_out=T(BF16, Tk, N, Hckv), q_rope_out=T(BF16, Tk, N, Dr))
+    t.update(kw)
+    return t
+
+
+def ws_code(tensors, eps=1e-5, mode="PA_BSND"):
+    try:
+        mla.mla_prolog_workspace_size(tensors, eps, eps, mode)
+        return 0
+    except mla.MlaError as e:
+        return e.code
+
+
+def test_valid_arguments_pass_validation(lib):
+    # Valid: validation passes and the library then asks the CUDA runtime for the device
+    # (MLA_OK on a GPU machine, MLA_ERR_RUNTIME where there is no GPU).
+    assert ws_code(dsv3()) in (0, 361001)
+    assert ws_code(dsv3(Tk=0, x=T(BF16, 0, 7168), rope_sin=T(BF16, 0, 64), rope_cos=T(BF16, 0, 64),
+                        cache_index=T(I64, 0), q_out=T(BF16, 0, 128, 512), q_rope_out=T(BF16, 0, 128, 64))) == 0
+
+
+def test_null_required_tensor(lib):
+    t = dsv3()
+    t["w_uk"] = None
+    assert ws_code(t) == 161001
+    t = dsv3()
+    t["x"].data = None
+    assert ws_code(t) == 161001
+
+
+def test_bad_shapes_and_dtypes(lib):
+    assert ws_code(dsv3(w_dkvkr=T(BF16, 7168, 512))) == 161002                 # missing the rope columns
+    assert ws_code(dsv3(cache_index=T(F32, 32))) == 161002                    # cacheIndex must be int64
+    assert ws_code(dsv3(kv_cache=T(BF16, 16, 128, 2, 512))) == 161002         # Nkv must be 1
+    assert ws_code(dsv3(q_rope_out=T(BF16, 32, 128, 32))) == 161002
+    assert ws_code(dsv3(gamma_cq=T(F32, 1536))) == 161002
+    assert ws_code(dsv3(), mode="PA_NZ") == 161002                            # only PA_BSND is built
+    assert ws_code(dsv3(), eps=-1.0) == 161002
+
+
+def test_scenario_patterns(lib):
+    # int8 queryOut needs its scale output
+    assert ws_code(dsv3(q_out=T(I8, 32, 128, 512))) == 161001
+    assert ws_code(dsv3(q_out=T(I8, 32, 128, 512), dequant_scale_q_nope_out=T(F32, 32, 128, 1))) in (0, 361001)
+    # non-quantised scenario takes no scales
+    assert ws_code(dsv3(quant_scale_ckv=T(F32, 1, 512))) == 161002
+    # int8 tokenX needs int8 weights and all four dequant scales
+    full = dict(x=T(I8, 32, 7168), w_dq=T(I8, 7168, 1536), w_uqqr=T(I8, 1536, 24576), w_dkvkr=T(I8, 7168, 576))
+    assert ws_code(dsv3(**full)) == 161001
+    scales = dict(dequant_scale_x=T(F32, 32, 1), dequant_scale_w_dq=T(F32, 1, 1536),
+                  dequant_scale_w_uqqr=T(F32, 1, 24576), dequant_scale_w_dkvkr=T(F32, 1, 576))
+    assert ws_code(dsv3(**full, **scales)) in (0, 361001)
+    assert ws_code(dsv3(**full, **scales, kv_cache=T(I8, 16, 128, 1, 512))) == 161001   # needs quantScaleCkv
+    assert ws_code(dsv3(**full, **scales, kv_cache=T(I8, 16, 128, 1, 512),
+                        quant_scale_ckv=T(F32, 1, 512))) in (0, 361001)
+    # partial quantisation with int8 caches needs both cache scales
+    part = dict(w_uqqr=T(I8, 1536, 24576), dequant_scale_w_uqqr=T(F32, 1, 24576))
+    assert ws_code(dsv3(**part)) in (0, 361001)
+    assert ws_code(dsv3(**part, kv_cache=T(I8, 16, 128, 1, 512), quant_scale_ckv=T(F32, 1, 512))) == 161002
+    assert ws_code(dsv3(**part, kv_cache=T(I8, 16, 128, 1, 512), kr_cache=T(I8, 16, 128, 1, 64),
+                        quant_scale_ckv=T(F32, 1, 512), quant_scale_ckr=T(F32, 1, 64))) in (0, 361001)
+
+
+def test_tiling_rules(lib):
+    He = 7168
+    t = dsv3(w_dq=T(BF16, He, 1500), w_uqqr=T(BF16, 1500, 24576), gamma_cq=T(BF16, 1500))
+    assert ws_code(t) == 561002                                               # Hcq % 64
+    t = dsv3(q_out=T(I8, 32, 128, 1024), dequant_scale_q_nope_out=T(F32, 32, 128, 1),
+             w_uk=T(BF16, 128, 128, 1024), w_dkvkr=T(BF16, He, 1024 + 64), gamma_ckv=T(BF16, 1024),
+             kv_cache=T(BF16, 16, 128, 1, 1024))
+    assert ws_code(t) == 561002                                               # int8 row longer than 512
+
+
+def test_misaligned_pointer(lib):
+    t = dsv3()
+    t["x"].data = t["x"].data + 2
+    assert ws_code(t) == 161002
+
+
+def test_batch_seq_views_accepted(lib):
+    t = dsv3(x=T(BF16, 4, 8, 7168), rope_sin=T(BF16, 4, 8, 64), rope_cos=T(BF16, 4, 8, 64),
+             cache_index=T(I64, 4, 8), q_out=T(BF16, 4, 8, 128, 512), q_rope_out=T(BF16, 4, 8, 128, 64))
+    assert ws_code(t) in (0, 361001)
+
+
+def test_product_has_no_cpu_fallback():
+    """The package never reaches for the oracle: no module of it imports or names it."""
+    pkg = os.path.join(ROOT, "attention_pre_processing_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text and "mla_oracle" not in text, fn
