@@ -1,11 +1,11 @@
 // Row-wise kernels around the GEMMs:
-//   finalize_down: adds the down-projection's fp32 partials, then RmsNorm of c^Q and c^KV,
+//   finalize_down: reads the down-projection's fp32 rows, then RmsNorm of c^Q and c^KV,
 //                  "half" RoPE of k^R, the paged-cache writes of c^KV and k^R, and the bf16
 //                  (or int8-coded) c^Q that feeds the up-projection.
-//   finalize_up:   adds the up-projection's fp32 partials, applies RoPE to each head's rope
+//   finalize_up:   reads the up-projection's fp32 rows, applies RoPE to each head's rope
 //                  columns (q^R) and writes q^C of every head for the W^UK contraction.
 //   convert_i8_to_bf16: exact int8 -> bf16 widening of the int8 operands.
-// One CTA handles one token at a time; every sum runs in a fixed order (deterministic).
+// Every sum runs in a fixed order (deterministic).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -18,69 +18,25 @@ namespace mla {
 
 constexpr int kRowThreads = 256;
 
-// Where the fp32 partial products of a GEMM live, and how to add them up.
+// fp32 product rows written by a GEMM: `slots` k-range slots of T x ncols, row-major, added
+// in slot order.
 struct PartialSrc {
     const float* p;
-    int split;         // 1: stream-K slots (see gemm_tc.cuh); 0: one T x ncols matrix
-    long long total;   // split: n_tiles * kblocks
-    int grid;          // split: CTAs of the GEMM
-    int kblocks;
-    int bn;
-    int T;
     int ncols;
+    int slots;
+    size_t slot_stride;   // T * ncols
 };
 
-// The CTA whose piece holds flattened k-block x.
-__device__ __forceinline__ int piece_owner(long long x, long long total, int G) {
-    long long c = ((x + 1) * G + total - 1) / total - 1;
-    return (int)(c < G - 1 ? c : G - 1);
-}
-
 __device__ __forceinline__ float gather_sum(const PartialSrc& s, int t, int col) {
-    if (!s.split) return s.p[(size_t)t * s.ncols + col];
-    const int tile = col / s.bn;
-    const int cin = col - tile * s.bn;
-    const long long x0 = (long long)tile * s.kblocks;
-    const int c0 = piece_owner(x0, s.total, s.grid);
-    const int c1 = piece_owner(x0 + s.kblocks - 1, s.total, s.grid);
-    float acc = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-        const long long lo = (long long)c * s.total / s.grid;
-        const int part = (lo / s.kblocks == tile) ? 0 : 1;
-        acc += s.p[((size_t)(2 * c + part) * s.T + t) * s.bn + cin];
-    }
-    return acc;
-}
-
-// Deterministic block-wide sum / max (fixed shuffle tree, fixed warp order).
-template <bool kMax>
-__device__ __forceinline__ float block_reduce(float v, float* red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float w = __shfl_xor_sync(0xffffffffu, v, o);
-        v = kMax ? fmaxf(v, w) : v + w;
-    }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float r = kMax ? 0.f : 0.f;
-    if (threadIdx.x < 32) {
-        r = (lane < (int)(blockDim.x >> 5)) ? red[lane] : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float w = __shfl_xor_sync(0xffffffffu, r, o);
-            r = kMax ? fmaxf(r, w) : r + w;
-        }
-        if (lane == 0) red[32] = r;
-    }
-    __syncthreads();
-    return red[32];
+    const float* p = s.p + (size_t)t * s.ncols + col;
+    float v = __ldcg(p);
+    for (int k = 1; k < s.slots; ++k) v += __ldcg(p + k * s.slot_stride);
+    return v;
 }
 
 struct DownArgs {
     int T, Hcq, Hckv, Dr;
-    PartialSrc src;                     // ncols = Hcq + Hckv + Dr
+    PartialSrc src;                     // T x (Hcq + Hckv + Dr)
     const float* scale_x;               // int8 tokenX: (T) per-token dequant, else null
     const float* scale_w_dq;            // (Hcq)
     const float* scale_w_dkvkr;         // (Hckv + Dr)
@@ -104,91 +60,176 @@ struct DownArgs {
     uint32_t* status;
 };
 
-__global__ void __launch_bounds__(kRowThreads) finalize_down_kernel(const DownArgs a) {
-    extern __shared__ float ys[];   // Hcq + Hckv + Dr
-    __shared__ float red[33];
-    pdl_wait();
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Barrier over the threads that share one row: the whole CTA, or the 128 epilogue threads of
+// the fused decode kernel (named barrier 1).
+struct CtaSync {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+struct EpiSync {
+    __device__ __forceinline__ void operator()() const { epi_bar(); }
+};
+
+// Deterministic reduction over NT threads (tid in [0, NT)): fixed shuffle tree per warp, then
+// the per-warp values in warp order.  `red` holds NT/32 + 1 floats.
+template <int NT, bool kMax, class Sync>
+__device__ __forceinline__ float group_reduce(float v, float* red, int tid, Sync sync) {
+    v = kMax ? warp_max(v) : warp_sum(v);
+    const int warp = tid >> 5, lane = tid & 31;
+    sync();
+    if (lane == 0) red[warp] = v;
+    sync();
+    if (warp == 0) {
+        float r = lane < NT / 32 ? red[lane] : 0.f;
+        r = kMax ? warp_max(r) : warp_sum(r);
+        if (lane == 0) red[NT / 32] = r;
+    }
+    sync();
+    return red[NT / 32];
+}
+
+// The row work after the down-projection, for token t, by NT threads (tid in [0, NT)):
+// add the k-range slots of the fp32 row (fixed order), RmsNorm of c^Q and c^KV (epsilon inside
+// the root), "half" RoPE of k^R, the cache writes at cacheIndex[t], and c^Q for the
+// up-projection (bf16, or per-token int8 codes held as bf16 when weightUqQr is int8).
+// ys: Hcq + Hckv + Dr floats of shared memory; red: NT/32 + 1 floats.
+template <int NT, class Sync>
+__device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, float* ys, float* red, Sync sync) {
     const int ncols = a.Hcq + a.Hckv + a.Dr;
     const int h = a.Dr / 2;
-    for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
-        const float sx = a.scale_x ? a.scale_x[t] : 1.f;
-        for (int c = threadIdx.x; c < ncols; c += blockDim.x) {
-            float v = gather_sum(a.src, t, c);
-            if (a.scale_x) v *= sx * (c < a.Hcq ? a.scale_w_dq[c] : a.scale_w_dkvkr[c - a.Hcq]);
-            ys[c] = v;
+    const long long slot = a.nslots > 0 ? a.cache_index[t] : -1;
+    const float* src = a.src.p + (size_t)t * a.src.ncols;
+    const float sx = a.scale_x ? a.scale_x[t] : 1.f;
+    float sq = 0.f, skv = 0.f;
+    // Four columns per thread per round, every slot load of a round in flight together.
+    for (int c0 = tid; c0 < ncols; c0 += 4 * NT) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * NT;
+            v[u] = c < ncols ? __ldcg(src + c) : 0.f;
         }
-        __syncthreads();
-        float sq = 0.f, skv = 0.f;
-        for (int j = threadIdx.x; j < a.Hcq; j += blockDim.x) sq += ys[j] * ys[j];
-        for (int j = threadIdx.x; j < a.Hckv; j += blockDim.x) skv += ys[a.Hcq + j] * ys[a.Hcq + j];
-        sq = block_reduce<false>(sq, red);
-        skv = block_reduce<false>(skv, red);
-        // RmsNorm: gamma * y / sqrt(mean(y^2) + eps), epsilon inside the root.
-        const float inv_q = 1.f / sqrtf(sq / (float)a.Hcq + a.eps_cq);
-        const float inv_kv = 1.f / sqrtf(skv / (float)a.Hckv + a.eps_ckv);
-
-        if (!a.cq_quant) {
-            for (int j = threadIdx.x; j < a.Hcq; j += blockDim.x)
-                a.c_q[(size_t)t * a.Hcq + j] = __float2bfloat16_rn(__bfloat162float(a.gamma_cq[j]) * ys[j] * inv_q);
-        } else {
-            // Per-token dynamic int8 codes of c^Q (times the smooth scales when given).
-            float m = 0.f;
-            for (int j = threadIdx.x; j < a.Hcq; j += blockDim.x) {
-                float u = __bfloat162float(a.gamma_cq[j]) * ys[j] * inv_q;
-                if (a.smooth_cq) u *= a.smooth_cq[j];
-                m = fmaxf(m, fabsf(u));
-            }
-            m = block_reduce<true>(m, red);
-            const float scale = m / 127.f;
-            for (int j = threadIdx.x; j < a.Hcq; j += blockDim.x) {
-                float u = __bfloat162float(a.gamma_cq[j]) * ys[j] * inv_q;
-                if (a.smooth_cq) u *= a.smooth_cq[j];
-                const int q = scale > 0.f ? quant_i8(__fdiv_rn(u, scale)) : 0;
-                a.c_q[(size_t)t * a.Hcq + j] = __int2bfloat16_rn(q);
-            }
-            if (threadIdx.x == 0) a.c_q_scale[t] = scale;
-        }
-
-        if (a.nslots > 0) {
-            const long long slot = a.cache_index[t];
-            if (slot < 0 || slot >= a.nslots) {
-                if (threadIdx.x == 0) atomicOr(a.status, kStatusCacheIndexRange);
-            } else {
-                for (int j = threadIdx.x; j < a.Hckv; j += blockDim.x) {
-                    const float v = __bfloat162float(a.gamma_ckv[j]) * ys[a.Hcq + j] * inv_kv;
-                    if (a.kv_int8)
-                        reinterpret_cast<int8_t*>(a.kv_cache)[slot * a.Hckv + j] =
-                            (int8_t)quant_i8(v * a.quant_scale_ckv[j]);
-                    else
-                        reinterpret_cast<__nv_bfloat16*>(a.kv_cache)[slot * a.Hckv + j] = __float2bfloat16_rn(v);
+        for (int k0 = 1; k0 < a.src.slots; k0 += 4) {
+            float w[4][4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + u * NT;
+                    w[k][u] = (k0 + k < a.src.slots && c < ncols) ? __ldcg(src + (k0 + k) * a.src.slot_stride + c) : 0.f;
                 }
-                const float* kr = ys + a.Hcq + a.Hckv;
-                const __nv_bfloat16* cs = a.rope_cos + (size_t)t * a.Dr;
-                const __nv_bfloat16* sn = a.rope_sin + (size_t)t * a.Dr;
-                for (int j = threadIdx.x; j < h; j += blockDim.x) {
-                    const float x0 = kr[j], x1 = kr[j + h];
-                    const float o0 = x0 * __bfloat162float(cs[j]) - x1 * __bfloat162float(sn[j]);
-                    const float o1 = x1 * __bfloat162float(cs[j + h]) + x0 * __bfloat162float(sn[j + h]);
-                    if (a.kr_int8) {
-                        int8_t* d = reinterpret_cast<int8_t*>(a.kr_cache) + slot * a.Dr;
-                        d[j] = (int8_t)quant_i8(o0 * a.quant_scale_ckr[j]);
-                        d[j + h] = (int8_t)quant_i8(o1 * a.quant_scale_ckr[j + h]);
-                    } else {
-                        __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(a.kr_cache) + slot * a.Dr;
-                        d[j] = __float2bfloat16_rn(o0);
-                        d[j + h] = __float2bfloat16_rn(o1);
-                    }
-                }
-            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] += w[k][u];
         }
-        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * NT;
+            if (c >= ncols) continue;
+            float y = v[u];
+            if (a.scale_x) y *= sx * (c < a.Hcq ? a.scale_w_dq[c] : a.scale_w_dkvkr[c - a.Hcq]);
+            ys[c] = y;
+            if (c < a.Hcq) sq += y * y;
+            else if (c < a.Hcq + a.Hckv) skv += y * y;
+        }
     }
+    sq = group_reduce<NT, false>(sq, red, tid, sync);
+    skv = group_reduce<NT, false>(skv, red, tid, sync);   // its barriers also publish ys
+    // RmsNorm: gamma * y / sqrt(mean(y^2) + eps), epsilon inside the root.
+    const float inv_q = 1.f / sqrtf(sq / (float)a.Hcq + a.eps_cq);
+    const float inv_kv = 1.f / sqrtf(skv / (float)a.Hckv + a.eps_ckv);
+
+    __nv_bfloat16* cq = a.c_q + (size_t)t * a.Hcq;
+    if (!a.cq_quant) {
+        for (int j = 2 * tid; j < a.Hcq; j += 2 * NT) {
+            const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(a.gamma_cq + j);
+            *reinterpret_cast<__nv_bfloat162*>(cq + j) =
+                __floats2bfloat162_rn(__low2float(g2) * ys[j] * inv_q, __high2float(g2) * ys[j + 1] * inv_q);
+        }
+    } else {
+        // Per-token dynamic int8 codes of c^Q (times the smooth scales when given).
+        float m = 0.f;
+        for (int j = tid; j < a.Hcq; j += NT) {
+            float u = __bfloat162float(a.gamma_cq[j]) * ys[j] * inv_q;
+            if (a.smooth_cq) u *= a.smooth_cq[j];
+            m = fmaxf(m, fabsf(u));
+        }
+        m = group_reduce<NT, true>(m, red, tid, sync);
+        const float scale = m / 127.f;
+        for (int j = tid; j < a.Hcq; j += NT) {
+            float u = __bfloat162float(a.gamma_cq[j]) * ys[j] * inv_q;
+            if (a.smooth_cq) u *= a.smooth_cq[j];
+            const int q = scale > 0.f ? quant_i8(__fdiv_rn(u, scale)) : 0;
+            cq[j] = __int2bfloat16_rn(q);
+        }
+        if (tid == 0) a.c_q_scale[t] = scale;
+    }
+
+    if (a.nslots > 0) {
+        if (slot < 0 || slot >= a.nslots) {
+            if (tid == 0) atomicOr(a.status, kStatusCacheIndexRange);
+        } else {
+            const float* ykv = ys + a.Hcq;
+            if (a.kv_int8) {
+                int8_t* d = reinterpret_cast<int8_t*>(a.kv_cache) + slot * a.Hckv;
+                for (int j = tid; j < a.Hckv; j += NT)
+                    d[j] = (int8_t)quant_i8(__bfloat162float(a.gamma_ckv[j]) * ykv[j] * inv_kv * a.quant_scale_ckv[j]);
+            } else {
+                __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(a.kv_cache) + slot * a.Hckv;
+                for (int j = 2 * tid; j < a.Hckv; j += 2 * NT) {
+                    const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(a.gamma_ckv + j);
+                    *reinterpret_cast<__nv_bfloat162*>(d + j) =
+                        __floats2bfloat162_rn(__low2float(g2) * ykv[j] * inv_kv, __high2float(g2) * ykv[j + 1] * inv_kv);
+                }
+            }
+            const float* kr = ys + a.Hcq + a.Hckv;
+            const __nv_bfloat16* cs = a.rope_cos + (size_t)t * a.Dr;
+            const __nv_bfloat16* sn = a.rope_sin + (size_t)t * a.Dr;
+            for (int j = tid; j < h; j += NT) {
+                const float x0 = kr[j], x1 = kr[j + h];
+                const float o0 = x0 * __bfloat162float(cs[j]) - x1 * __bfloat162float(sn[j]);
+                const float o1 = x1 * __bfloat162float(cs[j + h]) + x0 * __bfloat162float(sn[j + h]);
+                if (a.kr_int8) {
+                    int8_t* d = reinterpret_cast<int8_t*>(a.kr_cache) + slot * a.Dr;
+                    d[j] = (int8_t)quant_i8(o0 * a.quant_scale_ckr[j]);
+                    d[j + h] = (int8_t)quant_i8(o1 * a.quant_scale_ckr[j + h]);
+                } else {
+                    __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(a.kr_cache) + slot * a.Dr;
+                    d[j] = __float2bfloat16_rn(o0);
+                    d[j + h] = __float2bfloat16_rn(o1);
+                }
+            }
+        }
+    }
+    sync();   // ys and red are reused by the next row
+}
+
+// One CTA per token (grid-stride).
+__global__ void __launch_bounds__(kRowThreads) finalize_down_kernel(const DownArgs a) {
+    extern __shared__ float ys[];   // Hcq + Hckv + Dr
+    __shared__ float red[kRowThreads / 32 + 1];
+    // All CTAs of this grid are resident once every one has passed here: the next kernel may
+    // start its prologue (and its first weight loads) now.
     pdl_launch_dependents();
+    pdl_wait();
+    for (int t = blockIdx.x; t < a.T; t += gridDim.x)
+        down_row<kRowThreads>(a, t, threadIdx.x, ys, red, CtaSync{});
 }
 
 struct UpArgs {
     int T, N, D, Dr;
-    PartialSrc src;                     // ncols = N * (D + Dr)
+    PartialSrc src;                     // T x N * (D + Dr)
     const float* row_scale;             // (T) dequant of int8 c^Q codes, or null
     const float* col_scale;             // (N*(D+Dr)) dequant of int8 weightUqQr, or null
     const __nv_bfloat16* rope_cos;
@@ -198,6 +239,7 @@ struct UpArgs {
 };
 
 __global__ void __launch_bounds__(kRowThreads) finalize_up_kernel(const UpArgs a) {
+    pdl_launch_dependents();
     pdl_wait();
     const int h = a.Dr / 2;
     const int per_head = a.D + h;       // work items per head: D nope columns + Dr/2 rope pairs
@@ -230,12 +272,12 @@ __global__ void __launch_bounds__(kRowThreads) finalize_up_kernel(const UpArgs a
             }
         }
     }
-    pdl_launch_dependents();
 }
 
 // Exact int8 -> bf16 widening (|v| <= 128 has at most 8 significant bits).
 __global__ void __launch_bounds__(256) convert_i8_to_bf16_kernel(const int8_t* __restrict__ src,
                                                                  __nv_bfloat16* __restrict__ dst, long long n) {
+    pdl_launch_dependents();
     pdl_wait();
     const long long n16 = n / 16;
     const long long stride = (long long)gridDim.x * blockDim.x;
@@ -258,7 +300,6 @@ __global__ void __launch_bounds__(256) convert_i8_to_bf16_kernel(const int8_t* _
     }
     for (long long i = n16 * 16 + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
         dst[i] = __int2bfloat16_rn((int)src[i]);
-    pdl_launch_dependents();
 }
 
 }  // namespace mla

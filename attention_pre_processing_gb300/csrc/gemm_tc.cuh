@@ -2,21 +2,24 @@
 //
 //   D[rows, cols] = A[rows, K] . B[K, cols]
 //   A: activations, K-major bf16 (x, c^Q, or q^C of one head), fetched by TMA, 128-byte swizzle.
+//      The A box has a_box_rows rows (T rounded up to 8 when T <= 128): rows past it in the
+//      128-row MMA operand hold stale shared memory and only feed accumulator rows >= T,
+//      which are never stored.
 //   B: weights in their (k, n) orientation (n contiguous), i.e. MN-major, fetched by TMA in
 //      64-column boxes, 128-byte swizzle.
 //   D: fp32 in tensor memory; MSUB sub-tiles of 128 rows, BN columns each.
 //
-// Roles (192 threads): warp 0 issues TMA loads into a STAGES-deep shared-memory ring, warp 1
-// allocates tensor memory and issues tcgen05.mma, warps 2..5 drain the accumulator through
+// Roles (192 threads): warp 0 issues TMA loads into a `stages`-deep shared-memory ring, warp 1
+// allocates tensor memory and issues tcgen05.mma, warps 2..5 drain the accumulator with
 // tcgen05.ld and run the epilogue.  Every wait is bounded (kWaitLimitNs); a wait that gives up
 // raises MLA_DEV_WAIT_TIMEOUT, the other roles stop at their next wait, tensor memory is freed
 // and the kernel returns.
 //
-// Work: "tile" mode walks whole (row tile, column tile) pairs with the full K range.  "split"
-// mode (few rows: decode) cuts the flattened (column tile, k-block) range into one contiguous
-// piece per CTA, so that every SM streams the same number of weight bytes; a CTA's piece covers
-// at most two column tiles and each part is written as an fp32 partial slot (2*cta + part).
-// The finalize kernels add the slots of a tile in fixed CTA order (deterministic).
+// Work: units are (row tile, column tile, k range).  With ksplit = S > 1 (decode-sized T) the
+// K dimension is cut into S equal ranges and each unit's fp32 product goes to its own slot of a
+// S x T x ncols buffer, which the row-wise finalize kernel adds in fixed order (deterministic).
+// All CTAs start together and walk K in the same order, so CTAs of one k range read the same
+// weight rows at the same time (DRAM page locality).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -29,6 +32,7 @@ namespace mla {
 constexpr int kBK = 64;          // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kGemmThreads = 192;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr size_t kSmemLimit = 232448;             // 227 KB opt-in per CTA
 
 constexpr uint32_t kStatusCacheIndexRange = 0x1u;
 constexpr uint32_t kStatusWaitTimeout = 0x2u;
@@ -40,15 +44,16 @@ struct GemmArgs {
     int kblocks;         // ceil(K / 64)
     int ncols;           // valid product columns (EPI_QN: Hckv of one head)
     int n_tiles;         // column tiles (EPI_QN: N * tiles_per_head)
-    int m_tiles;         // row tiles of MSUB*128 rows (tile mode)
-    int split;           // 1: stream-K pieces with fp32 partial slots
-    long long total;     // split: n_tiles * kblocks
+    int m_tiles;         // row tiles of MSUB*128 rows
+    int ksplit;          // k ranges (EPI_F32 only): unit products go to slot k_range
     int b_split_col;     // B columns below this come from map b0, the rest from b1
     int head_mode;       // A and B are per-head 3D maps (W^UK contraction)
     int tiles_per_head;  // EPI_QN
     int clear_status;    // block 0 zeroes *status once earlier grids have finished
-    // EPI_F32
-    float* out_f32;      // split: slots of T x BN; tile: T x ncols
+    int a_box_rows;      // rows of one A TMA box (multiple of 8, <= 128)
+    int stages;          // ring depth actually used (<= MAXST)
+    // EPI_F32: ksplit slots of T x ncols row-major fp32
+    float* out_f32;
     // EPI_QROPE (one head of D=128 nope + Dr=64 rope columns per tile)
     int N;
     __nv_bfloat16* q_c;            // (T, N, 128)
@@ -65,62 +70,51 @@ struct GemmArgs {
     uint32_t* status;
 };
 
-template <int BN, int MSUB, int STAGES>
+template <int BN, int MSUB, int MAXST>
 struct GemmCfg {
-    static constexpr int kASub = 128 * kBK * 2;             // one 128-row A sub-tile: 16 KB
-    static constexpr int kAStage = MSUB * kASub;
     static constexpr int kBStage = BN * kBK * 2;            // BN/64 boxes of 64 x 64
-    static constexpr int kStageBytes = kAStage + kBStage;
     static constexpr int kAcc = MSUB * BN;                  // TMEM columns per accumulator set
     static constexpr int kNBuf = (2 * kAcc <= 512) ? 2 : 1;
     static constexpr int kTmemCols = (kNBuf * kAcc <= 32) ? 32 : (kNBuf * kAcc <= 64) ? 64
                                      : (kNBuf * kAcc <= 128) ? 128 : (kNBuf * kAcc <= 256) ? 256 : 512;
     static constexpr int kNParts = BN > 256 ? 2 : 1;        // MMA N <= 256
     static constexpr int kMmaN = BN / kNParts;
-    static constexpr int kBarBytes = 8 * (2 * STAGES + 2 * 2 + 1) + 16;
-    static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStageBytes + kBarBytes;
+    static constexpr int kBarBytes = 1024;                  // mbarriers + flags, first in smem
+    static_assert(8 * (2 * MAXST + 5) + 16 <= kBarBytes, "barrier area");
     static_assert(BN % 64 == 0, "BN must be a multiple of 64");
     static_assert(kMmaN % 16 == 0 && kMmaN <= 256, "bad MMA N");
     static_assert(kAcc <= 512, "accumulator exceeds TMEM");
+
+    static __host__ __device__ int a_stage_bytes(int a_box_rows) { return MSUB * a_box_rows * 128; }
+    static __host__ __device__ int stage_bytes(int a_box_rows) { return a_stage_bytes(a_box_rows) + kBStage; }
+    // A region first: a 128-row MMA operand read from the last A stage with a short box runs
+    // at most 16 KB past it, into the B ring (>= 2 stages of >= 8 KB), inside the block.
+    static __host__ __device__ size_t smem_bytes(int stages, int a_box_rows) {
+        return 1024 + kBarBytes + (size_t)stages * stage_bytes(a_box_rows);
+    }
+    static __host__ int max_stages(int a_box_rows) {
+        int s = (int)((kSmemLimit - 1024 - kBarBytes) / stage_bytes(a_box_rows));
+        return s < MAXST ? s : MAXST;
+    }
+    static_assert(2 * kBStage >= 16384, "B ring must cover the A over-read");
 };
 
 struct Unit {
-    int m_tile, n_tile, kb0, kb1, slot;
+    int m_tile, n_tile, kb0, kb1, ks;
 };
 
-// The idx-th unit of work of this CTA.
+// The idx-th unit of work of this CTA: k range slowest, row tile fastest (neighbouring CTAs
+// share a weight tile; CTAs of one k range stream the same weight rows).
 __device__ __forceinline__ bool get_unit(const GemmArgs& a, int idx, Unit& u) {
-    if (a.split) {
-        const long long G = gridDim.x;
-        const long long lo = (long long)blockIdx.x * a.total / G;
-        const long long hi = ((long long)blockIdx.x + 1) * a.total / G;
-        if (lo >= hi || idx > 1) return false;
-        const int KB = a.kblocks;
-        const int t0 = (int)(lo / KB);
-        if (idx == 0) {
-            u.m_tile = 0;
-            u.n_tile = t0;
-            u.kb0 = (int)(lo - (long long)t0 * KB);
-            long long e = hi - (long long)t0 * KB;
-            u.kb1 = (int)(e < KB ? e : KB);
-            u.slot = 2 * blockIdx.x;
-            return true;
-        }
-        if (hi <= (long long)(t0 + 1) * KB) return false;
-        u.m_tile = 0;
-        u.n_tile = t0 + 1;
-        u.kb0 = 0;
-        u.kb1 = (int)(hi - (long long)(t0 + 1) * KB);
-        u.slot = 2 * blockIdx.x + 1;
-        return true;
-    }
     const long long i = (long long)blockIdx.x + (long long)idx * gridDim.x;
-    if (i >= (long long)a.m_tiles * a.n_tiles) return false;
-    u.m_tile = (int)(i % a.m_tiles);   // row tiles fastest: neighbouring CTAs share a weight tile
-    u.n_tile = (int)(i / a.m_tiles);
-    u.kb0 = 0;
-    u.kb1 = a.kblocks;
-    u.slot = 0;
+    const long long per_k = (long long)a.m_tiles * a.n_tiles;
+    if (i >= per_k * a.ksplit) return false;
+    u.ks = (int)(i / per_k);
+    const long long r = i - (long long)u.ks * per_k;
+    u.m_tile = (int)(r % a.m_tiles);
+    u.n_tile = (int)(r / a.m_tiles);
+    u.kb0 = (int)((long long)u.ks * a.kblocks / a.ksplit);
+    u.kb1 = (int)((long long)(u.ks + 1) * a.kblocks / a.ksplit);
     return true;
 }
 
@@ -141,20 +135,37 @@ __device__ __forceinline__ int quant_i8(float v) {
     return (int)r;
 }
 
-// ------------------------------------------------------------------ epilogues
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// fp32 store of one 32-column chunk of one row.
-__device__ __forceinline__ void store_f32_chunk(float* dst, const uint32_t (&r)[32], int nvalid) {
-    if (nvalid >= 32 && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            reinterpret_cast<uint4*>(dst)[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < nvalid) dst[i] = bits_f(r[i]);
-    }
+// Barrier over the 128 epilogue threads that also ORs a flag: every thread gets the same answer.
+__device__ __forceinline__ bool epi_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
 }
+
+// ----------------------------------------------------------- accumulator sources
+
+// Rows of the accumulator, 32 columns at a time, straight from tensor memory (warp-collective).
+struct TmemSrc {
+    uint32_t tacc;
+    __device__ __forceinline__ void load(int ms, int bn, int col, float (&v)[32]) const {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tacc + ms * bn + col, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = bits_f(r[i]);
+    }
+};
+
+// ------------------------------------------------------------------ epilogues
 
 // bf16 store of one 32-column chunk (64 bytes) of one row.
 __device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16* dst, const float (&v)[32], int nvalid) {
@@ -175,64 +186,62 @@ __device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16* dst, const float
     }
 }
 
-template <int BN, int MSUB>
-__device__ __forceinline__ void epilogue_f32(const GemmArgs& a, const Unit& u, uint32_t tacc, int row_in) {
-    float* base;
-    long long ld;
-    int col_limit;
-    if (a.split) {
-        base = a.out_f32 + (size_t)u.slot * (size_t)a.T * BN;
-        ld = BN;
-        col_limit = BN;
+__device__ __forceinline__ void store_f32_chunk(float* dst, const float (&v)[32], int nvalid) {
+    if (nvalid >= 32 && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     } else {
-        base = a.out_f32 + (size_t)u.n_tile * BN;
-        ld = a.ncols;
-        col_limit = a.ncols - u.n_tile * BN;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nvalid) dst[i] = v[i];
     }
+}
+
+// fp32 rows of the product into slot ks of the ksplit x T x ncols buffer.
+template <int BN, int MSUB, class Src>
+__device__ __forceinline__ void epilogue_f32(const GemmArgs& a, int row0, int n_tile, int ks, const Src& src) {
+    const int col_limit = a.ncols - n_tile * BN;
+    float* out = a.out_f32 + (size_t)ks * a.T * a.ncols;
 #pragma unroll 1
     for (int ms = 0; ms < MSUB; ++ms) {
-        const int row = (u.m_tile * MSUB + ms) * 128 + row_in;
+        const int row = row0 + ms * 128;
 #pragma unroll 1
         for (int ch = 0; ch < BN / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tacc + ms * BN + ch * 32, r);
-            tmem_ld_wait();
-            if (row < a.T && ch * 32 < col_limit)
-                store_f32_chunk(base + (size_t)row * ld + ch * 32, r, col_limit - ch * 32);
+            if (ch * 32 >= col_limit) break;   // uniform across the warp
+            float v[32];
+            src.load(ms, BN, ch * 32, v);
+            if (row < a.T) store_f32_chunk(out + (size_t)row * a.ncols + n_tile * BN + ch * 32, v,
+                                           col_limit - ch * 32);
         }
     }
 }
 
 // One head per tile: columns [0,128) are q^C (nope), [128,192) the rope part of W^QR.
-template <int MSUB>
-__device__ __forceinline__ void epilogue_qrope(const GemmArgs& a, const Unit& u, uint32_t tacc, int row_in) {
+template <int MSUB, class Src>
+__device__ __forceinline__ void epilogue_qrope(const GemmArgs& a, int row0, int head, const Src& src) {
     constexpr int D = 128, DR = 64, H = 32, BN = 192;
-    const int head = u.n_tile;
 #pragma unroll 1
     for (int ms = 0; ms < MSUB; ++ms) {
-        const int row = (u.m_tile * MSUB + ms) * 128 + row_in;
+        const int row = row0 + ms * 128;
         const bool valid = row < a.T;
         const float rs = (valid && a.row_scale) ? a.row_scale[row] : 1.f;
         const float* cs = a.col_scale ? a.col_scale + (size_t)head * BN : nullptr;
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tacc + ms * BN + ch * 32, r);
-            tmem_ld_wait();
+            float v[32];
+            src.load(ms, BN, ch * 32, v);
             if (valid) {
-                float v[32];
+                if (cs) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    v[i] = bits_f(r[i]);
-                    if (cs) v[i] *= rs * cs[ch * 32 + i];
+                    for (int i = 0; i < 32; ++i) v[i] *= rs * cs[ch * 32 + i];
                 }
                 store_bf16_chunk(a.q_c + ((size_t)row * a.N + head) * D + ch * 32, v, 32);
             }
         }
-        uint32_t ra[32], rb[32];
-        tmem_ld_32x32b_x32(tacc + ms * BN + D, ra);
-        tmem_ld_32x32b_x32(tacc + ms * BN + D + H, rb);
-        tmem_ld_wait();
+        float x0[32], x1[32];
+        src.load(ms, BN, D, x0);
+        src.load(ms, BN, D + H, x1);
         if (valid) {
             const uint4* cp = reinterpret_cast<const uint4*>(a.rope_cos + (size_t)row * DR);
             const uint4* sp = reinterpret_cast<const uint4*>(a.rope_sin + (size_t)row * DR);
@@ -249,13 +258,13 @@ __device__ __forceinline__ void epilogue_qrope(const GemmArgs& a, const Unit& u,
                     const float sj = (e & 1) ? bf16_hi(sw0[e >> 1]) : bf16_lo(sw0[e >> 1]);
                     const float ch = (e & 1) ? bf16_hi(cw1[e >> 1]) : bf16_lo(cw1[e >> 1]);
                     const float sh = (e & 1) ? bf16_hi(sw1[e >> 1]) : bf16_lo(sw1[e >> 1]);
-                    float x0 = bits_f(ra[j]), x1 = bits_f(rb[j]);
+                    float a0 = x0[j], a1 = x1[j];
                     if (cs) {
-                        x0 *= rs * cs[D + j];
-                        x1 *= rs * cs[D + H + j];
+                        a0 *= rs * cs[D + j];
+                        a1 *= rs * cs[D + H + j];
                     }
-                    o0[j] = x0 * cj - x1 * sj;
-                    o1[j] = x1 * ch + x0 * sh;
+                    o0[j] = a0 * cj - a1 * sj;
+                    o1[j] = a1 * ch + a0 * sh;
                 }
             }
             __nv_bfloat16* dst = a.q_rope + ((size_t)row * a.N + head) * DR;
@@ -266,7 +275,7 @@ __device__ __forceinline__ void epilogue_qrope(const GemmArgs& a, const Unit& u,
 }
 
 template <int BN>
-__device__ __forceinline__ void epilogue_qn(const GemmArgs& a, const Unit& u, uint32_t tacc, int row_in) {
+__device__ __forceinline__ void epilogue_qn(const GemmArgs& a, const Unit& u, const TmemSrc& src, int row_in) {
     const int head = u.n_tile / a.tiles_per_head;
     const int c0 = (u.n_tile % a.tiles_per_head) * BN;
     const int row = u.m_tile * 128 + row_in;
@@ -277,15 +286,9 @@ __device__ __forceinline__ void epilogue_qn(const GemmArgs& a, const Unit& u, ui
         for (int ch = 0; ch < BN / 32; ++ch) {
             const int col = c0 + ch * 32;
             if (col >= a.Hckv) break;   // uniform across the warp
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tacc + ch * 32, r);
-            tmem_ld_wait();
-            if (valid) {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = bits_f(r[i]);
-                store_bf16_chunk(a.q_out_bf16 + rowoff + col, v, a.Hckv - col);
-            }
+            float v[32];
+            src.load(0, BN, ch * 32, v);
+            if (valid) store_bf16_chunk(a.q_out_bf16 + rowoff + col, v, a.Hckv - col);
         }
         return;
     }
@@ -295,21 +298,19 @@ __device__ __forceinline__ void epilogue_qn(const GemmArgs& a, const Unit& u, ui
     for (int ch = 0; ch < BN / 32; ++ch) {
         const int col = ch * 32;
         if (col >= a.Hckv) break;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tacc + col, r);
-        tmem_ld_wait();
+        float v[32];
+        src.load(0, BN, col, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-            if (col + i < a.Hckv) m = fmaxf(m, fabsf(bits_f(r[i])));
+            if (col + i < a.Hckv) m = fmaxf(m, fabsf(v[i]));
     }
     const float scale = m / 127.f;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
         const int col = ch * 32;
         if (col >= a.Hckv) break;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tacc + col, r);
-        tmem_ld_wait();
+        float v[32];
+        src.load(0, BN, col, v);
         if (valid) {
             uint32_t w[8];
 #pragma unroll
@@ -317,7 +318,7 @@ __device__ __forceinline__ void epilogue_qn(const GemmArgs& a, const Unit& u, ui
                 uint32_t packed = 0;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int q = (scale > 0.f) ? quant_i8(__fdiv_rn(bits_f(r[4 * i + e]), scale)) : 0;
+                    const int q = (scale > 0.f) ? quant_i8(__fdiv_rn(v[4 * i + e], scale)) : 0;
                     packed |= ((uint32_t)(q & 0xFF)) << (8 * e);
                 }
                 w[i] = packed;
@@ -335,25 +336,69 @@ __device__ __forceinline__ void epilogue_qn(const GemmArgs& a, const Unit& u, ui
     if (valid) a.q_scale[(size_t)row * a.N + head] = scale;
 }
 
+// ---------------------------------------------------------------------- loads
+
+// Weight tile of k-block kb: BN/64 boxes of 64 columns x 64 rows.
+template <int BN>
+__device__ __forceinline__ void load_b(const GemmArgs& a, const Unit& u, int kb, uint32_t dst, uint32_t bar,
+                                       const CUtensorMap* b0, const CUtensorMap* b1, uint64_t pol) {
+    int head = 0, c0;
+    if (a.head_mode) {
+        head = u.n_tile / a.tiles_per_head;
+        c0 = (u.n_tile % a.tiles_per_head) * BN;
+    } else {
+        c0 = u.n_tile * BN;
+    }
+#pragma unroll
+    for (int j = 0; j < BN / 64; ++j) {
+        const int col = c0 + 64 * j;
+        const uint32_t d = dst + j * (64 * kBK * 2);
+        if (a.head_mode)
+            tma_load_3d(d, b0, bar, col, kb * kBK, head, pol);
+        else if (col < a.b_split_col)
+            tma_load_2d(d, b0, bar, col, kb * kBK, pol);
+        else
+            tma_load_2d(d, b1, bar, col - a.b_split_col, kb * kBK, pol);
+    }
+}
+
+// Activation tile of k-block kb: MSUB boxes of a_box_rows rows x 64 columns.
+template <int MSUB>
+__device__ __forceinline__ void load_a(const GemmArgs& a, const Unit& u, int kb, uint32_t dst, int a_box,
+                                       uint32_t bar, const CUtensorMap* map, uint64_t pol) {
+    const int head = a.head_mode ? u.n_tile / a.tiles_per_head : 0;
+#pragma unroll
+    for (int ms = 0; ms < MSUB; ++ms) {
+        const int r0 = (u.m_tile * MSUB + ms) * 128;
+        if (a.head_mode)
+            tma_load_3d(dst + ms * a_box, map, bar, kb * kBK, head, r0, pol);
+        else
+            tma_load_2d(dst + ms * a_box, map, bar, kb * kBK, r0, pol);
+    }
+}
+
 // ---------------------------------------------------------------------- kernel
 
-template <int BN, int MSUB, int STAGES, int EPI>
+template <int BN, int MSUB, int MAXST, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                    const __grid_constant__ CUtensorMap map_b1, const GemmArgs args) {
-    using C = GemmCfg<BN, MSUB, STAGES>;
+    using C = GemmCfg<BN, MSUB, MAXST>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + (size_t)STAGES * C::kAStage;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * C::kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     uint64_t* full = bars;
-    uint64_t* empty = bars + STAGES;
-    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* empty = bars + MAXST;
+    uint64_t* tfull = bars + 2 * MAXST;
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tempty + 2;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    const int stages = args.stages;
+    const int a_stage = C::a_stage_bytes(args.a_box_rows);
+    const int a_box = args.a_box_rows * 128;
+    uint8_t* sA = smem + C::kBarBytes;
+    uint8_t* sB = sA + (size_t)stages * a_stage;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -362,7 +407,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b0);
         tma_prefetch_map(&map_b1);
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
@@ -383,55 +428,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
 
-    // Everything above overlaps the previous grid; inputs are read only after it completes.
-    pdl_wait();
-    if (args.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *args.status = 0u;
+    // Everything above overlaps the previous grid.  Once every CTA of this grid is resident the
+    // next kernel may start its own prologue on free SMs.
+    pdl_launch_dependents();
+    if (warp != 0) pdl_wait();   // the producer waits inside its role, after the first weight loads
+    if (args.clear_status && blockIdx.x == 0 && threadIdx.x == 64) *args.status = 0u;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_a = policy_evict_last();
-            uint32_t it = 0;
+            int s = 0;
+            uint32_t ph = 0;
             Unit u;
             bool ok = true;
-            for (int idx = 0; ok && get_unit(args, idx, u); ++idx) {
-                int head = 0, c0 = 0;
-                if (args.head_mode) {
-                    head = u.n_tile / args.tiles_per_head;
-                    c0 = (u.n_tile % args.tiles_per_head) * BN;
-                } else {
-                    c0 = u.n_tile * BN;
+            // Weights do not depend on the previous kernel: the first ring of weight tiles is
+            // requested before waiting for it; activation tiles follow once it has finished.
+            int pre = 0;
+            Unit u0;
+            const bool have0 = get_unit(args, 0, u0);
+            if (have0) {
+                const int n0 = u0.kb1 - u0.kb0;
+                pre = n0 < stages ? n0 : stages;
+                for (int i = 0; i < pre; ++i) {
+                    const uint32_t fb = smem_u32(&full[i]);
+                    mbar_arrive_expect_tx(fb, (uint32_t)(a_stage + C::kBStage));
+                    load_b<BN>(args, u0, u0.kb0 + i, smem_u32(sB + (size_t)i * C::kBStage), fb, &map_b0, &map_b1,
+                               pol_w);
                 }
-                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i)
+                load_a<MSUB>(args, u0, u0.kb0 + i, smem_u32(sA + (size_t)i * a_stage), a_box,
+                             smem_u32(&full[i]), &map_a, pol_a);
+            s = pre % stages;
+            ph = (pre == stages) ? 1u : 0u;
+            for (int idx = 0; ok && get_unit(args, idx, u); ++idx) {
+                for (int kb = u.kb0 + (idx == 0 ? pre : 0); kb < u.kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, s_abort, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = smem_u32(&full[s]);
-                    mbar_arrive_expect_tx(fb, C::kStageBytes);
-                    const uint32_t a_dst = smem_u32(sA + (size_t)s * C::kAStage);
-                    const uint32_t b_dst = smem_u32(sB + (size_t)s * C::kBStage);
-#pragma unroll
-                    for (int ms = 0; ms < MSUB; ++ms) {
-                        const int r0 = (u.m_tile * MSUB + ms) * 128;
-                        if (args.head_mode)
-                            tma_load_3d(a_dst + ms * C::kASub, &map_a, fb, kb * kBK, head, r0, pol_a);
-                        else
-                            tma_load_2d(a_dst + ms * C::kASub, &map_a, fb, kb * kBK, r0, pol_a);
-                    }
-#pragma unroll
-                    for (int j = 0; j < BN / 64; ++j) {
-                        const int col = c0 + 64 * j;
-                        const uint32_t dst = b_dst + j * (64 * kBK * 2);
-                        if (args.head_mode)
-                            tma_load_3d(dst, &map_b0, fb, col, kb * kBK, head, pol_w);
-                        else if (col < args.b_split_col)
-                            tma_load_2d(dst, &map_b0, fb, col, kb * kBK, pol_w);
-                        else
-                            tma_load_2d(dst, &map_b1, fb, col - args.b_split_col, kb * kBK, pol_w);
+                    mbar_arrive_expect_tx(fb, (uint32_t)(a_stage + C::kBStage));
+                    load_b<BN>(args, u, kb, smem_u32(sB + (size_t)s * C::kBStage), fb, &map_b0, &map_b1, pol_w);
+                    load_a<MSUB>(args, u, kb, smem_u32(sA + (size_t)s * a_stage), a_box, fb, &map_a, pol_a);
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1;
                     }
                 }
             }
@@ -439,12 +484,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 *s_abort = 1;
                 atomicOr(args.status, kStatusWaitTimeout);
             }
+        } else {
+            pdl_wait();
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, C::kMmaN, false, true);
-            uint32_t it = 0, ai = 0;
+            int s = 0;
+            uint32_t ph = 0, ai = 0;
             Unit u;
             bool ok = true;
             for (int idx = 0; ok && get_unit(args, idx, u); ++idx, ++ai) {
@@ -456,21 +504,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_base = tmem_base + b * C::kAcc;
-                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&full[s]), ph, s_abort, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + (size_t)s * C::kAStage);
+                    const uint32_t a_base = smem_u32(sA + (size_t)s * a_stage);
                     const uint32_t b_base = smem_u32(sB + (size_t)s * C::kBStage);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
 #pragma unroll
                         for (int ms = 0; ms < MSUB; ++ms) {
-                            const uint64_t adesc = smem_desc_sw128(a_base + ms * C::kASub + kk * 32, 16, 1024);
+                            const uint64_t adesc = smem_desc_sw128(a_base + ms * a_box + kk * 32, 16, 1024);
 #pragma unroll
                             for (int np = 0; np < C::kNParts; ++np) {
                                 const uint64_t bdesc = smem_desc_sw128(
@@ -481,6 +527,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
                     }
                     umma_commit(smem_u32(&empty[s]));
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
                 }
                 if (!ok) break;
                 umma_commit(smem_u32(&tfull[b]));
@@ -505,30 +555,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int ok = 1;
             if (lane == 0) ok = mbar_wait(smem_u32(&tfull[b]), aph, s_abort, kWaitLimitNs) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
-                if (lane == 0) {
-                    *s_abort = 1;
-                    atomicOr(args.status, kStatusWaitTimeout);
-                }
-                break;
+            if (!ok && lane == 0) {
+                *s_abort = 1;
+                atomicOr(args.status, kStatusWaitTimeout);
             }
+            // The four epilogue warps stop together or not at all.
+            if (epi_any(!ok)) break;
             __syncwarp();
             tc_fence_after();
-            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + b * C::kAcc;
+            const TmemSrc tsrc{tmem_base + ((uint32_t)(q * 32) << 16) + b * C::kAcc};
+            const int row0 = u.m_tile * MSUB * 128 + row_in;
             if constexpr (EPI == EPI_F32) {
-                epilogue_f32<BN, MSUB>(args, u, tacc, row_in);
+                epilogue_f32<BN, MSUB>(args, row0, u.n_tile, u.ks, tsrc);
             } else if constexpr (EPI == EPI_QROPE) {
-                epilogue_qrope<MSUB>(args, u, tacc, row_in);
+                epilogue_qrope<MSUB>(args, row0, u.n_tile, tsrc);
             } else {
-                epilogue_qn<BN>(args, u, tacc, row_in);
+                epilogue_qn<BN>(args, u, tsrc, row_in);
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[b]));
         }
     }
 
-    // Let the next grid start its prologue while this one tears down.
-    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     if (*s_abort) {

@@ -15,9 +15,12 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
+#include <random>
 
-#include "../../include/mla_prolog.h"
+#include "mla_prolog.h"
+#include "decode_fused.cuh"
 #include "finalize.cuh"
 #include "gemm_tc.cuh"
 
@@ -209,28 +212,34 @@ mla_status validate(const Args& a, Dims& d, Scenario& sc) {
     if (d.He % 8 || d.Hcq % 64 || d.D % 8 || (d.Dr & 1) || W % 8 || (d.Hckv + d.Dr) % 8 || d.Hckv % 8)
         return MLA_ERR_TILING;
     if (sc.q_i8 && d.Hckv > 512) return MLA_ERR_TILING;
+    if ((d.Hcq + d.Hckv + d.Dr) * 4 > 48 * 1024) return MLA_ERR_TILING;   // one fp32 row in shared memory
     if (d.T > (int64_t)INT32_MAX || d.He > (int64_t)INT32_MAX || W > (int64_t)INT32_MAX) return MLA_ERR_TILING;
     return MLA_OK;
 }
 
 // ---------------------------------------------------------------------- plan
 
-constexpr int kBN12 = 192;   // column tile of the two weight-streaming GEMMs (one head of 128+64)
-
+// One GEMM launch: tile shape, work split and grid.
 struct GemmPlan {
-    int split = 0, msub = 1, grid = 0, m_tiles = 1, n_tiles = 0, kblocks = 0, bn = kBN12;
-    long long total = 0;
+    int msub = 1, grid = 0, m_tiles = 1, n_tiles = 0, kblocks = 0, bn = 192, ksplit = 1, a_box_rows = 128;
 };
 
 struct Plan {
     GemmPlan g1, g2, g3;
-    bool g2_fused = false;   // K2 epilogue does RoPE and q^C (no F2)
+    bool fused = false;      // decode-sized: the one persistent kernel of decode_fused.cuh
+    int fused_ra = 0, fused_rb = 0, fused_s1 = 1, fused_nt1 = 0;
+    size_t fused_smem = 0;
+    bool g2_fused = false;   // K2 epilogue does RoPE and q^C (no finalize_up)
     int64_t ncols1 = 0, ncols2 = 0;
-    size_t off_cq = 0, off_cqs = 0, off_qc = 0, off_p1 = 0, off_p2 = 0, off_xb = 0, off_wdq = 0, off_wdkvkr = 0,
-           off_wuqqr = 0, bytes = 0;
+    size_t off_cq = 0, off_cqs = 0, off_qc = 0, off_y1 = 0, off_y2 = 0, off_xb = 0, off_wdq = 0, off_wdkvkr = 0,
+           off_wuqqr = 0, off_flags = 0, bytes = 0;
 };
 
 constexpr size_t kStatusBytes = 1024;
+constexpr int kDecodeRows = 256;   // up to this many tokens: one row tile, weight streaming
+// The single persistent decode kernel is correct but slower than the four-launch path on
+// GB300 (its per-SM weight stream stalls behind MMA issue), so it is built but not planned.
+constexpr bool kFusedDecode = false;
 
 size_t up1024(size_t v) { return (v + 1023) & ~size_t(1023); }
 
@@ -243,22 +252,28 @@ int device_sms(int* out) {
     return 0;
 }
 
-void plan_split_or_tile(GemmPlan& g, int64_t T, int64_t ncols, int64_t K, int sms) {
+// Tiles of bn columns; at decode-sized T one row tile of MSUB*128 rows and, when asked,
+// k ranges so that (tiles x ranges) covers the SMs.
+void plan_gemm(GemmPlan& g, int64_t T, int64_t ncols, int64_t K, int sms, int bn, bool allow_ksplit) {
+    g.bn = bn;
     g.kblocks = (int)((K + kBK - 1) / kBK);
-    g.n_tiles = (int)((ncols + g.bn - 1) / g.bn);
-    if (T <= 256 && g.n_tiles <= sms) {
-        g.split = 1;
+    g.n_tiles = (int)((ncols + bn - 1) / bn);
+    if (T <= kDecodeRows) {
         g.msub = T <= 128 ? 1 : 2;
         g.m_tiles = 1;
-        g.total = (long long)g.n_tiles * g.kblocks;
-        g.grid = (int)(g.total < sms ? g.total : sms);
+        g.a_box_rows = g.msub == 1 ? (int)((T + 7) / 8 * 8) : 128;
+        int S = allow_ksplit ? sms / g.n_tiles : 1;
+        if (S > g.kblocks) S = g.kblocks;
+        if (S > 16) S = 16;
+        g.ksplit = S < 1 ? 1 : S;
     } else {
-        g.split = 0;
         g.msub = 2;
         g.m_tiles = (int)((T + 255) / 256);
-        const long long tiles = (long long)g.m_tiles * g.n_tiles;
-        g.grid = (int)(tiles < sms ? tiles : sms);
+        g.a_box_rows = 128;
+        g.ksplit = 1;
     }
+    const long long units = (long long)g.m_tiles * g.n_tiles * g.ksplit;
+    g.grid = (int)(units < sms ? units : sms);
 }
 
 Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
@@ -266,9 +281,12 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     const int64_t T = d.T;
     p.ncols1 = d.Hcq + d.Hckv + d.Dr;
     p.ncols2 = d.N * (d.D + d.Dr);
-    plan_split_or_tile(p.g1, T, p.ncols1, d.He, sms);
-    plan_split_or_tile(p.g2, T, p.ncols2, d.Hcq, sms);
-    p.g2_fused = !p.g2.split && d.D == 128 && d.Dr == 64;
+    // Down-projection: at decode, 64-column tiles x k ranges; two 128-row sub-tiles or
+    // prefill use 192-column tiles.
+    plan_gemm(p.g1, T, p.ncols1, d.He, sms, T <= 128 ? 64 : 192, true);
+    // Up-projection: one head (192 columns) per tile, full K, fused RoPE epilogue.
+    plan_gemm(p.g2, T, p.ncols2, d.Hcq, sms, 192, false);
+    p.g2_fused = d.D == 128 && d.Dr == 64;
     // K3: per head, 128-row tiles; an int8 output needs the whole Hckv row in one tile.
     p.g3.bn = sc.q_i8 ? 512 : 256;
     p.g3.kblocks = (int)((d.D + kBK - 1) / kBK);
@@ -276,9 +294,36 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     p.g3.n_tiles = (int)(d.N * tph);
     p.g3.m_tiles = (int)((T + 127) / 128);
     p.g3.msub = 1;
+    p.g3.a_box_rows = T < 128 ? (int)((T + 7) / 8 * 8) : 128;
     {
         const long long tiles = (long long)p.g3.m_tiles * p.g3.n_tiles;
         p.g3.grid = (int)(tiles < sms ? tiles : sms);
+    }
+
+    // One persistent kernel for decode-sized T with the 128 + 64 head layout, when every head
+    // and every down-projection tile gets its own CTA.
+    {
+        const int nt1 = (int)((p.ncols1 + 63) / 64);
+        const int a_bytes = (int)((T + 7) / 8 * 8) * 128;
+        int ra = 32768 / a_bytes;
+        ra = ra < 2 ? 2 : (ra > kFusedMaxA ? kFusedMaxA : ra);
+        const size_t fixed = fused_smem_bytes((int)p.ncols1, a_bytes, ra, 0);
+        int rb = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kBox) : 0;
+        if (rb > kFusedMaxB) rb = kFusedMaxB;
+        if (kFusedDecode && T <= 128 && d.D == 128 && d.Dr == 64 && d.Hckv <= 512 && d.Hckv % 64 == 0 && d.N <= sms &&
+            nt1 <= sms && rb >= 8 && d.Hcq % 64 == 0) {
+            p.fused = true;
+            p.fused_nt1 = nt1;
+            int s1 = sms / nt1;
+            const int kb1 = (int)((d.He + 63) / 64);
+            if (s1 > kb1) s1 = kb1;
+            if (s1 > 16) s1 = 16;
+            p.fused_s1 = s1 < 1 ? 1 : s1;
+            p.fused_ra = ra;
+            p.fused_rb = rb;
+            p.fused_smem = fused_smem_bytes((int)p.ncols1, a_bytes, ra, rb);
+            p.g1.ksplit = p.fused_s1;
+        }
     }
 
     size_t off = kStatusBytes;
@@ -290,19 +335,27 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     p.off_cq = take((size_t)T * d.Hcq * 2);
     p.off_cqs = take((size_t)T * 4);
     p.off_qc = take((size_t)T * d.N * d.D * 2);
-    p.off_p1 = take(p.g1.split ? (size_t)2 * p.g1.grid * T * p.g1.bn * 4 : (size_t)T * p.ncols1 * 4);
-    if (p.g2.split)
-        p.off_p2 = take((size_t)2 * p.g2.grid * T * p.g2.bn * 4);
-    else if (!p.g2_fused)
-        p.off_p2 = take((size_t)T * p.ncols2 * 4);
+    p.off_y1 = take((size_t)p.g1.ksplit * T * p.ncols1 * 4);
+    if (!p.g2_fused) p.off_y2 = take((size_t)T * p.ncols2 * 4);
     if (sc.x_i8) {
         p.off_xb = take((size_t)T * d.He * 2);
         p.off_wdq = take((size_t)d.He * d.Hcq * 2);
         p.off_wdkvkr = take((size_t)d.He * (d.Hckv + d.Dr) * 2);
     }
     if (sc.uqqr_i8) p.off_wuqqr = take((size_t)d.Hcq * p.ncols2 * 2);
+    p.off_flags = take((size_t)2 * sms * 8 + (size_t)2 * sms * kDoneStride * 8);
     p.bytes = off;
     return p;
+}
+
+// A unique 48-bit tag per call for the fused kernel's barrier flags.  It starts at a random value
+// so that flags left in a reused workspace never match by accident.
+unsigned long long next_tag() {
+    static std::atomic<unsigned long long> ctr{[] {
+        std::random_device rd;
+        return ((unsigned long long)rd() << 20) ^ (unsigned long long)rd();
+    }()};
+    return (ctr.fetch_add(1) + 1) & 0xFFFFFFFFFFFFull;
 }
 
 // --------------------------------------------------------------- tensor maps
@@ -361,11 +414,20 @@ Timing g_timing;
 std::mutex g_timing_mu;
 
 // Records the event that closes the interval of the kernel just launched.
+// Inside stream capture the record must be "external" to become a graph node.
+void timing_record(cudaEvent_t ev, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, st);
+}
+
 void timing_mark(cudaStream_t st, const char* name) {
     if (!g_timing.enabled || g_timing.n >= 15) return;
     if (!g_timing.ev[g_timing.n + 1] && cudaEventCreate(&g_timing.ev[g_timing.n + 1]) != cudaSuccess) return;
     g_timing.name[g_timing.n] = name;
-    cudaEventRecord(g_timing.ev[g_timing.n + 1], st);
+    timing_record(g_timing.ev[g_timing.n + 1], st);
     ++g_timing.n;
 }
 
@@ -374,13 +436,18 @@ void timing_begin(cudaStream_t st) {
     g_timing.n = 0;
     g_timing.have = false;
     if (!g_timing.ev[0] && cudaEventCreate(&g_timing.ev[0]) != cudaSuccess) return;
-    cudaEventRecord(g_timing.ev[0], st);
+    timing_record(g_timing.ev[0], st);
 }
 
 // --------------------------------------------------------------------- launch
 
 template <typename Kernel, typename... ArgsT>
 cudaError_t launch(Kernel k, int grid, int block, size_t smem, cudaStream_t st, ArgsT... args) {
+    // Every kernel of the prolog runs with the same (maximum) shared-memory carve-out, so the
+    // SMs never re-partition L1 / shared memory between consecutive kernels.
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)block);
@@ -394,15 +461,18 @@ cudaError_t launch(Kernel k, int grid, int block, size_t smem, cudaStream_t st, 
     return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
-template <int BN, int MSUB, int STAGES, int EPI>
+// Launches one GEMM instantiation; fills in the ring depth and dynamic shared memory.
+template <int BN, int MSUB, int MAXST, int EPI>
 cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                        const GemmArgs& args) {
-    using C = GemmCfg<BN, MSUB, STAGES>;
-    auto k = gemm_tc_kernel<BN, MSUB, STAGES, EPI>;
-    // The attribute is per function; setting it on every call is cheap and device-safe.
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+                        GemmArgs args) {
+    using C = GemmCfg<BN, MSUB, MAXST>;
+    auto k = gemm_tc_kernel<BN, MSUB, MAXST, EPI>;
+    args.stages = C::max_stages(args.a_box_rows);
+    if (args.stages < 2) return cudaErrorInvalidConfiguration;
+    const size_t smem = C::smem_bytes(args.stages, args.a_box_rows);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
     if (e != cudaSuccess) return e;
-    return launch(k, grid, kGemmThreads, C::kSmem, st, a, b0, b1, args);
+    return launch(k, grid, kGemmThreads, smem, st, a, b0, b1, args);
 }
 
 struct Launched {
@@ -415,7 +485,19 @@ struct Launched {
     int sms;
 };
 
-int sms_of(const Launched& L) { return L.sms; }
+GemmArgs gemm_args(const GemmPlan& g, int T, int64_t ncols, uint32_t* status) {
+    GemmArgs a = {};
+    a.T = T;
+    a.kblocks = g.kblocks;
+    a.ncols = (int)ncols;
+    a.n_tiles = g.n_tiles;
+    a.m_tiles = g.m_tiles;
+    a.ksplit = g.ksplit;
+    a.b_split_col = INT32_MAX;
+    a.a_box_rows = g.a_box_rows;
+    a.status = status;
+    return a;
+}
 
 mla_status run(const Launched& L) {
     const Args& a = *L.a;
@@ -457,36 +539,13 @@ mla_status run(const Launched& L) {
         wuqqr_bf = ws + p.off_wuqqr;
     }
 
-    // ---- K1: down-projection
-    CUtensorMap mA1, mB1a, mB1b;
-    if (!map_2d(&mA1, x_bf, d.T, d.He, 128) || !map_2d(&mB1a, wdq_bf, d.He, d.Hcq, 64) ||
-        !map_2d(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64))
-        return MLA_ERR_RUNTIME;
-    float* p1 = reinterpret_cast<float*>(ws + p.off_p1);
-    GemmArgs g1 = {};
-    g1.T = T;
-    g1.kblocks = p.g1.kblocks;
-    g1.ncols = (int)p.ncols1;
-    g1.n_tiles = p.g1.n_tiles;
-    g1.m_tiles = p.g1.m_tiles;
-    g1.split = p.g1.split;
-    g1.total = p.g1.total;
-    g1.b_split_col = (int)d.Hcq;
-    g1.clear_status = 1;
-    g1.out_f32 = p1;
-    g1.status = status;
-    cudaError_t e = (p.g1.msub == 1) ? launch_gemm<kBN12, 1, 5, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
-                                     : launch_gemm<kBN12, 2, 3, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
-    if (e != cudaSuccess) return MLA_ERR_RUNTIME;
-    timing_mark(st, "k1_down_proj");
-
-    // ---- F1: partial sums, RmsNorm, RoPE(k^R), cache writes, c^Q
     DownArgs f1 = {};
     f1.T = T;
     f1.Hcq = (int)d.Hcq;
     f1.Hckv = (int)d.Hckv;
     f1.Dr = (int)d.Dr;
-    f1.src = {p1, p.g1.split, p.g1.total, p.g1.grid, p.g1.kblocks, p.g1.bn, T, (int)p.ncols1};
+    float* y1 = reinterpret_cast<float*>(ws + p.off_y1);
+    f1.src = {y1, (int)p.ncols1, p.g1.ksplit, (size_t)d.T * p.ncols1};
     if (sc.x_i8) {
         f1.scale_x = static_cast<const float*>(a.sx->data);
         f1.scale_w_dq = static_cast<const float*>(a.swdq->data);
@@ -511,43 +570,139 @@ mla_status run(const Launched& L) {
     f1.smooth_cq = a.smooth ? static_cast<const float*>(a.smooth->data) : nullptr;
     f1.c_q_scale = reinterpret_cast<float*>(ws + p.off_cqs);
     f1.status = status;
+    const float* row_scale = sc.uqqr_i8 ? reinterpret_cast<const float*>(ws + p.off_cqs) : nullptr;
+    const float* col_scale = sc.uqqr_i8 ? static_cast<const float*>(a.swuqqr->data) : nullptr;
+    __nv_bfloat16* qc = reinterpret_cast<__nv_bfloat16*>(ws + p.off_qc);
+    cudaError_t e;
+
+    // The 3D map of q^C (one head's T x D slice per box) and of W^UK (one head's D x Hckv).
+    CUtensorMap mA3, mB3;
+    const uint32_t a3_rows = (uint32_t)(p.fused ? (d.T + 7) / 8 * 8 : p.g3.a_box_rows);
     {
-        const int grid = T < 16 * sms_of(L) ? T : 16 * sms_of(L);
+        const uint64_t dims[3] = {(uint64_t)d.D, (uint64_t)d.N, (uint64_t)d.T};
+        const uint64_t strides[2] = {(uint64_t)d.D * 2, (uint64_t)d.N * d.D * 2};
+        const uint32_t box[3] = {64, 1, a3_rows};
+        if (!encode_map(&mA3, qc, 3, dims, strides, box)) return MLA_ERR_RUNTIME;
+        const uint64_t dimsb[3] = {(uint64_t)d.Hckv, (uint64_t)d.D, (uint64_t)d.N};
+        const uint64_t stridesb[2] = {(uint64_t)d.Hckv * 2, (uint64_t)d.D * d.Hckv * 2};
+        const uint32_t boxb[3] = {64, 64, 1};
+        if (!encode_map(&mB3, a.wuk->data, 3, dimsb, stridesb, boxb)) return MLA_ERR_RUNTIME;
+    }
+
+    if (p.fused) {
+        // ---- the whole prolog in one persistent kernel
+        const uint32_t rows = (uint32_t)((d.T + 7) / 8 * 8);
+        CUtensorMap mx, mwdq, mwdkvkr, mcq, mwuqqr;
+        if (!map_2d(&mx, x_bf, d.T, d.He, rows) || !map_2d(&mwdq, wdq_bf, d.He, d.Hcq, 64) ||
+            !map_2d(&mwdkvkr, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64) || !map_2d(&mcq, ws + p.off_cq, d.T, d.Hcq, rows) ||
+            !map_2d(&mwuqqr, wuqqr_bf, d.Hcq, p.ncols2, 64))
+            return MLA_ERR_RUNTIME;
+        FusedArgs fa = {};
+        fa.T = T;
+        fa.a_bytes = (int)rows * 128;
+        fa.ra = p.fused_ra;
+        fa.rb = p.fused_rb;
+        fa.x = static_cast<const __nv_bfloat16*>(x_bf);
+        fa.ncols_x = (int)d.He;
+        fa.nt1 = p.fused_nt1;
+        fa.s1 = p.fused_s1;
+        fa.kb1 = (int)((d.He + 63) / 64);
+        fa.hcq = (int)d.Hcq;
+        fa.ncols1 = (int)p.ncols1;
+        fa.y1 = y1;
+        fa.down = f1;
+        fa.ep.T = T;
+        fa.ep.N = (int)d.N;
+        fa.ep.q_c = qc;
+        fa.ep.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
+        fa.ep.rope_cos = f1.rope_cos;
+        fa.ep.rope_sin = f1.rope_sin;
+        fa.ep.row_scale = row_scale;
+        fa.ep.col_scale = col_scale;
+        fa.ep.Hckv = (int)d.Hckv;
+        fa.ep.tiles_per_head = 1;
+        fa.ep.status = status;
+        if (sc.q_i8) {
+            fa.ep.q_out_i8 = static_cast<int8_t*>(a.qout->data);
+            fa.ep.q_scale = static_cast<float*>(a.qscale->data);
+        } else {
+            fa.ep.q_out_bf16 = static_cast<__nv_bfloat16*>(a.qout->data);
+        }
+        fa.N = (int)d.N;
+        fa.kb2 = (int)((d.Hcq + 63) / 64);
+        fa.kb4 = (int)((d.D + 63) / 64);
+        fa.nbox4 = (int)(d.Hckv / 64);
+        fa.arrive_flags = reinterpret_cast<unsigned long long*>(ws + p.off_flags);
+        fa.done_flags = fa.arrive_flags + 2 * L.sms;
+        fa.tag = next_tag();
+        fa.status = status;
+        e = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.fused_smem);
+        if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)L.sms);
+        cfg.blockDim = dim3((unsigned)kFusedThreads);
+        cfg.dynamicSmemBytes = p.fused_smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: the grid barriers need it
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, mx, mwdq, mwdkvkr, mcq, mwuqqr, mB3, fa);
+        if (e == cudaSuccess) {
+            timing_mark(st, "decode_fused");
+            if (g_timing.enabled) g_timing.have = true;
+            return MLA_OK;
+        }
+        // Not all CTAs can be resident (the device is shared): run the kernel-per-step path.
+        if (e != cudaErrorCooperativeLaunchTooLarge) return MLA_ERR_RUNTIME;
+        (void)cudaGetLastError();
+    }
+
+    // ---- K1: down-projection x . [W^DQ | W^DKV | W^KR] -> fp32 rows Y1
+    CUtensorMap mA1, mB1a, mB1b;
+    if (!map_2d(&mA1, x_bf, d.T, d.He, (uint32_t)p.g1.a_box_rows) || !map_2d(&mB1a, wdq_bf, d.He, d.Hcq, 64) ||
+        !map_2d(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64))
+        return MLA_ERR_RUNTIME;
+    GemmArgs g1 = gemm_args(p.g1, T, p.ncols1, status);
+    g1.b_split_col = (int)d.Hcq;
+    g1.clear_status = 1;
+    g1.out_f32 = y1;
+    if (p.g1.bn == 64)
+        e = launch_gemm<64, 1, 32, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+    else
+        e = launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+    if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+    timing_mark(st, "k1_down_proj");
+
+    // ---- F1: RmsNorm, RoPE(k^R), cache writes, c^Q
+    {
+        const int grid = T < 16 * L.sms ? T : 16 * L.sms;
         e = launch(finalize_down_kernel, grid, kRowThreads, (size_t)p.ncols1 * 4, st, f1);
         if (e != cudaSuccess) return MLA_ERR_RUNTIME;
         timing_mark(st, "f1_norm_rope_cache");
     }
 
-    // ---- K2: up-projection
+    // ---- K2: up-projection c^Q . W^UqQr -> RoPE(q^R) and q^C
     CUtensorMap mA2, mB2;
-    if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, 128) || !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64))
+    if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
+        !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64))
         return MLA_ERR_RUNTIME;
-    const float* row_scale = sc.uqqr_i8 ? reinterpret_cast<const float*>(ws + p.off_cqs) : nullptr;
-    const float* col_scale = sc.uqqr_i8 ? static_cast<const float*>(a.swuqqr->data) : nullptr;
-    __nv_bfloat16* qc = reinterpret_cast<__nv_bfloat16*>(ws + p.off_qc);
-    GemmArgs g2 = {};
-    g2.T = T;
-    g2.kblocks = p.g2.kblocks;
-    g2.ncols = (int)p.ncols2;
-    g2.n_tiles = p.g2.n_tiles;
-    g2.m_tiles = p.g2.m_tiles;
-    g2.split = p.g2.split;
-    g2.total = p.g2.total;
-    g2.b_split_col = INT32_MAX;   // one weight map
-    g2.status = status;
+    GemmArgs g2 = gemm_args(p.g2, T, p.ncols2, status);
+    g2.N = (int)d.N;
+    g2.q_c = qc;
+    g2.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
+    g2.rope_cos = f1.rope_cos;
+    g2.rope_sin = f1.rope_sin;
+    g2.row_scale = row_scale;
+    g2.col_scale = col_scale;
+    g2.out_f32 = reinterpret_cast<float*>(ws + p.off_y2);
     if (p.g2_fused) {
-        g2.N = (int)d.N;
-        g2.q_c = qc;
-        g2.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
-        g2.rope_cos = f1.rope_cos;
-        g2.rope_sin = f1.rope_sin;
-        g2.row_scale = row_scale;
-        g2.col_scale = col_scale;
-        e = launch_gemm<kBN12, 2, 3, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2);
+        e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2)
+                             : launch_gemm<192, 2, 4, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2);
     } else {
-        g2.out_f32 = reinterpret_cast<float*>(ws + p.off_p2);
-        e = (p.g2.msub == 1) ? launch_gemm<kBN12, 1, 5, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2)
-                             : launch_gemm<kBN12, 2, 3, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2);
+        e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2)
+                             : launch_gemm<192, 2, 4, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2);
     }
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k2_up_proj");
@@ -557,52 +712,32 @@ mla_status run(const Launched& L) {
         f2.N = (int)d.N;
         f2.D = (int)d.D;
         f2.Dr = (int)d.Dr;
-        f2.src = {reinterpret_cast<const float*>(ws + p.off_p2), p.g2.split, p.g2.total, p.g2.grid, p.g2.kblocks,
-                  p.g2.bn, T, (int)p.ncols2};
+        f2.src = {reinterpret_cast<const float*>(ws + p.off_y2), (int)p.ncols2, 1, (size_t)d.T * p.ncols2};
         f2.row_scale = row_scale;
         f2.col_scale = col_scale;
         f2.rope_cos = f1.rope_cos;
         f2.rope_sin = f1.rope_sin;
         f2.q_c = qc;
         f2.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
-        const int grid = T < 16 * sms_of(L) ? T : 16 * sms_of(L);
+        const int grid = T < 16 * L.sms ? T : 16 * L.sms;
         e = launch(finalize_up_kernel, grid, kRowThreads, 0, st, f2);
         if (e != cudaSuccess) return MLA_ERR_RUNTIME;
         timing_mark(st, "f2_rope_qc");
     }
 
     // ---- K3: per-head W^UK contraction
-    CUtensorMap mA3, mB3;
-    {
-        const uint64_t dims[3] = {(uint64_t)d.D, (uint64_t)d.N, (uint64_t)d.T};
-        const uint64_t strides[2] = {(uint64_t)d.D * 2, (uint64_t)d.N * d.D * 2};
-        const uint32_t box[3] = {64, 1, 128};
-        if (!encode_map(&mA3, qc, 3, dims, strides, box)) return MLA_ERR_RUNTIME;
-        const uint64_t dimsb[3] = {(uint64_t)d.Hckv, (uint64_t)d.D, (uint64_t)d.N};
-        const uint64_t stridesb[2] = {(uint64_t)d.Hckv * 2, (uint64_t)d.D * d.Hckv * 2};
-        const uint32_t boxb[3] = {64, 64, 1};
-        if (!encode_map(&mB3, a.wuk->data, 3, dimsb, stridesb, boxb)) return MLA_ERR_RUNTIME;
-    }
-    GemmArgs g3 = {};
-    g3.T = T;
-    g3.kblocks = p.g3.kblocks;
-    g3.ncols = (int)d.Hckv;
-    g3.n_tiles = p.g3.n_tiles;
-    g3.m_tiles = p.g3.m_tiles;
-    g3.split = 0;
-    g3.b_split_col = INT32_MAX;
+    GemmArgs g3 = gemm_args(p.g3, T, d.Hckv, status);
     g3.head_mode = 1;
     g3.tiles_per_head = p.g3.n_tiles / (int)d.N;
     g3.N = (int)d.N;
     g3.Hckv = (int)d.Hckv;
-    g3.status = status;
     if (sc.q_i8) {
         g3.q_out_i8 = static_cast<int8_t*>(a.qout->data);
         g3.q_scale = static_cast<float*>(a.qscale->data);
-        e = launch_gemm<512, 1, 2, EPI_QN>(p.g3.grid, st, mA3, mB3, mB3, g3);
+        e = launch_gemm<512, 1, 4, EPI_QN>(p.g3.grid, st, mA3, mB3, mB3, g3);
     } else {
         g3.q_out_bf16 = static_cast<__nv_bfloat16*>(a.qout->data);
-        e = launch_gemm<256, 1, 4, EPI_QN>(p.g3.grid, st, mA3, mB3, mB3, g3);
+        e = launch_gemm<256, 1, 8, EPI_QN>(p.g3.grid, st, mA3, mB3, mB3, g3);
     }
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k3_absorb_uk");

@@ -87,6 +87,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Asynchronous prefetch of [p, p + bytes) into L2 (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
 // L2 policies: streamed-once data (weights) goes first; reused data (activations) stays.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

@@ -145,10 +145,14 @@ def run_cuda(args, rank, world):
     call = PrologCall(cfg, inp, device=dev)
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
 
     def flush_l2():
-        flush.fill_(1)
+        # Write 2 x L2 bytes, then read another 2 x L2 bytes: the call starts with none of its
+        # data in L2 and with clean lines only (no write-back of the flush charged to it).
+        flush_w.fill_(1)
+        flush_r.sum()
 
     # warm-up
     for _ in range(args.warmup):
@@ -184,7 +188,6 @@ def run_cuda(args, rank, world):
     ms_per_step = total_ms / K
     tokens = s.T * K * world
     value = tokens / (total_ms / 1e3)
-    kernels_per_step = 5 if not cfg.x_int8 else 9
 
     # per-kernel durations (each kernel alone, events between kernels) for the roofline
     mla_prolog_timing_enable(True)
@@ -196,6 +199,7 @@ def run_cuda(args, rank, world):
             per_kernel.setdefault(name, []).append(ms)
     mla_prolog_timing_enable(False)
     kern_ms = {k: statistics.mean(v) for k, v in per_kernel.items()}
+    kernels_per_step = len(kern_ms)
     k2_ms = kern_ms.get("k2_up_proj")
     dom_bytes = k2_bytes(s)
     achieved = dom_bytes / (k2_ms / 1e3) / 1e9 if k2_ms else None
@@ -231,7 +235,8 @@ def run_cuda(args, rank, world):
             "config": {"workload": cfg.workload, "T": s.T, "He": s.He, "Hcq": s.Hcq, "N": s.N, "D": s.D,
                        "Dr": s.Dr, "Hckv": s.Hckv, "kv_cache": f"{s.block_num}x{s.block_size}",
                        "global_batch": s.T * world, "parallelism": f"replicas x{world}",
-                       "l2": "flushed before every step (2 x L2 bytes rewritten, outside the timed events)",
+                       "l2": ("flushed before every step: 2 x L2 bytes written, then another 2 x L2 bytes "
+                              "read, outside the timed events"),
                        "timing": "CUDA events around each mla_prolog call on its stream"},
             "roofline": roofline, "step_roofline": step_roof, "kernels_ms": kern_ms,
             "gpu_launches": kernels_per_step * K,
@@ -386,6 +391,23 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+def run_kernels_only(args):
+    """Just `warmup + steps` prolog calls on one workload (no flush, no extras): the command
+    the ncu captures profile."""
+    import torch
+    from attention_pre_processing_gb300 import build as cuda_build
+    from attention_pre_processing_gb300 import workloads
+    from attention_pre_processing_gb300.runner import PrologCall
+    cuda_build.build()
+    cfg = workloads.config(args.workload)
+    call = PrologCall(cfg, workloads.make_inputs(cfg))
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    if call.status() != 0:
+        raise SystemExit("device status bits set")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,7 +417,12 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--kernels-only", action="store_true", help="only warmup+steps calls of --workload")
+    ap.add_argument("--workload", default=HEADLINE)
     args = ap.parse_args()
+    if args.kernels_only:
+        run_kernels_only(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     rank = int(os.environ.get("RANK", 0))

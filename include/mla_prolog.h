@@ -126,7 +126,8 @@ typedef struct {
  * cache is written.
  *
  * Tiling rules (561002 when broken): He % 8 == 0, Hcq % 64 == 0, D % 8 == 0, Dr even,
- * N*(D+Dr) % 8 == 0, (Hckv+Dr) % 8 == 0, Hckv % 8 == 0, and Hckv <= 512 when queryOut is int8.
+ * N*(D+Dr) % 8 == 0, (Hckv+Dr) % 8 == 0, Hckv % 8 == 0, Hcq + Hckv + Dr <= 12288,
+ * and Hckv <= 512 when queryOut is int8.
  * Every device pointer must be 16-byte aligned.
  */
 MLA_API mla_status mla_prolog_workspace_size(
