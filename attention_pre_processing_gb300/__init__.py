@@ -16,15 +16,18 @@ __all__ = [
     "MlaError", "TENSOR_ARGS", "lib", "mla_prolog_workspace_size", "mla_prolog",
     "mla_prolog_device_status", "mla_prolog_status_string", "STATUS", "DEV_CACHE_INDEX_RANGE",
     "DEV_WAIT_TIMEOUT", "library_path", "mla_prolog_timing_enable", "mla_prolog_timing_read",
+    "mla_prolog_no_alloc", "NO_ALLOC_SCRATCH_BYTES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "libmla_prolog.so")
 
 STATUS = {0: "MLA_OK", 161001: "MLA_ERR_PARAM_NULLPTR", 161002: "MLA_ERR_PARAM_INVALID",
-          361001: "MLA_ERR_RUNTIME", 561002: "MLA_ERR_TILING"}
+          361001: "MLA_ERR_RUNTIME", 561002: "MLA_ERR_TILING", 561003: "MLA_ERR_SCRATCH_LIMIT"}
 DEV_CACHE_INDEX_RANGE = 0x1
 DEV_WAIT_TIMEOUT = 0x2
+# Size of the library's fixed scratch buffer behind mla_prolog_no_alloc (MLA_NO_ALLOC_SCRATCH_BYTES).
+NO_ALLOC_SCRATCH_BYTES = 16 << 20
 
 # Positional order of the tensor arguments of the C entry points (before the scalars).
 TENSOR_ARGS = ("x", "w_dq", "w_uqqr", "w_uk", "w_dkvkr", "gamma_cq", "gamma_ckv", "rope_sin", "rope_cos",
@@ -67,6 +70,8 @@ def lib():
         L.mla_prolog_workspace_size.restype = ctypes.c_int
         L.mla_prolog.argtypes = tens + scal + outs + [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
         L.mla_prolog.restype = ctypes.c_int
+        L.mla_prolog_no_alloc.argtypes = tens + scal + outs + [ctypes.c_void_p]
+        L.mla_prolog_no_alloc.restype = ctypes.c_int
         L.mla_prolog_device_status.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
                                                ctypes.POINTER(ctypes.c_uint32)]
         L.mla_prolog_device_status.restype = ctypes.c_int
@@ -147,6 +152,24 @@ def mla_prolog(tensors: Dict, eps_cq: float, eps_ckv: float, workspace, workspac
                           ctypes.c_void_p(stream))
     if check and rc != 0:
         raise MlaError(rc, "mla_prolog")
+    return rc
+
+
+def mla_prolog_no_alloc(tensors: Dict, eps_cq: float, eps_ckv: float, stream=None,
+                        cache_mode: Optional[str] = "PA_BSND", check: bool = True) -> int:
+    """mla_prolog without a workspace argument, for callers that cannot allocate device memory:
+    the library runs the same kernels on its own fixed scratch buffer (NO_ALLOC_SCRATCH_BYTES
+    per device).  Calls that overlap on the GPU share that buffer and race; the first call on a
+    device looks the buffer up and belongs before any stream capture."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    args, _keep = _marshal(tensors, eps_cq, eps_ckv, cache_mode)
+    rc = lib().mla_prolog_no_alloc(*args, ctypes.c_void_p(stream))
+    if check and rc != 0:
+        raise MlaError(rc, "mla_prolog_no_alloc")
     return rc
 
 

@@ -831,6 +831,53 @@ extern "C" mla_status mla_prolog(MLA_TENSOR_PARAMS, void* workspace, uint64_t wo
     return run(L);
 }
 
+// ------------------------------------------------------- no-allocation variant
+
+// The workspace of mla_prolog_no_alloc(): one buffer per device, part of the library's
+// device image.  Host code must not use this name as a device address; the address is
+// looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_no_alloc_scratch[MLA_NO_ALLOC_SCRATCH_BYTES];
+
+static constexpr int kMaxDevices = 64;
+static std::mutex g_scratch_mu;
+static void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch buffer on the current device (looked up on first use).
+static mla_status no_alloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_RUNTIME;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_RUNTIME;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return MLA_OK;
+}
+
+extern "C" mla_status mla_prolog_no_alloc(MLA_TENSOR_PARAMS, void* stream) {
+    const Args a = pack_args(MLA_TENSOR_ARGS);
+    Dims d;
+    Scenario sc;
+    const mla_status s = validate(a, d, sc);
+    if (s != MLA_OK) return s;
+    if (d.T == 0) return MLA_OK;
+    int sms = 0;
+    if (device_sms(&sms) != 0) return MLA_ERR_RUNTIME;
+    const Plan plan = make_plan(d, sc, sms);
+    if (plan.bytes > MLA_NO_ALLOC_SCRATCH_BYTES) return MLA_ERR_SCRATCH_LIMIT;
+    void* ws = nullptr;
+    const mla_status ss = no_alloc_scratch(&ws);
+    if (ss != MLA_OK) return ss;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The status word starts at zero; everything else the kernels read they write first.
+    if (cudaMemsetAsync(ws, 0, kStatusBytes, st) != cudaSuccess) return MLA_ERR_RUNTIME;
+    Launched L{&a, d, sc, plan, static_cast<uint8_t*>(ws), st, sms};
+    timing_begin(L.st);
+    return run(L);
+}
+
 extern "C" mla_status mla_prolog_device_status(const void* workspace, uint64_t workspaceSize, void* stream,
                                                uint32_t* bits) {
     if (workspace == nullptr || bits == nullptr) return MLA_ERR_PARAM_NULLPTR;
@@ -871,6 +918,9 @@ extern "C" const char* mla_prolog_status_string(mla_status status) {
         case MLA_ERR_PARAM_INVALID: return "MLA_ERR_PARAM_INVALID (161002): shape, dtype or scenario not accepted";
         case MLA_ERR_RUNTIME: return "MLA_ERR_RUNTIME (361001): a CUDA runtime call failed";
         case MLA_ERR_TILING: return "MLA_ERR_TILING (561002): shapes outside the kernels' tiling rules";
+        case MLA_ERR_SCRATCH_LIMIT:
+            return "MLA_ERR_SCRATCH_LIMIT (561003): the call needs more workspace than the fixed "
+                   "no-allocation scratch buffer (MLA_NO_ALLOC_SCRATCH_BYTES) holds";
     }
     return "unknown mla_status";
 }

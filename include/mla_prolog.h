@@ -58,7 +58,9 @@ typedef enum {
     MLA_ERR_PARAM_NULLPTR = 161001, /* a required tensor, its data pointer, or an out-pointer is NULL */
     MLA_ERR_PARAM_INVALID = 161002, /* shape / dtype / optional-argument pattern not accepted */
     MLA_ERR_RUNTIME = 361001,       /* a CUDA runtime call failed */
-    MLA_ERR_TILING = 561002         /* valid operation, but outside the kernels' tiling rules */
+    MLA_ERR_TILING = 561002,        /* valid operation, but outside the kernels' tiling rules */
+    MLA_ERR_SCRATCH_LIMIT = 561003  /* mla_prolog_no_alloc only: the call needs more scratch than
+                                       MLA_NO_ALLOC_SCRATCH_BYTES (no counterpart on the pages) */
 } mla_status;
 
 typedef enum {
@@ -198,6 +200,54 @@ typedef struct {
 
 MLA_API mla_status mla_prolog_timing_enable(int enable);
 MLA_API mla_status mla_prolog_timing_read(mla_kernel_time* out, int capacity, int* count);
+
+/*
+ * mla_prolog without a caller-supplied workspace.  The pages have no counterpart: their
+ * operator always takes a workspace from the caller.
+ *
+ * Some callers have no way to obtain device memory on their own: a plugin whose host
+ * process owns the whole device memory budget and hands out no allocator, or a runtime
+ * that plans every buffer once at start-up and may not call cudaMalloc afterwards.  They
+ * can provide the inputs and outputs, but not the workspace mla_prolog() needs.  This
+ * entry point takes the same tensor and scalar arguments (no workspace) and runs the same
+ * kernels, with the workspace placed in one fixed scratch buffer that the library itself
+ * holds in device memory: MLA_NO_ALLOC_SCRATCH_BYTES bytes, reserved on every GPU that
+ * loads the library, for the life of the process.
+ *
+ * - Size limit: calls whose workspace (as mla_prolog_workspace_size reports it) exceeds
+ *   MLA_NO_ALLOC_SCRATCH_BYTES return MLA_ERR_SCRATCH_LIMIT and launch nothing.  16 MiB
+ *   covers bf16 decode batches of up to 128 tokens with DeepSeek-V3 shapes; int8-input
+ *   calls (which widen the int8 weights into the workspace) do not fit.
+ * - No allocation: the call makes no cudaMalloc / cudaFree and no allocating library call.
+ *   The first call on each device looks up the scratch buffer's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before any
+ *   stream capture on the device.
+ * - Sharing: every call on a device uses the same scratch buffer, which keeps the previous
+ *   call's contents.  The call clears the part that must start at zero (the status word)
+ *   on `stream` before its kernels run.  Calls whose kernels overlap on the GPU (other
+ *   streams, or other host threads) race on the scratch buffer and give wrong results:
+ *   order them on one stream or with events.
+ * - The device status word lives in the scratch buffer and is not exposed; out-of-range
+ *   cacheIndex rows are still skipped.
+ *
+ * Returns the codes of mla_prolog(), plus MLA_ERR_SCRATCH_LIMIT, and 361001 if the scratch
+ * buffer's address cannot be obtained.
+ */
+#define MLA_NO_ALLOC_SCRATCH_BYTES (16ull << 20)
+
+MLA_API mla_status mla_prolog_no_alloc(
+    const mla_tensor* tokenX, const mla_tensor* weightDq, const mla_tensor* weightUqQr,
+    const mla_tensor* weightUk, const mla_tensor* weightDkvKr,
+    const mla_tensor* rmsnormGammaCq, const mla_tensor* rmsnormGammaCkv,
+    const mla_tensor* ropeSin, const mla_tensor* ropeCos, const mla_tensor* cacheIndex,
+    const mla_tensor* kvCache, const mla_tensor* krCache,
+    const mla_tensor* dequantScaleX, const mla_tensor* dequantScaleWDq,
+    const mla_tensor* dequantScaleWUqQr, const mla_tensor* dequantScaleWDkvKr,
+    const mla_tensor* quantScaleCkv, const mla_tensor* quantScaleCkr,
+    const mla_tensor* smoothScalesCq,
+    double rmsnormEpsilonCq, double rmsnormEpsilonCkv, const char* cacheMode,
+    const mla_tensor* queryOut, const mla_tensor* queryRopeOut,
+    const mla_tensor* dequantScaleQNopeOut, void* stream);
 
 /* A constant, human-readable name for a return code. */
 MLA_API const char* mla_prolog_status_string(mla_status status);

@@ -40,6 +40,7 @@ def test_status_strings(lib):
     assert mla.mla_prolog_status_string(0) == "MLA_OK"
     assert "161001" in mla.mla_prolog_status_string(161001)
     assert "561002" in mla.mla_prolog_status_string(561002)
+    assert "561003" in mla.mla_prolog_status_string(561003)
 
 
 # ---------------------------------------------------------- descriptors
