@@ -215,6 +215,24 @@ __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, floa
     sync();   // ys and red are reused by the next row
 }
 
+// L2 prefetch of everything the row work of this CTA's tokens reads besides the partials.
+__device__ __forceinline__ void prefetch_down_inputs(const DownArgs& a, int tid, int nthr) {
+    prefetch_l2_range(a.gamma_cq, (size_t)a.Hcq * 2, tid, nthr);
+    prefetch_l2_range(a.gamma_ckv, (size_t)a.Hckv * 2, tid, nthr);
+    prefetch_l2_range(a.scale_w_dq, a.scale_w_dq ? (size_t)a.Hcq * 4 : 0, tid, nthr);
+    prefetch_l2_range(a.scale_w_dkvkr, a.scale_w_dkvkr ? (size_t)(a.Hckv + a.Dr) * 4 : 0, tid, nthr);
+    prefetch_l2_range(a.quant_scale_ckv, a.quant_scale_ckv ? (size_t)a.Hckv * 4 : 0, tid, nthr);
+    prefetch_l2_range(a.smooth_cq, a.smooth_cq ? (size_t)a.Hcq * 4 : 0, tid, nthr);
+    if (tid == 0) {
+        for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+            prefetch_l2(a.rope_cos + (size_t)t * a.Dr);
+            prefetch_l2(a.rope_sin + (size_t)t * a.Dr);
+            prefetch_l2(a.cache_index + t);
+            if (a.scale_x) prefetch_l2(a.scale_x + t);
+        }
+    }
+}
+
 // One CTA per token (grid-stride).
 __global__ void __launch_bounds__(kRowThreads) finalize_down_kernel(const DownArgs a) {
     extern __shared__ float ys[];   // Hcq + Hckv + Dr
@@ -222,6 +240,9 @@ __global__ void __launch_bounds__(kRowThreads) finalize_down_kernel(const DownAr
     // All CTAs of this grid are resident once every one has passed here: the next kernel may
     // start its prologue (and its first weight loads) now.
     pdl_launch_dependents();
+    // The small inputs do not depend on the previous kernel: request them into L2 while it
+    // finishes, so that the row work does not wait on cold lines behind the weight stream.
+    prefetch_down_inputs(a, threadIdx.x, kRowThreads);
     pdl_wait();
     for (int t = blockIdx.x; t < a.T; t += gridDim.x)
         down_row<kRowThreads>(a, t, threadIdx.x, ys, red, CtaSync{});

@@ -67,11 +67,14 @@ struct GemmArgs {
     __nv_bfloat16* q_out_bf16;     // (T, N, Hckv)
     int8_t* q_out_i8;              // (T, N, Hckv)
     float* q_scale;                // (T, N)
+    int tma_out;                   // EPI_QN: store q^N through shared memory with TMA (map_o)
     uint32_t* status;
 };
 
-template <int BN, int MSUB, int MAXST>
+// OUTB: 4 KB staging buffers per epilogue warp for TMA stores of the output (0 = none).
+template <int BN, int MSUB, int MAXST, int OUTB = 0>
 struct GemmCfg {
+    static constexpr int kOutBytes = 4 * OUTB * 4096;
     static constexpr int kBStage = BN * kBK * 2;            // BN/64 boxes of 64 x 64
     static constexpr int kAcc = MSUB * BN;                  // TMEM columns per accumulator set
     static constexpr int kNBuf = (2 * kAcc <= 512) ? 2 : 1;
@@ -90,10 +93,10 @@ struct GemmCfg {
     // A region first: a 128-row MMA operand read from the last A stage with a short box runs
     // at most 16 KB past it, into the B ring (>= 2 stages of >= 8 KB), inside the block.
     static __host__ __device__ size_t smem_bytes(int stages, int a_box_rows) {
-        return 1024 + kBarBytes + (size_t)stages * stage_bytes(a_box_rows);
+        return 1024 + kBarBytes + (size_t)stages * stage_bytes(a_box_rows) + kOutBytes;
     }
     static __host__ int max_stages(int a_box_rows) {
-        int s = (int)((kSmemLimit - 1024 - kBarBytes) / stage_bytes(a_box_rows));
+        int s = (int)((kSmemLimit - 1024 - kBarBytes - kOutBytes) / stage_bytes(a_box_rows));
         return s < MAXST ? s : MAXST;
     }
     static_assert(2 * kBStage >= 16384, "B ring must cover the A over-read");
@@ -336,6 +339,103 @@ __device__ __forceinline__ void epilogue_qn(const GemmArgs& a, const Unit& u, co
     if (valid) a.q_scale[(size_t)row * a.N + head] = scale;
 }
 
+// q^N of one tile through shared memory and TMA stores.  Each epilogue warp turns its 32 rows,
+// one 128-byte column chunk at a time, into a 32 x 128-byte box in the 128-byte-swizzled
+// layout (16-byte chunk c of row r at (c ^ (r % 8)) * 16), then one lane stores the box with
+// TMA; rows at or past T fall outside the tensor map and are not written.  `obuf` holds the
+// warp's OUTB staging buffers, `ob` the next one to use.
+template <int OUTB>
+struct OutStage {
+    uint8_t* obuf;
+    int ob;
+    const CUtensorMap* map;
+    int lane;
+    __device__ __forceinline__ void put(const uint32_t (&w)[32], int x, int y) {
+        const uint32_t buf = smem_u32(obuf + ob * 4096);
+        if (lane == 0) bulk_wait_read<OUTB - 1>();   // the store that last read this buffer
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             buf + (uint32_t)(lane * 128 + ((c ^ (lane & 7)) << 4))),
+                         "r"(w[4 * c]), "r"(w[4 * c + 1]), "r"(w[4 * c + 2]), "r"(w[4 * c + 3])
+                         : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(map, buf, x, y);
+            bulk_commit();
+        }
+        ob = (ob + 1 == OUTB) ? 0 : ob + 1;
+    }
+    __device__ __forceinline__ void drain() const {
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+};
+
+template <int BN, int OUTB>
+__device__ __forceinline__ void epilogue_qn_tma(const GemmArgs& a, const Unit& u, const TmemSrc& src, int q,
+                                                OutStage<OUTB>& out) {
+    const int head = u.n_tile / a.tiles_per_head;
+    const int c0 = (u.n_tile % a.tiles_per_head) * BN;
+    const int row0 = u.m_tile * 128 + q * 32;   // this warp's first row
+    const int row = row0 + out.lane;
+    if (row0 >= a.T) return;                     // warp-uniform: no valid row here
+    if (a.q_out_i8 == nullptr) {
+#pragma unroll 1
+        for (int j = 0; j < BN / 64; ++j) {
+            const int col = c0 + 64 * j;
+            if (col >= a.Hckv) break;   // uniform across the warp
+            uint32_t w[32];
+            float v[32];
+            src.load(0, BN, 64 * j, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+            src.load(0, BN, 64 * j + 32, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+            out.put(w, head * a.Hckv + col, row0);
+        }
+        return;
+    }
+    // Dynamic int8 quantisation of the whole (token, head) row (c0 = 0: one tile per head).
+    float m = 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        const int col = ch * 32;
+        if (col >= a.Hckv) break;
+        float v[32];
+        src.load(0, BN, col, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+    }
+    const float scale = m / 127.f;
+#pragma unroll 1
+    for (int j = 0; j < BN / 128; ++j) {
+        const int col = 128 * j;
+        if (col >= a.Hckv) break;
+        uint32_t w[32];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float v[32];
+            src.load(0, BN, col + 32 * h, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint32_t packed = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int qv = (scale > 0.f) ? quant_i8(__fdiv_rn(v[4 * i + e], scale)) : 0;
+                    packed |= ((uint32_t)(qv & 0xFF)) << (8 * e);
+                }
+                w[8 * h + i] = packed;
+            }
+        }
+        out.put(w, head * a.Hckv + c0 + col, row0);
+    }
+    if (row < a.T) a.q_scale[(size_t)row * a.N + head] = scale;
+}
+
 // ---------------------------------------------------------------------- loads
 
 // Weight tile of k-block kb: BN/64 boxes of 64 columns x 64 rows.
@@ -379,11 +479,12 @@ __device__ __forceinline__ void load_a(const GemmArgs& a, const Unit& u, int kb,
 
 // ---------------------------------------------------------------------- kernel
 
-template <int BN, int MSUB, int MAXST, int EPI>
+template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
-                   const __grid_constant__ CUtensorMap map_b1, const GemmArgs args) {
-    using C = GemmCfg<BN, MSUB, MAXST>;
+                   const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_o,
+                   const GemmArgs args) {
+    using C = GemmCfg<BN, MSUB, MAXST, OUTB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -399,6 +500,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int a_box = args.a_box_rows * 128;
     uint8_t* sA = smem + C::kBarBytes;
     uint8_t* sB = sA + (size_t)stages * a_stage;
+    uint8_t* sOut = sB + (size_t)stages * C::kBStage;   // OUTB x 4 KB per epilogue warp
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -407,6 +509,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b0);
         tma_prefetch_map(&map_b1);
+        if (OUTB > 0 && args.tma_out) tma_prefetch_map(&map_o);
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
@@ -547,6 +650,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------------ epilogue warps
         const int q = warp & 3;   // TMEM lane quarter this warp may access
         const int row_in = q * 32 + lane;
+        OutStage<OUTB> ostage{sOut + (size_t)(warp - 2) * OUTB * 4096, 0, &map_o, lane};
+        if constexpr (EPI == EPI_QROPE) {
+            // This thread's RoPE table rows of its first tile, into L2 during the main loop.
+            Unit u0;
+            if (get_unit(args, 0, u0)) {
+                for (int ms = 0; ms < MSUB; ++ms) {
+                    const int r = u0.m_tile * MSUB * 128 + ms * 128 + row_in;
+                    if (r < args.T) {
+                        prefetch_l2(args.rope_cos + (size_t)r * 64);
+                        prefetch_l2(args.rope_sin + (size_t)r * 64);
+                    }
+                }
+            }
+        }
         uint32_t ai = 0;
         Unit u;
         for (int idx = 0; get_unit(args, idx, u); ++idx, ++ai) {
@@ -570,11 +687,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             } else if constexpr (EPI == EPI_QROPE) {
                 epilogue_qrope<MSUB>(args, row0, u.n_tile, tsrc);
             } else {
-                epilogue_qn<BN>(args, u, tsrc, row_in);
+                if constexpr (OUTB > 0) {
+                    if (args.tma_out)
+                        epilogue_qn_tma<BN, OUTB>(args, u, tsrc, q, ostage);
+                    else
+                        epilogue_qn<BN>(args, u, tsrc, row_in);
+                } else {
+                    epilogue_qn<BN>(args, u, tsrc, row_in);
+                }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[b]));
         }
+        if constexpr (OUTB > 0) ostage.drain();   // stores read their shared memory and land
     }
 
     tc_fence_before();

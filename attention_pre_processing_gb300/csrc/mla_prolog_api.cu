@@ -377,7 +377,7 @@ bool get_encoder() {
 
 // bf16 map with a 64-element (128-byte) inner box and 128-byte swizzle.
 bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-                const uint32_t* box) {
+                const uint32_t* box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     cuuint64_t gd[3];
     cuuint64_t gs[2];
     cuuint32_t bx[3];
@@ -387,7 +387,7 @@ bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims
         bx[i] = box[i];
     }
     for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs,
+    const CUresult r = g_encode(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), gd, gs,
                                 bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -462,17 +462,20 @@ cudaError_t launch(Kernel k, int grid, int block, size_t smem, cudaStream_t st, 
 }
 
 // Launches one GEMM instantiation; fills in the ring depth and dynamic shared memory.
-template <int BN, int MSUB, int MAXST, int EPI>
+template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0>
 cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                        GemmArgs args) {
-    using C = GemmCfg<BN, MSUB, MAXST>;
-    auto k = gemm_tc_kernel<BN, MSUB, MAXST, EPI>;
+                        GemmArgs args, const CUtensorMap* out = nullptr) {
+    using C = GemmCfg<BN, MSUB, MAXST, OUTB>;
+    auto k = gemm_tc_kernel<BN, MSUB, MAXST, EPI, OUTB>;
+    CUtensorMap mo;
+    std::memset(&mo, 0, sizeof mo);
+    if (out != nullptr) mo = *out;
     args.stages = C::max_stages(args.a_box_rows);
     if (args.stages < 2) return cudaErrorInvalidConfiguration;
     const size_t smem = C::smem_bytes(args.stages, args.a_box_rows);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
     if (e != cudaSuccess) return e;
-    return launch(k, grid, kGemmThreads, smem, st, a, b0, b1, args);
+    return launch(k, grid, kGemmThreads, smem, st, a, b0, b1, mo, args);
 }
 
 struct Launched {
@@ -731,13 +734,31 @@ mla_status run(const Launched& L) {
     g3.tiles_per_head = p.g3.n_tiles / (int)d.N;
     g3.N = (int)d.N;
     g3.Hckv = (int)d.Hckv;
+    // queryOut as a (T, N * Hckv) matrix for TMA stores of 32-row x 128-byte boxes (whole boxes
+    // stay inside one head when Hckv is a multiple of the box width).
+    CUtensorMap mO3;
+    {
+        const uint64_t cols = (uint64_t)d.N * (uint64_t)d.Hckv;
+        if (sc.q_i8) {
+            const uint64_t dims[2] = {cols, (uint64_t)d.T};
+            const uint64_t strides[1] = {cols};
+            const uint32_t box[2] = {128, 32};
+            g3.tma_out = d.Hckv % 128 == 0 && encode_map(&mO3, a.qout->data, 2, dims, strides, box,
+                                                          CU_TENSOR_MAP_DATA_TYPE_UINT8);
+        } else {
+            const uint64_t dims[2] = {cols, (uint64_t)d.T};
+            const uint64_t strides[1] = {cols * 2};
+            const uint32_t box[2] = {64, 32};
+            g3.tma_out = d.Hckv % 64 == 0 && encode_map(&mO3, a.qout->data, 2, dims, strides, box);
+        }
+    }
     if (sc.q_i8) {
         g3.q_out_i8 = static_cast<int8_t*>(a.qout->data);
         g3.q_scale = static_cast<float*>(a.qscale->data);
-        e = launch_gemm<512, 1, 4, EPI_QN>(p.g3.grid, st, mA3, mB3, mB3, g3);
+        e = launch_gemm<512, 1, 4, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr);
     } else {
         g3.q_out_bf16 = static_cast<__nv_bfloat16*>(a.qout->data);
-        e = launch_gemm<256, 1, 8, EPI_QN>(p.g3.grid, st, mA3, mB3, mB3, g3);
+        e = launch_gemm<256, 1, 8, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr);
     }
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k3_absorb_uk");

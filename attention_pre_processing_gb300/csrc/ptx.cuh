@@ -87,6 +87,38 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Tiled TMA store of a shared-memory box to global memory (bulk async group).  Box elements
+// outside the tensor's extent are not written.  x must be 16-byte aligned, x and y >= 0.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N committed bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until every committed bulk group of this thread has completed its global writes.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
+// (TMA stores, tcgen05.mma operands).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Prefetch of one cache line into L2 (a hint: never faults, never waits).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+// Lines of [p, p + bytes) into L2, spread over nthr threads (thread tid of them).
+__device__ __forceinline__ void prefetch_l2_range(const void* p, size_t bytes, int tid, int nthr) {
+    if (p == nullptr) return;
+    const char* c = static_cast<const char*>(p);
+    for (size_t o = (size_t)tid * 128; o < bytes; o += (size_t)nthr * 128) prefetch_l2(c + o);
+}
+
 // Asynchronous prefetch of [p, p + bytes) into L2 (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
