@@ -71,13 +71,9 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// Barrier over the threads that share one row: the whole CTA, or the 128 epilogue threads of
-// the fused decode kernel (named barrier 1).
+// Barrier over the threads that share one row (the whole CTA).
 struct CtaSync {
     __device__ __forceinline__ void operator()() const { __syncthreads(); }
-};
-struct EpiSync {
-    __device__ __forceinline__ void operator()() const { epi_bar(); }
 };
 
 // Deterministic reduction over NT threads (tid in [0, NT)): fixed shuffle tree per warp, then
@@ -102,39 +98,53 @@ __device__ __forceinline__ float group_reduce(float v, float* red, int tid, Sync
 // add the k-range slots of the fp32 row (fixed order), RmsNorm of c^Q and c^KV (epsilon inside
 // the root), "half" RoPE of k^R, the cache writes at cacheIndex[t], and c^Q for the
 // up-projection (bf16, or per-token int8 codes held as bf16 when weightUqQr is int8).
-// ys: Hcq + Hckv + Dr floats of shared memory; red: NT/32 + 1 floats.
+// ys: Hcq + Hckv + Dr floats of shared memory; red: NT/32 + 1 floats; gcq / gckv: the gammas,
+// already staged in shared memory.  Every load that does not depend on the partial sums is
+// issued before them, and a thread's partial loads for up to kRowCols columns are in flight
+// together, so the row costs about one memory latency.
+constexpr int kRowCols = 9;
+
 template <int NT, class Sync>
-__device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, float* ys, float* red, Sync sync) {
+__device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, float* ys, float* red,
+                                         const __nv_bfloat16* gcq, const __nv_bfloat16* gckv, Sync sync) {
     const int ncols = a.Hcq + a.Hckv + a.Dr;
     const int h = a.Dr / 2;
     const long long slot = a.nslots > 0 ? a.cache_index[t] : -1;
-    const float* src = a.src.p + (size_t)t * a.src.ncols;
     const float sx = a.scale_x ? a.scale_x[t] : 1.f;
+    const __nv_bfloat16* rc = a.rope_cos + (size_t)t * a.Dr;
+    const __nv_bfloat16* rs = a.rope_sin + (size_t)t * a.Dr;
+    float cos0 = 0.f, cos1 = 0.f, sin0 = 0.f, sin1 = 0.f;
+    if (tid < h) {
+        cos0 = __bfloat162float(rc[tid]);
+        cos1 = __bfloat162float(rc[tid + h]);
+        sin0 = __bfloat162float(rs[tid]);
+        sin1 = __bfloat162float(rs[tid + h]);
+    }
+    const float* src = a.src.p + (size_t)t * a.src.ncols;
     float sq = 0.f, skv = 0.f;
-    // Four columns per thread per round, every slot load of a round in flight together.
-    for (int c0 = tid; c0 < ncols; c0 += 4 * NT) {
-        float v[4];
+    for (int c0 = tid; c0 < ncols; c0 += kRowCols * NT) {
+        float v[kRowCols];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kRowCols; ++u) {
             const int c = c0 + u * NT;
             v[u] = c < ncols ? __ldcg(src + c) : 0.f;
         }
         for (int k0 = 1; k0 < a.src.slots; k0 += 4) {
-            float w[4][4];
+            float w[4][kRowCols];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < kRowCols; ++u) {
                     const int c = c0 + u * NT;
                     w[k][u] = (k0 + k < a.src.slots && c < ncols) ? __ldcg(src + (k0 + k) * a.src.slot_stride + c) : 0.f;
                 }
 #pragma unroll
             for (int k = 0; k < 4; ++k)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] += w[k][u];
+                for (int u = 0; u < kRowCols; ++u) v[u] += w[k][u];
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kRowCols; ++u) {
             const int c = c0 + u * NT;
             if (c >= ncols) continue;
             float y = v[u];
@@ -153,7 +163,7 @@ __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, floa
     __nv_bfloat16* cq = a.c_q + (size_t)t * a.Hcq;
     if (!a.cq_quant) {
         for (int j = 2 * tid; j < a.Hcq; j += 2 * NT) {
-            const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(a.gamma_cq + j);
+            const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(gcq + j);
             *reinterpret_cast<__nv_bfloat162*>(cq + j) =
                 __floats2bfloat162_rn(__low2float(g2) * ys[j] * inv_q, __high2float(g2) * ys[j + 1] * inv_q);
         }
@@ -161,14 +171,14 @@ __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, floa
         // Per-token dynamic int8 codes of c^Q (times the smooth scales when given).
         float m = 0.f;
         for (int j = tid; j < a.Hcq; j += NT) {
-            float u = __bfloat162float(a.gamma_cq[j]) * ys[j] * inv_q;
+            float u = __bfloat162float(gcq[j]) * ys[j] * inv_q;
             if (a.smooth_cq) u *= a.smooth_cq[j];
             m = fmaxf(m, fabsf(u));
         }
         m = group_reduce<NT, true>(m, red, tid, sync);
         const float scale = m / 127.f;
         for (int j = tid; j < a.Hcq; j += NT) {
-            float u = __bfloat162float(a.gamma_cq[j]) * ys[j] * inv_q;
+            float u = __bfloat162float(gcq[j]) * ys[j] * inv_q;
             if (a.smooth_cq) u *= a.smooth_cq[j];
             const int q = scale > 0.f ? quant_i8(__fdiv_rn(u, scale)) : 0;
             cq[j] = __int2bfloat16_rn(q);
@@ -184,22 +194,25 @@ __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, floa
             if (a.kv_int8) {
                 int8_t* d = reinterpret_cast<int8_t*>(a.kv_cache) + slot * a.Hckv;
                 for (int j = tid; j < a.Hckv; j += NT)
-                    d[j] = (int8_t)quant_i8(__bfloat162float(a.gamma_ckv[j]) * ykv[j] * inv_kv * a.quant_scale_ckv[j]);
+                    d[j] = (int8_t)quant_i8(__bfloat162float(gckv[j]) * ykv[j] * inv_kv * a.quant_scale_ckv[j]);
             } else {
                 __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(a.kv_cache) + slot * a.Hckv;
                 for (int j = 2 * tid; j < a.Hckv; j += 2 * NT) {
-                    const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(a.gamma_ckv + j);
+                    const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(gckv + j);
                     *reinterpret_cast<__nv_bfloat162*>(d + j) =
                         __floats2bfloat162_rn(__low2float(g2) * ykv[j] * inv_kv, __high2float(g2) * ykv[j + 1] * inv_kv);
                 }
             }
             const float* kr = ys + a.Hcq + a.Hckv;
-            const __nv_bfloat16* cs = a.rope_cos + (size_t)t * a.Dr;
-            const __nv_bfloat16* sn = a.rope_sin + (size_t)t * a.Dr;
             for (int j = tid; j < h; j += NT) {
+                const bool pre = j < NT;   // this thread's first pair: tables already in registers
+                const float cj = pre ? cos0 : __bfloat162float(rc[j]);
+                const float ch = pre ? cos1 : __bfloat162float(rc[j + h]);
+                const float sj = pre ? sin0 : __bfloat162float(rs[j]);
+                const float sh = pre ? sin1 : __bfloat162float(rs[j + h]);
                 const float x0 = kr[j], x1 = kr[j + h];
-                const float o0 = x0 * __bfloat162float(cs[j]) - x1 * __bfloat162float(sn[j]);
-                const float o1 = x1 * __bfloat162float(cs[j + h]) + x0 * __bfloat162float(sn[j + h]);
+                const float o0 = x0 * cj - x1 * sj;
+                const float o1 = x1 * ch + x0 * sh;
                 if (a.kr_int8) {
                     int8_t* d = reinterpret_cast<int8_t*>(a.kr_cache) + slot * a.Dr;
                     d[j] = (int8_t)quant_i8(o0 * a.quant_scale_ckr[j]);
@@ -217,8 +230,6 @@ __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, floa
 
 // L2 prefetch of everything the row work of this CTA's tokens reads besides the partials.
 __device__ __forceinline__ void prefetch_down_inputs(const DownArgs& a, int tid, int nthr) {
-    prefetch_l2_range(a.gamma_cq, (size_t)a.Hcq * 2, tid, nthr);
-    prefetch_l2_range(a.gamma_ckv, (size_t)a.Hckv * 2, tid, nthr);
     prefetch_l2_range(a.scale_w_dq, a.scale_w_dq ? (size_t)a.Hcq * 4 : 0, tid, nthr);
     prefetch_l2_range(a.scale_w_dkvkr, a.scale_w_dkvkr ? (size_t)(a.Hckv + a.Dr) * 4 : 0, tid, nthr);
     prefetch_l2_range(a.quant_scale_ckv, a.quant_scale_ckv ? (size_t)a.Hckv * 4 : 0, tid, nthr);
@@ -233,19 +244,33 @@ __device__ __forceinline__ void prefetch_down_inputs(const DownArgs& a, int tid,
     }
 }
 
+// Dynamic shared memory of finalize_down_kernel: the fp32 row, then the two gammas.
+__host__ __device__ inline size_t down_smem_bytes(int Hcq, int Hckv, int Dr) {
+    return (((size_t)(Hcq + Hckv + Dr) * 4 + 15) & ~(size_t)15) + (size_t)(Hcq + Hckv) * 2;
+}
+
 // One CTA per token (grid-stride).
 __global__ void __launch_bounds__(kRowThreads) finalize_down_kernel(const DownArgs a) {
-    extern __shared__ float ys[];   // Hcq + Hckv + Dr
+    extern __shared__ __align__(16) uint8_t fsm[];
+    float* ys = reinterpret_cast<float*>(fsm);
+    __nv_bfloat16* gcq = reinterpret_cast<__nv_bfloat16*>(fsm + (((size_t)(a.Hcq + a.Hckv + a.Dr) * 4 + 15) & ~(size_t)15));
+    __nv_bfloat16* gckv = gcq + a.Hcq;
     __shared__ float red[kRowThreads / 32 + 1];
     // All CTAs of this grid are resident once every one has passed here: the next kernel may
     // start its prologue (and its first weight loads) now.
     pdl_launch_dependents();
-    // The small inputs do not depend on the previous kernel: request them into L2 while it
-    // finishes, so that the row work does not wait on cold lines behind the weight stream.
+    // The gammas and the other small inputs do not depend on the previous kernel: stage and
+    // prefetch them while it finishes, so that the row work does not wait on cold lines.
+    // (Hcq and Hckv are multiples of 8: 16-byte copies.)
+    for (int i = threadIdx.x; i < a.Hcq / 8; i += kRowThreads)
+        reinterpret_cast<uint4*>(gcq)[i] = reinterpret_cast<const uint4*>(a.gamma_cq)[i];
+    for (int i = threadIdx.x; i < a.Hckv / 8; i += kRowThreads)
+        reinterpret_cast<uint4*>(gckv)[i] = reinterpret_cast<const uint4*>(a.gamma_ckv)[i];
     prefetch_down_inputs(a, threadIdx.x, kRowThreads);
     pdl_wait();
+    __syncthreads();
     for (int t = blockIdx.x; t < a.T; t += gridDim.x)
-        down_row<kRowThreads>(a, t, threadIdx.x, ys, red, CtaSync{});
+        down_row<kRowThreads>(a, t, threadIdx.x, ys, red, gcq, gckv, CtaSync{});
 }
 
 struct UpArgs {

@@ -50,6 +50,8 @@ struct GemmArgs {
     int head_mode;       // A and B are per-head 3D maps (W^UK contraction)
     int tiles_per_head;  // EPI_QN
     int clear_status;    // block 0 zeroes *status once earlier grids have finished
+    int a_ready;         // A is a caller input (not written by an earlier kernel of the call):
+                         // its tiles may be requested before the grid dependency resolves
     int a_box_rows;      // rows of one A TMA box (multiple of 8, <= 128)
     int stages;          // ring depth actually used (<= MAXST)
     // EPI_F32: ksplit slots of T x ncols row-major fp32
@@ -557,14 +559,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int i = 0; i < pre; ++i) {
                     const uint32_t fb = smem_u32(&full[i]);
                     mbar_arrive_expect_tx(fb, (uint32_t)(a_stage + C::kBStage));
+                    if (args.a_ready)   // stage i complete as early as possible
+                        load_a<MSUB>(args, u0, u0.kb0 + i, smem_u32(sA + (size_t)i * a_stage), a_box, fb, &map_a,
+                                     pol_a);
                     load_b<BN>(args, u0, u0.kb0 + i, smem_u32(sB + (size_t)i * C::kBStage), fb, &map_b0, &map_b1,
                                pol_w);
                 }
             }
             pdl_wait();
-            for (int i = 0; i < pre; ++i)
-                load_a<MSUB>(args, u0, u0.kb0 + i, smem_u32(sA + (size_t)i * a_stage), a_box,
-                             smem_u32(&full[i]), &map_a, pol_a);
+            if (!args.a_ready)
+                for (int i = 0; i < pre; ++i)
+                    load_a<MSUB>(args, u0, u0.kb0 + i, smem_u32(sA + (size_t)i * a_stage), a_box,
+                                 smem_u32(&full[i]), &map_a, pol_a);
             s = pre % stages;
             ph = (pre == stages) ? 1u : 0u;
             for (int idx = 0; ok && get_unit(args, idx, u); ++idx) {

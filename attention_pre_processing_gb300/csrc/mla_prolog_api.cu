@@ -20,7 +20,6 @@
 #include <random>
 
 #include "mla_prolog.h"
-#include "decode_fused.cuh"
 #include "finalize.cuh"
 #include "gemm_tc.cuh"
 
@@ -226,20 +225,14 @@ struct GemmPlan {
 
 struct Plan {
     GemmPlan g1, g2, g3;
-    bool fused = false;      // decode-sized: the one persistent kernel of decode_fused.cuh
-    int fused_ra = 0, fused_rb = 0, fused_s1 = 1, fused_nt1 = 0;
-    size_t fused_smem = 0;
     bool g2_fused = false;   // K2 epilogue does RoPE and q^C (no finalize_up)
     int64_t ncols1 = 0, ncols2 = 0;
     size_t off_cq = 0, off_cqs = 0, off_qc = 0, off_y1 = 0, off_y2 = 0, off_xb = 0, off_wdq = 0, off_wdkvkr = 0,
-           off_wuqqr = 0, off_flags = 0, bytes = 0;
+           off_wuqqr = 0, bytes = 0;
 };
 
 constexpr size_t kStatusBytes = 1024;
 constexpr int kDecodeRows = 256;   // up to this many tokens: one row tile, weight streaming
-// The single persistent decode kernel is correct but slower than the four-launch path on
-// GB300 (its per-SM weight stream stalls behind MMA issue), so it is built but not planned.
-constexpr bool kFusedDecode = false;
 
 size_t up1024(size_t v) { return (v + 1023) & ~size_t(1023); }
 
@@ -300,32 +293,6 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
         p.g3.grid = (int)(tiles < sms ? tiles : sms);
     }
 
-    // One persistent kernel for decode-sized T with the 128 + 64 head layout, when every head
-    // and every down-projection tile gets its own CTA.
-    {
-        const int nt1 = (int)((p.ncols1 + 63) / 64);
-        const int a_bytes = (int)((T + 7) / 8 * 8) * 128;
-        int ra = 32768 / a_bytes;
-        ra = ra < 2 ? 2 : (ra > kFusedMaxA ? kFusedMaxA : ra);
-        const size_t fixed = fused_smem_bytes((int)p.ncols1, a_bytes, ra, 0);
-        int rb = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kBox) : 0;
-        if (rb > kFusedMaxB) rb = kFusedMaxB;
-        if (kFusedDecode && T <= 128 && d.D == 128 && d.Dr == 64 && d.Hckv <= 512 && d.Hckv % 64 == 0 && d.N <= sms &&
-            nt1 <= sms && rb >= 8 && d.Hcq % 64 == 0) {
-            p.fused = true;
-            p.fused_nt1 = nt1;
-            int s1 = sms / nt1;
-            const int kb1 = (int)((d.He + 63) / 64);
-            if (s1 > kb1) s1 = kb1;
-            if (s1 > 16) s1 = 16;
-            p.fused_s1 = s1 < 1 ? 1 : s1;
-            p.fused_ra = ra;
-            p.fused_rb = rb;
-            p.fused_smem = fused_smem_bytes((int)p.ncols1, a_bytes, ra, rb);
-            p.g1.ksplit = p.fused_s1;
-        }
-    }
-
     size_t off = kStatusBytes;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -343,19 +310,8 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
         p.off_wdkvkr = take((size_t)d.He * (d.Hckv + d.Dr) * 2);
     }
     if (sc.uqqr_i8) p.off_wuqqr = take((size_t)d.Hcq * p.ncols2 * 2);
-    p.off_flags = take((size_t)2 * sms * 8 + (size_t)2 * sms * kDoneStride * 8);
     p.bytes = off;
     return p;
-}
-
-// A unique 48-bit tag per call for the fused kernel's barrier flags.  It starts at a random value
-// so that flags left in a reused workspace never match by accident.
-unsigned long long next_tag() {
-    static std::atomic<unsigned long long> ctr{[] {
-        std::random_device rd;
-        return ((unsigned long long)rd() << 20) ^ (unsigned long long)rd();
-    }()};
-    return (ctr.fetch_add(1) + 1) & 0xFFFFFFFFFFFFull;
 }
 
 // --------------------------------------------------------------- tensor maps
@@ -580,7 +536,7 @@ mla_status run(const Launched& L) {
 
     // The 3D map of q^C (one head's T x D slice per box) and of W^UK (one head's D x Hckv).
     CUtensorMap mA3, mB3;
-    const uint32_t a3_rows = (uint32_t)(p.fused ? (d.T + 7) / 8 * 8 : p.g3.a_box_rows);
+    const uint32_t a3_rows = (uint32_t)p.g3.a_box_rows;
     {
         const uint64_t dims[3] = {(uint64_t)d.D, (uint64_t)d.N, (uint64_t)d.T};
         const uint64_t strides[2] = {(uint64_t)d.D * 2, (uint64_t)d.N * d.D * 2};
@@ -592,76 +548,6 @@ mla_status run(const Launched& L) {
         if (!encode_map(&mB3, a.wuk->data, 3, dimsb, stridesb, boxb)) return MLA_ERR_RUNTIME;
     }
 
-    if (p.fused) {
-        // ---- the whole prolog in one persistent kernel
-        const uint32_t rows = (uint32_t)((d.T + 7) / 8 * 8);
-        CUtensorMap mx, mwdq, mwdkvkr, mcq, mwuqqr;
-        if (!map_2d(&mx, x_bf, d.T, d.He, rows) || !map_2d(&mwdq, wdq_bf, d.He, d.Hcq, 64) ||
-            !map_2d(&mwdkvkr, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64) || !map_2d(&mcq, ws + p.off_cq, d.T, d.Hcq, rows) ||
-            !map_2d(&mwuqqr, wuqqr_bf, d.Hcq, p.ncols2, 64))
-            return MLA_ERR_RUNTIME;
-        FusedArgs fa = {};
-        fa.T = T;
-        fa.a_bytes = (int)rows * 128;
-        fa.ra = p.fused_ra;
-        fa.rb = p.fused_rb;
-        fa.x = static_cast<const __nv_bfloat16*>(x_bf);
-        fa.ncols_x = (int)d.He;
-        fa.nt1 = p.fused_nt1;
-        fa.s1 = p.fused_s1;
-        fa.kb1 = (int)((d.He + 63) / 64);
-        fa.hcq = (int)d.Hcq;
-        fa.ncols1 = (int)p.ncols1;
-        fa.y1 = y1;
-        fa.down = f1;
-        fa.ep.T = T;
-        fa.ep.N = (int)d.N;
-        fa.ep.q_c = qc;
-        fa.ep.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
-        fa.ep.rope_cos = f1.rope_cos;
-        fa.ep.rope_sin = f1.rope_sin;
-        fa.ep.row_scale = row_scale;
-        fa.ep.col_scale = col_scale;
-        fa.ep.Hckv = (int)d.Hckv;
-        fa.ep.tiles_per_head = 1;
-        fa.ep.status = status;
-        if (sc.q_i8) {
-            fa.ep.q_out_i8 = static_cast<int8_t*>(a.qout->data);
-            fa.ep.q_scale = static_cast<float*>(a.qscale->data);
-        } else {
-            fa.ep.q_out_bf16 = static_cast<__nv_bfloat16*>(a.qout->data);
-        }
-        fa.N = (int)d.N;
-        fa.kb2 = (int)((d.Hcq + 63) / 64);
-        fa.kb4 = (int)((d.D + 63) / 64);
-        fa.nbox4 = (int)(d.Hckv / 64);
-        fa.arrive_flags = reinterpret_cast<unsigned long long*>(ws + p.off_flags);
-        fa.done_flags = fa.arrive_flags + 2 * L.sms;
-        fa.tag = next_tag();
-        fa.status = status;
-        e = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.fused_smem);
-        if (e != cudaSuccess) return MLA_ERR_RUNTIME;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)L.sms);
-        cfg.blockDim = dim3((unsigned)kFusedThreads);
-        cfg.dynamicSmemBytes = p.fused_smem;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: the grid barriers need it
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, mx, mwdq, mwdkvkr, mcq, mwuqqr, mB3, fa);
-        if (e == cudaSuccess) {
-            timing_mark(st, "decode_fused");
-            if (g_timing.enabled) g_timing.have = true;
-            return MLA_OK;
-        }
-        // Not all CTAs can be resident (the device is shared): run the kernel-per-step path.
-        if (e != cudaErrorCooperativeLaunchTooLarge) return MLA_ERR_RUNTIME;
-        (void)cudaGetLastError();
-    }
-
     // ---- K1: down-projection x . [W^DQ | W^DKV | W^KR] -> fp32 rows Y1
     CUtensorMap mA1, mB1a, mB1b;
     if (!map_2d(&mA1, x_bf, d.T, d.He, (uint32_t)p.g1.a_box_rows) || !map_2d(&mB1a, wdq_bf, d.He, d.Hcq, 64) ||
@@ -670,6 +556,7 @@ mla_status run(const Launched& L) {
     GemmArgs g1 = gemm_args(p.g1, T, p.ncols1, status);
     g1.b_split_col = (int)d.Hcq;
     g1.clear_status = 1;
+    g1.a_ready = sc.x_i8 ? 0 : 1;   // bf16 tokenX is read as passed; int8 is widened first
     g1.out_f32 = y1;
     if (p.g1.bn == 64)
         e = launch_gemm<64, 1, 32, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
@@ -681,7 +568,10 @@ mla_status run(const Launched& L) {
     // ---- F1: RmsNorm, RoPE(k^R), cache writes, c^Q
     {
         const int grid = T < 16 * L.sms ? T : 16 * L.sms;
-        e = launch(finalize_down_kernel, grid, kRowThreads, (size_t)p.ncols1 * 4, st, f1);
+        const size_t fsmem = down_smem_bytes((int)d.Hcq, (int)d.Hckv, (int)d.Dr);
+        e = cudaFuncSetAttribute(finalize_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
+        if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+        e = launch(finalize_down_kernel, grid, kRowThreads, fsmem, st, f1);
         if (e != cudaSuccess) return MLA_ERR_RUNTIME;
         timing_mark(st, "f1_norm_rope_cache");
     }
