@@ -1,0 +1,712 @@
+// The whole bf16 prolog for decode-sized token counts in ONE persistent kernel: one CTA per SM,
+// all CTAs co-resident (cooperative launch).  Every CTA streams its weights through one ring of
+// 24 KB stages (three 64 x 64 boxes) from the first to the last phase, so HBM never waits for a
+// kernel boundary; only the tensor-core work waits for the two grid barriers.
+//
+//   P1   x . [W^DQ | W^DkvKr]: 192-column tiles x s1 k ranges, one unit per CTA, fp32 products
+//        into slot k-range of a s1 x T x ncols1 buffer
+//   R    once the s1 CTAs of its tile have stored their products: the k-range slots added in
+//        fixed order, one 16-column chunk per CTA: for c^Q columns bf16(gamma * y) (the A
+//        operand of P3) and the chunk's sum of y^2 per token; for c^KV and k^R columns the fp32
+//        y (the RmsNorm scale needs every chunk of the row)
+//   P3   head n = CTA index, each k-block as soon as its four chunks are reduced:
+//        (gamma * y) . W^UqQr[:, head n]; the epilogue multiplies by the
+//        token's 1 / RMS (from the chunk sums), applies RoPE to the rope columns
+//        (queryRopeOut) and writes q^C straight into shared memory as P4's A operand
+//   P4   q^C . W^UK[n] (512 columns) -> queryOut through TMA stores
+//   KV   CTAs without a head: RmsNorm of c^KV and RoPE of k^R, written to the caches at
+//        cacheIndex
+//
+// RmsNorm(y) . W = (1 / RMS(y)) * ((gamma * y) . W): the per-token scale moves behind the
+// contraction, so no row pass sits between the reduction and P3.
+//
+// Cross-CTA dependencies are flags, not grid barriers: every producer of data (a P1 unit, a
+// reduced chunk) stores the call's tag in its own 8-byte flag after its data, and each
+// consumer waits for exactly the flags it reads.  Flags from another call carry another tag,
+// so the workspace needs no initialisation.
+//
+// Roles (256 threads): warp 0 streams weight stages with TMA; warp 1 allocates tensor memory
+// and issues tcgen05.mma; warp 2 loads P1's activation tiles (x) with TMA; warp 3 is idle;
+// warps 4..7 run the epilogues, the reduction, the cache rows, and load P3's
+// activation tiles (c^Q) with ordinary loads: a TMA load queues behind the weight stages the
+// SM has in flight, which would hold every P3 step for an HBM round trip.  Every wait is
+// bounded: a wait that gives up sets MLA_DEV_WAIT_TIMEOUT, the other roles stop at their next
+// wait, tensor memory is freed and the kernel returns.
+
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "gemm_tc.cuh"
+#include "ptx.cuh"
+
+namespace mla {
+
+constexpr int kPThreads = 256;
+constexpr int kPBox = 8192;                  // one 64 x 64 bf16 weight box
+constexpr int kPStage = 3 * kPBox;           // one weight stage: up to 192 columns
+constexpr int kPMaxW = 12;                   // weight stages at most
+constexpr int kPA = 4;                       // P1 activation slots (TMA)
+constexpr int kPA3 = 8;                      // P3 activation slots (loaded by the epilogue warps)
+constexpr int kPChunk = 16;                  // columns per reduction chunk
+constexpr int kPMaxT = 64;                   // tokens at most
+constexpr int kPMaxS = 16;                   // k ranges at most
+
+struct PersistArgs {
+    int T, a_rows, a_bytes, wst;        // tokens, A box rows, A slot bytes, weight stages
+    // P1
+    int hcq, hckv, dr, ncols1, n1, s1, kb1;
+    float* y1;                          // s1 x T x ncols1
+    // R
+    const __nv_bfloat16* gamma_cq;
+    const __nv_bfloat16* gamma_ckv;
+    __nv_bfloat16* cq;                  // T x Hcq: bf16(gamma_cq * y)
+    float* ss;                          // (Hcq + Hckv) / 16 chunks x T
+    float* ykv;                         // T x (Hckv + Dr)
+    float eps_cq, eps_ckv;
+    // KV
+    const long long* cache_index;
+    long long nslots;
+    __nv_bfloat16* kv_cache;
+    __nv_bfloat16* kr_cache;
+    const __nv_bfloat16* rope_cos;      // (T, Dr)
+    const __nv_bfloat16* rope_sin;
+    // P3 / P4
+    int N, kb2;                         // heads, k-blocks of Hcq
+    __nv_bfloat16* q_rope;              // T x N x 64
+    __nv_bfloat16* q_out;               // T x N x 512
+    // dependency flags
+    unsigned long long* p1flags;        // gridDim.x: P1 product stored
+    unsigned long long* cflags;         // ncols1 / 16: chunk reduced
+    unsigned long long tag;             // unique per call
+    uint32_t* status;
+};
+
+// One weight stage of this CTA's sequence: P1 k-blocks, then P3 k-blocks, then P4 groups.
+struct PStep {
+    int phase;    // 1, 3, 4
+    int kb;       // k-block
+    int g;        // P4: column group (0: 0..191, 1: 192..383, 2: 384..511)
+    int nbox;     // boxes in the stage
+    bool first;   // overwrite the accumulator
+    bool last;    // last stage of the phase: commit the accumulator
+};
+
+__device__ __forceinline__ int p1_range(const PersistArgs& a, int* tile, int* ks, int* kb0) {
+    const int u = blockIdx.x;
+    if (u >= a.n1 * a.s1) return 0;
+    *tile = u % a.n1;
+    *ks = u / a.n1;
+    *kb0 = *ks * a.kb1 / a.s1;
+    return (*ks + 1) * a.kb1 / a.s1 - *kb0;
+}
+
+__device__ __forceinline__ bool p_step(const PersistArgs& a, int i, int n1s, PStep& s) {
+    if (i < n1s) {
+        s = {1, i, 0, 3, i == 0, i == n1s - 1};
+        return true;
+    }
+    i -= n1s;
+    if ((int)blockIdx.x >= a.N) return false;
+    if (i < a.kb2) {
+        s = {3, i, 0, 3, i == 0, i == a.kb2 - 1};
+        return true;
+    }
+    i -= a.kb2;
+    if (i < 6) {   // D = 128: two k-blocks x three column groups
+        const int kb = i / 3, g = i % 3;
+        s = {4, kb, g, g == 2 ? 2 : 3, kb == 0, i == 5};
+        return true;
+    }
+    return false;
+}
+
+// ------------------------------------------------------------------ dependency flags
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits (bounded) until flags f[0], f[stride], ..., f[(n-1) * stride] all hold `tag`.  Called
+// by all 128 epilogue threads together: thread i polls flags i, i + 128, ... so that every
+// flag's round trip overlaps; the result is combined over the 128 threads (every thread gets
+// the same answer), and the named barrier orders every thread's later loads after the flags.
+__device__ __forceinline__ bool wait_flags(const unsigned long long* f, int n, int stride, unsigned long long tag,
+                                           const volatile int* abort, int etid) {
+    bool ok = true;
+    const uint64_t t0 = global_timer_ns();
+    for (int i = etid; ok && i < n; i += 128) {
+        while (ld_acquire_u64(f + (size_t)i * stride) != tag) {
+            if (*abort || global_timer_ns() - t0 > kWaitLimitNs) {
+                ok = false;
+                break;
+            }
+            __nanosleep(32);
+        }
+    }
+    const bool bad = epi_any(!ok);
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    return !bad;
+}
+
+// ------------------------------------------------------------------ helpers
+
+// 32 values of row `row` (columns col0..col0+31 of a head's q^C) -> bf16 into the K-major,
+// 128-byte-swizzled A operand of P4: k-block col/64 at slot base + kb * slot_bytes.
+__device__ __forceinline__ void chain_store(uint32_t base, int slot_bytes, int row, int col0, const float (&v)[32]) {
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+        const int d = col0 + c8 * 8;
+        const uint32_t addr =
+            base + (uint32_t)((d >> 6) * slot_bytes + row * 128 + ((((d & 63) >> 3) ^ (row & 7)) << 4));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pack_bf16(v[8 * c8], v[8 * c8 + 1])),
+                     "r"(pack_bf16(v[8 * c8 + 2], v[8 * c8 + 3])), "r"(pack_bf16(v[8 * c8 + 4], v[8 * c8 + 5])),
+                     "r"(pack_bf16(v[8 * c8 + 6], v[8 * c8 + 7]))
+                     : "memory");
+    }
+}
+
+// P3's activation tiles: c^Q k-blocks of T rows x 128 bytes in the 128-byte-swizzled K-major
+// layout, loaded by the 128 epilogue threads with ordinary 16-byte loads into the kPA3-slot
+// ring (so they never queue behind weight stages in the TMA engine).  The first batch fills
+// the ring; later batches of four follow as the tensor core frees slots.  Every load of a batch
+// is in flight together.  UPT: 16-byte chunks per thread and tile (T <= 16 * UPT).
+template <int FIRST, int UPT>
+__device__ __forceinline__ bool load_cq_tiles(const PersistArgs& a, uint8_t* ring, uint64_t* full, uint64_t* empty,
+                                              const volatile int* abort, int etid) {
+    const int chunks = a.T * 8;
+    int sa = 0;
+    uint32_t ph = 0;
+    for (int kb0 = 0; kb0 < a.kb2;) {
+        const int want = kb0 == 0 ? FIRST : 4;
+        const int nb = a.kb2 - kb0 < want ? a.kb2 - kb0 : want;
+        // One thread waits for the batch's slots; the others block at the named barrier (a
+        // spinning warp would take issue slots from the MMA warp on its scheduler).
+        bool ok = true;
+        if (etid == 0) {
+            int s2 = sa;
+            uint32_t p2 = ph;
+            for (int k = 0; k < nb && ok; ++k) {
+                ok = mbar_wait(smem_u32(&empty[s2]), p2 ^ 1, abort, kWaitLimitNs);
+                if (++s2 == kPA3) {
+                    s2 = 0;
+                    p2 ^= 1;
+                }
+            }
+        }
+        if (epi_any(!ok)) return false;   // all 128 threads leave together
+        uint4 v[FIRST][UPT];
+#pragma unroll
+        for (int k = 0; k < FIRST; ++k)
+#pragma unroll
+            for (int u = 0; u < UPT; ++u) {
+                const int c = etid + 128 * u;
+                v[k][u] = make_uint4(0, 0, 0, 0);
+                if (k < nb && c < chunks)
+                    v[k][u] = __ldcg(reinterpret_cast<const uint4*>(a.cq + (size_t)(c >> 3) * a.hcq + (kb0 + k) * 64 +
+                                                                   (c & 7) * 8));
+            }
+        int s3 = sa;
+#pragma unroll
+        for (int k = 0; k < FIRST; ++k) {
+            if (k >= nb) break;
+            const uint32_t slot = smem_u32(ring + (size_t)s3 * a.a_bytes);
+#pragma unroll
+            for (int u = 0; u < UPT; ++u) {
+                const int c = etid + 128 * u;
+                if (c < chunks) {
+                    const int r = c >> 3, ch = c & 7;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     slot + (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4))),
+                                 "r"(v[k][u].x), "r"(v[k][u].y), "r"(v[k][u].z), "r"(v[k][u].w)
+                                 : "memory");
+                }
+            }
+            if (++s3 == kPA3) s3 = 0;
+        }
+        // One proxy fence for the whole batch (generic writes -> tensor-core reads): the fence
+        // waits on the SM's busy async proxy, so one per tile would pace the tiles.
+        fence_proxy_async_smem();
+        for (int k = 0; k < nb; ++k) {
+            mbar_arrive(smem_u32(&full[sa]));
+            if (++sa == kPA3) {
+                sa = 0;
+                ph ^= 1;
+            }
+        }
+        kb0 += nb;
+    }
+    return true;
+}
+
+// Alignment slack, barriers and a 1 KB scratch, the activation region (P1's TMA ring, later
+// P3's ring, later P4's A operand) and the weight ring.
+__host__ __device__ inline size_t persist_smem_bytes(int a_bytes, int wst) {
+    return 1024 + 2048 + (size_t)kPA3 * a_bytes + (size_t)wst * kPStage;
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    decode_persist_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wdq,
+                          const __grid_constant__ CUtensorMap map_wdkvkr, const __grid_constant__ CUtensorMap map_cq,
+                          const __grid_constant__ CUtensorMap map_wuqqr, const __grid_constant__ CUtensorMap map_wuk,
+                          const __grid_constant__ CUtensorMap map_o, const PersistArgs args) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* wfull = bars;                       // [kPMaxW]
+    uint64_t* wempty = wfull + kPMaxW;            // [kPMaxW]
+    uint64_t* afull = wempty + kPMaxW;            // [kPA]
+    uint64_t* aempty = afull + kPA;               // [kPA]
+    uint64_t* afull3 = aempty + kPA;              // [kPA3]
+    uint64_t* aempty3 = afull3 + kPA3;            // [kPA3]
+    uint64_t* tfull = aempty3 + kPA3;             // [3]: P1, P3, P4 accumulators
+    uint64_t* chain_full = tfull + 3;
+    uint64_t* done = chain_full + 1;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    float* ssum = reinterpret_cast<float*>(smem + 1024);   // 4 x 64 partial sums of squares
+    uint8_t* aring = smem + 2048;
+    uint8_t* wring = aring + (size_t)kPA3 * args.a_bytes;
+    const int wst = args.wst;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = gridDim.x;
+    const bool head = (int)blockIdx.x < args.N;
+    int tile = 0, ks = 0, kb0 = 0;
+    const int n1s = p1_range(args, &tile, &ks, &kb0);
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&map_x);
+        tma_prefetch_map(&map_wdq);
+        tma_prefetch_map(&map_wdkvkr);
+        tma_prefetch_map(&map_wuqqr);
+        tma_prefetch_map(&map_wuk);
+        for (int s = 0; s < wst; ++s) {
+            mbar_init(smem_u32(&wfull[s]), 1);
+            mbar_init(smem_u32(&wempty[s]), 1);
+        }
+        for (int s = 0; s < kPA; ++s) {
+            mbar_init(smem_u32(&afull[s]), 1);
+            mbar_init(smem_u32(&aempty[s]), 1);
+        }
+        for (int s = 0; s < kPA3; ++s) {
+            mbar_init(smem_u32(&afull3[s]), 128);
+            mbar_init(smem_u32(&aempty3[s]), 1);
+        }
+        for (int p = 0; p < 3; ++p) mbar_init(smem_u32(&tfull[p]), 1);
+        mbar_init(smem_u32(chain_full), 128);
+        mbar_init(smem_u32(done), 1);
+        *s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(s_tmem), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    if (blockIdx.x == 0 && threadIdx.x == 32) *args.status = 0u;
+
+    auto fail = [&]() {
+        *s_abort = 1;
+        atomicOr(args.status, kStatusWaitTimeout);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ weight stream
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int s = 0;
+            uint32_t ph = 0;
+            PStep st;
+            for (int i = 0; p_step(args, i, n1s, st); ++i) {
+                if (!mbar_wait(smem_u32(&wempty[s]), ph ^ 1, s_abort, kWaitLimitNs)) {
+                    fail();
+                    break;
+                }
+                const uint32_t fb = smem_u32(&wfull[s]);
+                const uint32_t dst = smem_u32(wring + (size_t)s * kPStage);
+                mbar_arrive_expect_tx(fb, (uint32_t)(st.nbox * kPBox));
+                for (int j = 0; j < st.nbox; ++j) {
+                    if (st.phase == 1) {
+                        const int col = tile * 192 + 64 * j;
+                        if (col < args.hcq)
+                            tma_load_2d(dst + j * kPBox, &map_wdq, fb, col, (kb0 + st.kb) * 64, pol);
+                        else
+                            tma_load_2d(dst + j * kPBox, &map_wdkvkr, fb, col - args.hcq, (kb0 + st.kb) * 64, pol);
+                    } else if (st.phase == 3) {
+                        tma_load_2d(dst + j * kPBox, &map_wuqqr, fb, (int)blockIdx.x * 192 + 64 * j, st.kb * 64, pol);
+                    } else {
+                        tma_load_3d(dst + j * kPBox, &map_wuk, fb, st.g * 192 + 64 * j, st.kb * 64, (int)blockIdx.x,
+                                    pol);
+                    }
+                }
+                if (++s == wst) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id192 = idesc_bf16_f32(128, 192, false, true);
+            constexpr uint32_t id128 = idesc_bf16_f32(128, 128, false, true);
+            int sw = 0, sa = 0, sa3 = 0;
+            uint32_t phw = 0, pha = 0, pha3 = 0;
+            bool ok = true;
+            PStep st;
+            for (int i = 0; ok && p_step(args, i, n1s, st); ++i) {
+                uint32_t a_base;
+                if (st.phase == 4) {
+                    if (st.first && st.g == 0 && !mbar_wait(smem_u32(chain_full), 0, s_abort, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    a_base = smem_u32(aring + (size_t)st.kb * args.a_bytes);
+                } else if (st.phase == 3) {
+                    if (!mbar_wait(smem_u32(&afull3[sa3]), pha3, s_abort, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    a_base = smem_u32(aring + (size_t)sa3 * args.a_bytes);
+                } else {
+                    if (!mbar_wait(smem_u32(&afull[sa]), pha, s_abort, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    a_base = smem_u32(aring + (size_t)sa * args.a_bytes);
+                }
+                if (!mbar_wait(smem_u32(&wfull[sw]), phw, s_abort, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t b_base = smem_u32(wring + (size_t)sw * kPStage);
+                const uint32_t d = tmem_base + (st.phase == 1 ? 256u : 0u) + (st.phase == 4 ? (uint32_t)(st.g * 192) : 0u);
+                const uint32_t idesc = st.nbox == 3 ? id192 : id128;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16(d, smem_desc_sw128(a_base + kk * 32, 16, 1024),
+                              smem_desc_sw128(b_base + kk * 16 * 128, kPBox, 1024), idesc,
+                              (st.first && kk == 0) ? 0u : 1u);
+                umma_commit(smem_u32(&wempty[sw]));
+                if (++sw == wst) {
+                    sw = 0;
+                    phw ^= 1;
+                }
+                if (st.phase == 1) {
+                    umma_commit(smem_u32(&aempty[sa]));
+                    if (++sa == kPA) {
+                        sa = 0;
+                        pha ^= 1;
+                    }
+                } else if (st.phase == 3) {
+                    umma_commit(smem_u32(&aempty3[sa3]));
+                    if (++sa3 == kPA3) {
+                        sa3 = 0;
+                        pha3 ^= 1;
+                    }
+                }
+                if (st.last) umma_commit(smem_u32(&tfull[st.phase == 1 ? 0 : (st.phase == 3 ? 1 : 2)]));
+            }
+            if (!ok) fail();
+            umma_commit(smem_u32(done));
+            mbar_wait(smem_u32(done), 0, s_abort, kWaitLimitNs / 4);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ activation tiles
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            int sa = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            auto put = [&](const CUtensorMap* map, int kb) -> bool {
+                if (!mbar_wait(smem_u32(&aempty[sa]), ph ^ 1, s_abort, kWaitLimitNs)) return false;
+                const uint32_t fb = smem_u32(&afull[sa]);
+                mbar_arrive_expect_tx(fb, (uint32_t)args.a_bytes);
+                tma_load_2d(smem_u32(aring + (size_t)sa * args.a_bytes), map, fb, kb * 64, 0, pol);
+                if (++sa == kPA) {
+                    sa = 0;
+                    ph ^= 1;
+                }
+                return true;
+            };
+            for (int i = 0; ok && i < n1s; ++i) ok = put(&map_x, kb0 + i);
+            if (!ok) fail();
+        }
+    } else if (warp == 3) {
+        // idle
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int etid = threadIdx.x - 128;   // 0..127
+        const int q = warp & 3;               // TMEM lane quarter
+        const int row = q * 32 + lane;
+        const int T = args.T;
+        bool ok = true;
+        auto acc_ready = [&](int p) -> bool {
+            int r = 1;
+            if (lane == 0) r = mbar_wait(smem_u32(&tfull[p]), 0, s_abort, kWaitLimitNs) ? 1 : 0;
+            r = __shfl_sync(0xffffffffu, r, 0);
+            __syncwarp();
+            tc_fence_after();
+            return r != 0;
+        };
+        // The epilogue threads' stores so far become visible, then the flag says so.
+        auto publish = [&](unsigned long long* flag) {
+            __threadfence();
+            epi_bar();
+            if (etid == 0) asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flag), "l"(args.tag) : "memory");
+        };
+
+        // ---- P1: this CTA's k-range product of one 192-column tile -> slot ks
+        if (n1s > 0) {
+            ok = acc_ready(0);
+            if (ok && q * 32 < T) {
+                float* dst = args.y1 + ((size_t)ks * T + row) * args.ncols1 + tile * 192;
+#pragma unroll 1
+                for (int ch = 0; ch < 6; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + 256 + ch * 32, r);
+                    tmem_ld_wait();
+                    if (row < T) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            reinterpret_cast<float4*>(dst + ch * 32)[i] =
+                                make_float4(bits_f(r[4 * i]), bits_f(r[4 * i + 1]), bits_f(r[4 * i + 2]), bits_f(r[4 * i + 3]));
+                    }
+                }
+            }
+        }
+        if (!ok) fail();
+        ok = !epi_any(!ok);   // uniform over the 128 threads: the flag waits below are collective
+        if (n1s > 0) publish(args.p1flags + blockIdx.x);
+
+        // ---- R: the k-range sum of one 16-column chunk, once its tile's s1 units are stored
+        const int nchunks = args.ncols1 / kPChunk;
+        if (ok && (int)blockIdx.x < nchunks) {
+            const int rtile = (int)blockIdx.x / (192 / kPChunk);
+            ok = wait_flags(args.p1flags + rtile, args.s1, args.n1, args.tag, s_abort, etid);
+        }
+        if (ok && (int)blockIdx.x < nchunks) {
+            const int col0 = (int)blockIdx.x * kPChunk;
+            const int cg = etid & 3;
+            const int col = col0 + 4 * cg;
+            const size_t slot_stride = (size_t)T * args.ncols1;
+            // Rows in rounds of 32; every lane runs every round (the shuffles need the whole
+            // warp), rows at or past T only skip their loads and stores.
+            for (int r0 = 0; r0 < T; r0 += 32) {
+                const int r = r0 + (etid >> 2);
+                const bool valid = r < T;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (valid) {
+                    float4 w[kPMaxS];
+#pragma unroll
+                    for (int k = 0; k < kPMaxS; ++k)
+                        if (k < args.s1)
+                            w[k] = __ldcg(reinterpret_cast<const float4*>(args.y1 + k * slot_stride + (size_t)r * args.ncols1 + col));
+                    v = w[0];
+#pragma unroll
+                    for (int k = 1; k < kPMaxS; ++k)
+                        if (k < args.s1) {
+                            v.x += w[k].x;
+                            v.y += w[k].y;
+                            v.z += w[k].z;
+                            v.w += w[k].w;
+                        }
+                }
+                float s2 = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+                s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+                if (!valid) continue;
+                if (col0 < args.hcq + args.hckv && cg == 0) args.ss[(size_t)blockIdx.x * T + r] = s2;
+                if (col0 < args.hcq) {
+                    const uint2 g = *reinterpret_cast<const uint2*>(args.gamma_cq + col);
+                    uint2 o;
+                    o.x = pack_bf16(bf16_lo(g.x) * v.x, bf16_hi(g.x) * v.y);
+                    o.y = pack_bf16(bf16_lo(g.y) * v.z, bf16_hi(g.y) * v.w);
+                    *reinterpret_cast<uint2*>(args.cq + (size_t)r * args.hcq + col) = o;
+                } else {
+                    *reinterpret_cast<float4*>(args.ykv + (size_t)r * (args.hckv + args.dr) + (col - args.hcq)) = v;
+                }
+            }
+        }
+        if ((int)blockIdx.x < nchunks) publish(args.cflags + blockIdx.x);
+
+        if (ok && head) {
+            // Every c^Q chunk is reduced (one collective wait for all of them) ...
+            ok = wait_flags(args.cflags, args.hcq / kPChunk, 1, args.tag, s_abort, etid);
+            // ... then the P3 activation tiles, with ordinary loads, the first batch filling the
+            // whole ring ...
+            if (ok) {
+                if (T <= 32)
+                    ok = load_cq_tiles<8, 2>(args, aring, afull3, aempty3, s_abort, etid);
+                else
+                    ok = load_cq_tiles<4, 4>(args, aring, afull3, aempty3, s_abort, etid);
+            }
+            // ... and each row's 1 / RMS: the 128 threads split the chunk sums (a fixed order in
+            // each part, the parts added in order).
+            float inv = 0.f;
+            {
+                const int nq = args.hcq / kPChunk;
+                const int rows_per = T <= 32 ? 32 : 64;
+                const int parts = 128 / rows_per;
+                const int pr = etid % rows_per, pp = etid / rows_per;
+                const int per = (nq + parts - 1) / parts;
+                float part = 0.f;
+                if (ok && pr < T) {
+                    const int c0 = pp * per, c1 = nq < c0 + per ? nq : c0 + per;
+                    const float* sp = args.ss + pr;
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                    int c = c0;
+#pragma unroll 2
+                    for (; c + 3 < c1; c += 4) {
+                        a0 += __ldcg(sp + (size_t)c * T);
+                        a1 += __ldcg(sp + (size_t)(c + 1) * T);
+                        a2 += __ldcg(sp + (size_t)(c + 2) * T);
+                        a3 += __ldcg(sp + (size_t)(c + 3) * T);
+                    }
+                    for (; c < c1; ++c) a0 += __ldcg(sp + (size_t)c * T);
+                    part = (a0 + a1) + (a2 + a3);
+                }
+                ssum[pp * 64 + pr] = part;
+                epi_bar();
+                if (row < T) {
+                    float s2 = 0.f;
+                    for (int k = 0; k < parts; ++k) s2 += ssum[k * 64 + row];
+                    inv = 1.f / sqrtf(s2 / (float)args.hcq + args.eps_cq);
+                }
+            }
+            // ---- P3 epilogue: 1 / RMS per token, RoPE -> queryRopeOut, q^C -> P4's A operand
+            ok = acc_ready(1);
+            if (ok && q * 32 < T) {
+                const TmemSrc src{tmem_base + ((uint32_t)(q * 32) << 16)};
+                const uint32_t chain = smem_u32(aring);
+#pragma unroll 1
+                for (int ch = 0; ch < 4; ++ch) {
+                    float v[32];
+                    src.load(0, 0, ch * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= inv;
+                    if (row < T) chain_store(chain, args.a_bytes, row, ch * 32, v);
+                }
+                float x0[32], x1[32];
+                src.load(0, 0, 128, x0);
+                src.load(0, 0, 160, x1);
+                if (row < T) {
+                    const uint4* cp = reinterpret_cast<const uint4*>(args.rope_cos + (size_t)row * 64);
+                    const uint4* sp = reinterpret_cast<const uint4*>(args.rope_sin + (size_t)row * 64);
+                    float o0[32], o1[32];
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const uint4 c0 = cp[qq], c1 = cp[qq + 4], s0 = sp[qq], s1 = sp[qq + 4];
+                        const uint32_t cw0[4] = {c0.x, c0.y, c0.z, c0.w}, cw1[4] = {c1.x, c1.y, c1.z, c1.w};
+                        const uint32_t sw0[4] = {s0.x, s0.y, s0.z, s0.w}, sw1[4] = {s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = qq * 8 + e;
+                            const float cj = (e & 1) ? bf16_hi(cw0[e >> 1]) : bf16_lo(cw0[e >> 1]);
+                            const float sj = (e & 1) ? bf16_hi(sw0[e >> 1]) : bf16_lo(sw0[e >> 1]);
+                            const float ch = (e & 1) ? bf16_hi(cw1[e >> 1]) : bf16_lo(cw1[e >> 1]);
+                            const float sh = (e & 1) ? bf16_hi(sw1[e >> 1]) : bf16_lo(sw1[e >> 1]);
+                            const float a0 = x0[j] * inv, a1 = x1[j] * inv;
+                            o0[j] = a0 * cj - a1 * sj;
+                            o1[j] = a1 * ch + a0 * sh;
+                        }
+                    }
+                    __nv_bfloat16* dst = args.q_rope + ((size_t)row * args.N + blockIdx.x) * 64;
+                    store_bf16_chunk(dst, o0, 32);
+                    store_bf16_chunk(dst + 32, o1, 32);
+                }
+            }
+            fence_proxy_async_smem();   // q^C written by threads, read by the tensor core
+            tc_fence_before();
+            mbar_arrive(smem_u32(chain_full));
+
+            // ---- P4 epilogue: queryOut through shared memory and TMA stores
+            ok = ok && acc_ready(2);
+            if (ok && q * 32 < T) {
+                // every weight stage has been consumed: the ring is free for staging
+                OutStage<2> out{wring + (size_t)(warp - 4) * 2 * 4096, 0, &map_o, lane};
+                const TmemSrc src{tmem_base + ((uint32_t)(q * 32) << 16)};
+#pragma unroll 1
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t w[32];
+                    float v[32];
+                    src.load(0, 0, 64 * j, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+                    src.load(0, 0, 64 * j + 32, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+                    out.put(w, (int)blockIdx.x * 512 + 64 * j, q * 32);
+                }
+                out.drain();
+            }
+        }
+
+        // ---- KV: the cache rows, by the CTAs without a head (or by every CTA if none is free)
+        ok = !epi_any(!ok);
+        if (ok && args.nslots > 0) {
+            const int spare = G - args.N;
+            const int first = spare > 0 ? (int)blockIdx.x - args.N : (int)blockIdx.x;
+            const int step = spare > 0 ? spare : G;
+            const int ld = args.hckv + args.dr;
+            const int h = args.dr / 2;
+            const int c0 = args.hcq / kPChunk, nkv = (args.hckv + args.dr) / kPChunk;
+            if (first >= 0 && first < T) ok = wait_flags(args.cflags + c0, nkv, 1, args.tag, s_abort, etid);
+            if (ok && first >= 0) {
+                for (int t = first; t < T; t += step) {
+                    const long long slot = args.cache_index[t];
+                    if (slot < 0 || slot >= args.nslots) {
+                        if (etid == 0) atomicOr(args.status, kStatusCacheIndexRange);
+                        continue;
+                    }
+                    float s2 = 0.f;
+                    for (int c = 0; c < args.hckv / kPChunk; ++c) s2 += __ldcg(args.ss + (size_t)(c0 + c) * T + t);
+                    const float inv = 1.f / sqrtf(s2 / (float)args.hckv + args.eps_ckv);
+                    const float* y = args.ykv + (size_t)t * ld;
+                    __nv_bfloat16* kv = args.kv_cache + slot * args.hckv;
+                    for (int j = 2 * etid; j < args.hckv; j += 256) {
+                        const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(args.gamma_ckv + j);
+                        *reinterpret_cast<__nv_bfloat162*>(kv + j) =
+                            __floats2bfloat162_rn(__low2float(g2) * __ldcg(y + j) * inv, __high2float(g2) * __ldcg(y + j + 1) * inv);
+                    }
+                    const float* kr = y + args.hckv;
+                    const __nv_bfloat16* cs = args.rope_cos + (size_t)t * args.dr;
+                    const __nv_bfloat16* sn = args.rope_sin + (size_t)t * args.dr;
+                    __nv_bfloat16* dkr = args.kr_cache + slot * args.dr;
+                    for (int j = etid; j < h; j += 128) {
+                        const float x0 = __ldcg(kr + j), x1 = __ldcg(kr + j + h);
+                        dkr[j] = __float2bfloat16_rn(x0 * __bfloat162float(cs[j]) - x1 * __bfloat162float(sn[j]));
+                        dkr[j + h] = __float2bfloat16_rn(x1 * __bfloat162float(cs[j + h]) + x0 * __bfloat162float(sn[j + h]));
+                    }
+                }
+            }
+        }
+        if (!ok && etid == 0) fail();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*s_abort) {
+        // A wait gave up: give copies that may still be in flight time to land.
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 20000000ull) {
+        }
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+}  // namespace mla

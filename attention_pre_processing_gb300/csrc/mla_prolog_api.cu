@@ -20,6 +20,7 @@
 #include <random>
 
 #include "mla_prolog.h"
+#include "decode_persist.cuh"
 #include "finalize.cuh"
 #include "gemm_tc.cuh"
 
@@ -226,6 +227,9 @@ struct GemmPlan {
 struct Plan {
     GemmPlan g1, g2, g3;
     bool g2_fused = false;   // K2 epilogue does RoPE and q^C (no finalize_up)
+    bool persist = false;    // decode-sized bf16 call: the one persistent kernel of decode_persist.cuh
+    int p_n1 = 0, p_s1 = 0, p_wst = 0, p_arows = 0;
+    size_t p_smem = 0, off_pss = 0, off_pykv = 0, off_pbar = 0;
     int64_t ncols1 = 0, ncols2 = 0;
     size_t off_cq = 0, off_cqs = 0, off_qc = 0, off_y1 = 0, off_y2 = 0, off_xb = 0, off_wdq = 0, off_wdkvkr = 0,
            off_wuqqr = 0, bytes = 0;
@@ -293,6 +297,31 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
         p.g3.grid = (int)(tiles < sms ? tiles : sms);
     }
 
+    // The persistent decode kernel: bf16 operands and outputs, 128 + 64 head layout, 512-wide
+    // c^KV, every head and every reduction chunk on its own CTA.
+    {
+        const int64_t ncols1 = p.ncols1;
+        const int n1 = (int)(ncols1 / 192);
+        const int kb1 = (int)(d.He / 64);
+        const int arows = (int)((T + 7) / 8 * 8);
+        const size_t a_bytes = (size_t)arows * 128;
+        const int wst_fit = (int)((kSmemLimit - persist_smem_bytes((int)a_bytes, 0)) / kPStage);
+        const int wst = wst_fit < kPMaxW ? wst_fit : kPMaxW;
+        int s1 = n1 > 0 ? sms / n1 : 0;
+        if (s1 > kb1) s1 = kb1;
+        if (s1 > kPMaxS) s1 = kPMaxS;
+        if (!sc.x_i8 && !sc.uqqr_i8 && !sc.kv_i8 && !sc.kr_i8 && !sc.q_i8 && T >= 1 && T <= kPMaxT &&
+            d.D == 128 && d.Dr == 64 && d.Hckv == 512 && d.Hcq % 64 == 0 && d.He % 64 == 0 && ncols1 % 192 == 0 &&
+            d.N >= 1 && d.N <= sms && ncols1 / kPChunk <= sms && s1 >= 1 && wst >= 4) {
+            p.persist = true;
+            p.p_n1 = n1;
+            p.p_s1 = s1;
+            p.p_wst = wst;
+            p.p_arows = arows;
+            p.p_smem = persist_smem_bytes((int)a_bytes, wst);
+        }
+    }
+
     size_t off = kStatusBytes;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -302,7 +331,13 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     p.off_cq = take((size_t)T * d.Hcq * 2);
     p.off_cqs = take((size_t)T * 4);
     p.off_qc = take((size_t)T * d.N * d.D * 2);
-    p.off_y1 = take((size_t)p.g1.ksplit * T * p.ncols1 * 4);
+    const int y1_slots = p.persist && p.p_s1 > p.g1.ksplit ? p.p_s1 : p.g1.ksplit;
+    p.off_y1 = take((size_t)y1_slots * T * p.ncols1 * 4);
+    if (p.persist) {
+        p.off_pss = take((size_t)((d.Hcq + d.Hckv) / kPChunk) * T * 4);
+        p.off_pykv = take((size_t)T * (d.Hckv + d.Dr) * 4);
+        p.off_pbar = take((size_t)(sms + p.ncols1 / kPChunk) * 8);   // P1 and chunk flags
+    }
     if (!p.g2_fused) p.off_y2 = take((size_t)T * p.ncols2 * 4);
     if (sc.x_i8) {
         p.off_xb = take((size_t)T * d.He * 2);
@@ -312,6 +347,16 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     if (sc.uqqr_i8) p.off_wuqqr = take((size_t)d.Hcq * p.ncols2 * 2);
     p.bytes = off;
     return p;
+}
+
+// A per-call tag for the persistent kernel's dependency flags.  It starts at a random value
+// so that flags left in a reused workspace by earlier calls never match.
+unsigned long long next_tag() {
+    static std::atomic<unsigned long long> ctr{[] {
+        std::random_device rd;
+        return ((unsigned long long)rd() << 32) ^ (unsigned long long)rd();
+    }()};
+    return ctr.fetch_add(1) + 1;
 }
 
 // --------------------------------------------------------------- tensor maps
@@ -546,6 +591,76 @@ mla_status run(const Launched& L) {
         const uint64_t stridesb[2] = {(uint64_t)d.Hckv * 2, (uint64_t)d.D * d.Hckv * 2};
         const uint32_t boxb[3] = {64, 64, 1};
         if (!encode_map(&mB3, a.wuk->data, 3, dimsb, stridesb, boxb)) return MLA_ERR_RUNTIME;
+    }
+
+    if (p.persist) {
+        // ---- the whole prolog in one persistent kernel
+        const uint32_t rows = (uint32_t)p.p_arows;
+        CUtensorMap mx, mwdq, mwdkvkr, mcq, mwuqqr, mo;
+        const uint64_t ocols = (uint64_t)d.N * (uint64_t)d.Hckv;
+        const uint64_t odims[2] = {ocols, (uint64_t)d.T};
+        const uint64_t ostrides[1] = {ocols * 2};
+        const uint32_t obox[2] = {64, 32};
+        if (!map_2d(&mx, x_bf, d.T, d.He, rows) || !map_2d(&mwdq, wdq_bf, d.He, d.Hcq, 64) ||
+            !map_2d(&mwdkvkr, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64) || !map_2d(&mcq, ws + p.off_cq, d.T, d.Hcq, rows) ||
+            !map_2d(&mwuqqr, wuqqr_bf, d.Hcq, p.ncols2, 64) ||
+            !encode_map(&mo, a.qout->data, 2, odims, ostrides, obox))
+            return MLA_ERR_RUNTIME;
+        PersistArgs pa = {};
+        pa.T = T;
+        pa.a_rows = (int)rows;
+        pa.a_bytes = (int)rows * 128;
+        pa.wst = p.p_wst;
+        pa.hcq = (int)d.Hcq;
+        pa.hckv = (int)d.Hckv;
+        pa.dr = (int)d.Dr;
+        pa.ncols1 = (int)p.ncols1;
+        pa.n1 = p.p_n1;
+        pa.s1 = p.p_s1;
+        pa.kb1 = (int)(d.He / 64);
+        pa.y1 = y1;
+        pa.gamma_cq = f1.gamma_cq;
+        pa.gamma_ckv = f1.gamma_ckv;
+        pa.cq = f1.c_q;
+        pa.ss = reinterpret_cast<float*>(ws + p.off_pss);
+        pa.ykv = reinterpret_cast<float*>(ws + p.off_pykv);
+        pa.eps_cq = f1.eps_cq;
+        pa.eps_ckv = f1.eps_ckv;
+        pa.cache_index = f1.cache_index;
+        pa.nslots = f1.nslots;
+        pa.kv_cache = static_cast<__nv_bfloat16*>(a.kv->data);
+        pa.kr_cache = static_cast<__nv_bfloat16*>(a.kr->data);
+        pa.rope_cos = f1.rope_cos;
+        pa.rope_sin = f1.rope_sin;
+        pa.N = (int)d.N;
+        pa.kb2 = (int)(d.Hcq / 64);
+        pa.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
+        pa.q_out = static_cast<__nv_bfloat16*>(a.qout->data);
+        pa.p1flags = reinterpret_cast<unsigned long long*>(ws + p.off_pbar);
+        pa.cflags = pa.p1flags + L.sms;
+        pa.tag = next_tag();
+        pa.status = status;
+        e = cudaFuncSetAttribute(decode_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.p_smem);
+        if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)L.sms);
+        cfg.blockDim = dim3((unsigned)kPThreads);
+        cfg.dynamicSmemBytes = p.p_smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: the grid barriers need it
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, decode_persist_kernel, mx, mwdq, mwdkvkr, mcq, mwuqqr, mB3, mo, pa);
+        if (e == cudaSuccess) {
+            timing_mark(st, "decode_persist");
+            if (g_timing.enabled) g_timing.have = true;
+            return MLA_OK;
+        }
+        // Not every CTA can be resident (another context holds SMs): run the kernel-per-step path.
+        if (e != cudaErrorCooperativeLaunchTooLarge) return MLA_ERR_RUNTIME;
+        (void)cudaGetLastError();
     }
 
     // ---- K1: down-projection x . [W^DQ | W^DKV | W^KR] -> fp32 rows Y1

@@ -168,9 +168,10 @@ def test_prefill_t8192_bf16():
 
 # --------------------------------------------------------------- edge cases
 
-@pytest.mark.parametrize("T", [1, 37, 129, 200])
+@pytest.mark.parametrize("T", [1, 37, 64, 65, 129, 200])
 def test_decode_ragged_token_counts(T):
-    """Split-K path with ragged row counts (one and two 128-row sub-tiles)."""
+    """Decode sizes with ragged row counts: the persistent kernel (T <= 64), then the split-K
+    kernels with one and two 128-row sub-tiles."""
     case("decode_t32", T=T).check_all()
 
 
@@ -230,8 +231,10 @@ def test_no_cache_blocks_still_computes_queries():
     case("decode_t32", T=16, block_num=0).check_all()
 
 
-def test_out_of_range_slot_sets_status_and_skips_row():
-    cfg = workloads.config("tiny")
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("decode_t32", {"T": 8})])
+def test_out_of_range_slot_sets_status_and_skips_row(name, over):
+    """Kernel-per-step path (tiny) and the persistent decode kernel (DeepSeek-V3 shapes, T=8)."""
+    cfg = workloads.config(name, **over)
     inp = workloads.make_inputs(cfg)
     bad = int(cfg.shape.block_num * cfg.shape.block_size + 5)
     inp["cache_index"] = inp["cache_index"].clone()
