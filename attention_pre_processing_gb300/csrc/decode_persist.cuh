@@ -190,7 +190,7 @@ __device__ __forceinline__ bool load_cq_tiles(const PersistArgs& a, uint8_t* rin
             int s2 = sa;
             uint32_t p2 = ph;
             for (int k = 0; k < nb && ok; ++k) {
-                ok = mbar_wait(smem_u32(&empty[s2]), p2 ^ 1, abort, kWaitLimitNs);
+                ok = mbar_wait_sleep(smem_u32(&empty[s2]), p2 ^ 1, abort, kWaitLimitNs);
                 if (++s2 == kPA3) {
                     s2 = 0;
                     p2 ^= 1;
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             uint32_t ph = 0;
             PStep st;
             for (int i = 0; p_step(args, i, n1s, st); ++i) {
-                if (!mbar_wait(smem_u32(&wempty[s]), ph ^ 1, s_abort, kWaitLimitNs)) {
+                if (!mbar_wait_sleep(smem_u32(&wempty[s]), ph ^ 1, s_abort, kWaitLimitNs)) {
                     fail();
                     break;
                 }
@@ -357,66 +357,71 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // One explicit loop per phase; the operand descriptors are built once and advanced by
+        // constant offsets (their start-address field counts 16-byte units), so that a stage
+        // costs little more than its four MMAs.
         if (lane == 0) {
             constexpr uint32_t id192 = idesc_bf16_f32(128, 192, false, true);
             constexpr uint32_t id128 = idesc_bf16_f32(128, 128, false, true);
-            int sw = 0, sa = 0, sa3 = 0;
-            uint32_t phw = 0, pha = 0, pha3 = 0;
+            const uint64_t adesc0 = smem_desc_sw128(smem_u32(aring), 16, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(smem_u32(wring), kPBox, 1024);
+            const uint64_t a_unit = (uint64_t)(args.a_bytes >> 4);   // one activation slot
+            constexpr uint64_t w_unit = kPStage >> 4;                 // one weight stage
+            int sw = 0;
+            uint32_t phw = 0;
             bool ok = true;
-            PStep st;
-            for (int i = 0; ok && p_step(args, i, n1s, st); ++i) {
-                uint32_t a_base;
-                if (st.phase == 4) {
-                    if (st.first && st.g == 0 && !mbar_wait(smem_u32(chain_full), 0, s_abort, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    a_base = smem_u32(aring + (size_t)st.kb * args.a_bytes);
-                } else if (st.phase == 3) {
-                    if (!mbar_wait(smem_u32(&afull3[sa3]), pha3, s_abort, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    a_base = smem_u32(aring + (size_t)sa3 * args.a_bytes);
-                } else {
-                    if (!mbar_wait(smem_u32(&afull[sa]), pha, s_abort, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    a_base = smem_u32(aring + (size_t)sa * args.a_bytes);
-                }
-                if (!mbar_wait(smem_u32(&wfull[sw]), phw, s_abort, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
+            // One weight stage: K = 64 (four k16 MMAs) into accumulator columns d.
+            auto stage = [&](uint64_t adesc, uint32_t d, uint32_t idesc, bool first) -> bool {
+                if (!mbar_wait(smem_u32(&wfull[sw]), phw, s_abort, kWaitLimitNs)) return false;
                 tc_fence_after();
-                const uint32_t b_base = smem_u32(wring + (size_t)sw * kPStage);
-                const uint32_t d = tmem_base + (st.phase == 1 ? 256u : 0u) + (st.phase == 4 ? (uint32_t)(st.g * 192) : 0u);
-                const uint32_t idesc = st.nbox == 3 ? id192 : id128;
+                const uint64_t bdesc = bdesc0 + (uint64_t)sw * w_unit;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(d, smem_desc_sw128(a_base + kk * 32, 16, 1024),
-                              smem_desc_sw128(b_base + kk * 16 * 128, kPBox, 1024), idesc,
-                              (st.first && kk == 0) ? 0u : 1u);
+                    umma_bf16(d, adesc + 2 * kk, bdesc + 128 * kk, idesc, (first && kk == 0) ? 0u : 1u);
                 umma_commit(smem_u32(&wempty[sw]));
                 if (++sw == wst) {
                     sw = 0;
                     phw ^= 1;
                 }
-                if (st.phase == 1) {
+                return true;
+            };
+            // P1: activation slots filled by TMA
+            {
+                int sa = 0;
+                uint32_t pha = 0;
+                for (int i = 0; ok && i < n1s; ++i) {
+                    ok = mbar_wait(smem_u32(&afull[sa]), pha, s_abort, kWaitLimitNs) &&
+                         stage(adesc0 + (uint64_t)sa * a_unit, tmem_base + 256, id192, i == 0);
+                    if (!ok) break;
                     umma_commit(smem_u32(&aempty[sa]));
                     if (++sa == kPA) {
                         sa = 0;
                         pha ^= 1;
                     }
-                } else if (st.phase == 3) {
-                    umma_commit(smem_u32(&aempty3[sa3]));
-                    if (++sa3 == kPA3) {
-                        sa3 = 0;
-                        pha3 ^= 1;
+                }
+                if (ok && n1s > 0) umma_commit(smem_u32(&tfull[0]));
+            }
+            if (head) {
+                // P3: activation slots filled by the epilogue warps
+                int sa = 0;
+                uint32_t pha = 0;
+                for (int kb = 0; ok && kb < args.kb2; ++kb) {
+                    ok = mbar_wait(smem_u32(&afull3[sa]), pha, s_abort, kWaitLimitNs) &&
+                         stage(adesc0 + (uint64_t)sa * a_unit, tmem_base, id192, kb == 0);
+                    if (!ok) break;
+                    umma_commit(smem_u32(&aempty3[sa]));
+                    if (++sa == kPA3) {
+                        sa = 0;
+                        pha ^= 1;
                     }
                 }
-                if (st.last) umma_commit(smem_u32(&tfull[st.phase == 1 ? 0 : (st.phase == 3 ? 1 : 2)]));
+                if (ok) umma_commit(smem_u32(&tfull[1]));
+                // P4: A = q^C in activation slots 0 and 1; three column groups per k-block
+                ok = ok && mbar_wait(smem_u32(chain_full), 0, s_abort, kWaitLimitNs);
+                for (int kb = 0; ok && kb < 2; ++kb)
+                    for (int g = 0; ok && g < 3; ++g)
+                        ok = stage(adesc0 + (uint64_t)kb * a_unit, tmem_base + 192 * g, g == 2 ? id128 : id192, kb == 0);
+                if (ok) umma_commit(smem_u32(&tfull[2]));
             }
             if (!ok) fail();
             umma_commit(smem_u32(done));
@@ -430,7 +435,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             uint32_t ph = 0;
             bool ok = true;
             auto put = [&](const CUtensorMap* map, int kb) -> bool {
-                if (!mbar_wait(smem_u32(&aempty[sa]), ph ^ 1, s_abort, kWaitLimitNs)) return false;
+                if (!mbar_wait_sleep(smem_u32(&aempty[sa]), ph ^ 1, s_abort, kWaitLimitNs)) return false;
                 const uint32_t fb = smem_u32(&afull[sa]);
                 mbar_arrive_expect_tx(fb, (uint32_t)args.a_bytes);
                 tma_load_2d(smem_u32(aring + (size_t)sa * args.a_bytes), map, fb, kb * 64, 0, pol);
@@ -454,7 +459,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         bool ok = true;
         auto acc_ready = [&](int p) -> bool {
             int r = 1;
-            if (lane == 0) r = mbar_wait(smem_u32(&tfull[p]), 0, s_abort, kWaitLimitNs) ? 1 : 0;
+            if (lane == 0) r = mbar_wait_sleep(smem_u32(&tfull[p]), 0, s_abort, kWaitLimitNs) ? 1 : 0;
             r = __shfl_sync(0xffffffffu, r, 0);
             __syncwarp();
             tc_fence_after();

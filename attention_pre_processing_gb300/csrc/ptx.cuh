@@ -63,6 +63,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
+// Same, with a short sleep between polls: for waits off the tensor core's critical path, so
+// that the waiting warp does not take issue slots from the warps that share its scheduler.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                                uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(100);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
