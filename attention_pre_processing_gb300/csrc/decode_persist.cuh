@@ -124,31 +124,39 @@ __device__ __forceinline__ bool p_step(const PersistArgs& a, int i, int n1s, PSt
 
 // ------------------------------------------------------------------ dependency flags
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
     unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-// Waits (bounded) until flags f[0], f[stride], ..., f[(n-1) * stride] all hold `tag`.  Called
-// by all 128 epilogue threads together: thread i polls flags i, i + 128, ... so that every
-// flag's round trip overlaps; the result is combined over the 128 threads (every thread gets
-// the same answer), and the named barrier orders every thread's later loads after the flags.
+// Waits (bounded) until flags f[0], f[stride], ..., f[(n-1) * stride] (n <= 128) all hold
+// `tag`.  Called by all 128 epilogue threads together.  One warp polls: lane l reads flags
+// l, l + 32, l + 64, l + 96 together (relaxed loads), with a short sleep between rounds so that
+// the flag lines are not hammered while the data behind them is being read; the named barrier
+// releases the other warps, and every thread then takes an acquire fence.
 __device__ __forceinline__ bool wait_flags(const unsigned long long* f, int n, int stride, unsigned long long tag,
                                            const volatile int* abort, int etid) {
     bool ok = true;
-    const uint64_t t0 = global_timer_ns();
-    for (int i = etid; ok && i < n; i += 128) {
-        while (ld_acquire_u64(f + (size_t)i * stride) != tag) {
+    if (etid < 32) {
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+            bool all = true;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = etid + 32 * k;
+                if (i < n) all &= ld_relaxed_u64(f + (size_t)i * stride) == tag;
+            }
+            if (__all_sync(0xffffffffu, all)) break;
             if (*abort || global_timer_ns() - t0 > kWaitLimitNs) {
                 ok = false;
                 break;
             }
-            __nanosleep(32);
+            __nanosleep(64);
         }
     }
     const bool bad = epi_any(!ok);
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");   // acquire: what the flags published
     return !bad;
 }
 
@@ -465,9 +473,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc_fence_after();
             return r != 0;
         };
-        // The epilogue threads' stores so far become visible, then the flag says so.
+        // The epilogue threads' stores so far become visible, then the flag says so: the named
+        // barrier orders every thread's stores before thread 0's release store, and the release
+        // is cumulative over them.
         auto publish = [&](unsigned long long* flag) {
-            __threadfence();
             epi_bar();
             if (etid == 0) asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flag), "l"(args.tag) : "memory");
         };
