@@ -74,10 +74,12 @@ struct GemmArgs {
 };
 
 // OUTB: 4 KB staging buffers per epilogue warp for TMA stores of the output (0 = none).
-template <int BN, int MSUB, int MAXST, int OUTB = 0>
+// KPS: k-blocks per pipeline stage.  With KPS = 2 a weight box spans 128 k rows (16 KB): the
+// TMA engine moves far more bytes per box request from L2 than with 64-row boxes.
+template <int BN, int MSUB, int MAXST, int OUTB = 0, int KPS = 1>
 struct GemmCfg {
     static constexpr int kOutBytes = 4 * OUTB * 4096;
-    static constexpr int kBStage = BN * kBK * 2;            // BN/64 boxes of 64 x 64
+    static constexpr int kBStage = BN * kBK * 2 * KPS;      // BN/64 boxes of 64 cols x 64*KPS rows
     static constexpr int kAcc = MSUB * BN;                  // TMEM columns per accumulator set
     static constexpr int kNBuf = (2 * kAcc <= 512) ? 2 : 1;
     static constexpr int kTmemCols = (kNBuf * kAcc <= 32) ? 32 : (kNBuf * kAcc <= 64) ? 64
@@ -90,7 +92,7 @@ struct GemmCfg {
     static_assert(kMmaN % 16 == 0 && kMmaN <= 256, "bad MMA N");
     static_assert(kAcc <= 512, "accumulator exceeds TMEM");
 
-    static __host__ __device__ int a_stage_bytes(int a_box_rows) { return MSUB * a_box_rows * 128; }
+    static __host__ __device__ int a_stage_bytes(int a_box_rows) { return KPS * MSUB * a_box_rows * 128; }
     static __host__ __device__ int stage_bytes(int a_box_rows) { return a_stage_bytes(a_box_rows) + kBStage; }
     // A region first: a 128-row MMA operand read from the last A stage with a short box runs
     // at most 16 KB past it, into the B ring (>= 2 stages of >= 8 KB), inside the block.
@@ -440,8 +442,9 @@ __device__ __forceinline__ void epilogue_qn_tma(const GemmArgs& a, const Unit& u
 
 // ---------------------------------------------------------------------- loads
 
-// Weight tile of k-block kb: BN/64 boxes of 64 columns x 64 rows.
-template <int BN>
+// Weight tile of the stage starting at k-block kb: BN/64 boxes of 64 columns x (64 * KPS) rows
+// (the tensor maps' box height).
+template <int BN, int KPS = 1>
 __device__ __forceinline__ void load_b(const GemmArgs& a, const Unit& u, int kb, uint32_t dst, uint32_t bar,
                                        const CUtensorMap* b0, const CUtensorMap* b1, uint64_t pol) {
     int head = 0, c0;
@@ -454,7 +457,7 @@ __device__ __forceinline__ void load_b(const GemmArgs& a, const Unit& u, int kb,
 #pragma unroll
     for (int j = 0; j < BN / 64; ++j) {
         const int col = c0 + 64 * j;
-        const uint32_t d = dst + j * (64 * kBK * 2);
+        const uint32_t d = dst + j * (64 * kBK * 2 * KPS);
         if (a.head_mode)
             tma_load_3d(d, b0, bar, col, kb * kBK, head, pol);
         else if (col < a.b_split_col)
@@ -481,12 +484,12 @@ __device__ __forceinline__ void load_a(const GemmArgs& a, const Unit& u, int kb,
 
 // ---------------------------------------------------------------------- kernel
 
-template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0>
+template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0, int KPS = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                    const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_o,
                    const GemmArgs args) {
-    using C = GemmCfg<BN, MSUB, MAXST, OUTB>;
+    using C = GemmCfg<BN, MSUB, MAXST, OUTB, KPS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -553,36 +556,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int pre = 0;
             Unit u0;
             const bool have0 = get_unit(args, 0, u0);
+            // The activation tiles of one stage: KPS k-blocks of MSUB boxes each.
+            auto load_a_stage = [&](const Unit& uu, int kb, uint32_t dst, uint32_t fb) {
+#pragma unroll
+                for (int k = 0; k < KPS; ++k)
+                    load_a<MSUB>(args, uu, kb + k, dst + k * MSUB * a_box, a_box, fb, &map_a, pol_a);
+            };
             if (have0) {
-                const int n0 = u0.kb1 - u0.kb0;
+                const int n0 = (u0.kb1 - u0.kb0) / KPS;
                 pre = n0 < stages ? n0 : stages;
                 for (int i = 0; i < pre; ++i) {
                     const uint32_t fb = smem_u32(&full[i]);
                     mbar_arrive_expect_tx(fb, (uint32_t)(a_stage + C::kBStage));
                     if (args.a_ready)   // stage i complete as early as possible
-                        load_a<MSUB>(args, u0, u0.kb0 + i, smem_u32(sA + (size_t)i * a_stage), a_box, fb, &map_a,
-                                     pol_a);
-                    load_b<BN>(args, u0, u0.kb0 + i, smem_u32(sB + (size_t)i * C::kBStage), fb, &map_b0, &map_b1,
-                               pol_w);
+                        load_a_stage(u0, u0.kb0 + i * KPS, smem_u32(sA + (size_t)i * a_stage), fb);
+                    load_b<BN, KPS>(args, u0, u0.kb0 + i * KPS, smem_u32(sB + (size_t)i * C::kBStage), fb, &map_b0,
+                                    &map_b1, pol_w);
                 }
             }
             pdl_wait();
             if (!args.a_ready)
                 for (int i = 0; i < pre; ++i)
-                    load_a<MSUB>(args, u0, u0.kb0 + i, smem_u32(sA + (size_t)i * a_stage), a_box,
-                                 smem_u32(&full[i]), &map_a, pol_a);
+                    load_a_stage(u0, u0.kb0 + i * KPS, smem_u32(sA + (size_t)i * a_stage), smem_u32(&full[i]));
             s = pre % stages;
             ph = (pre == stages) ? 1u : 0u;
             for (int idx = 0; ok && get_unit(args, idx, u); ++idx) {
-                for (int kb = u.kb0 + (idx == 0 ? pre : 0); kb < u.kb1; ++kb) {
+                for (int kb = u.kb0 + (idx == 0 ? pre * KPS : 0); kb < u.kb1; kb += KPS) {
                     if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, s_abort, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = smem_u32(&full[s]);
                     mbar_arrive_expect_tx(fb, (uint32_t)(a_stage + C::kBStage));
-                    load_b<BN>(args, u, kb, smem_u32(sB + (size_t)s * C::kBStage), fb, &map_b0, &map_b1, pol_w);
-                    load_a<MSUB>(args, u, kb, smem_u32(sA + (size_t)s * a_stage), a_box, fb, &map_a, pol_a);
+                    load_b<BN, KPS>(args, u, kb, smem_u32(sB + (size_t)s * C::kBStage), fb, &map_b0, &map_b1, pol_w);
+                    load_a_stage(u, kb, smem_u32(sA + (size_t)s * a_stage), fb);
                     if (++s == stages) {
                         s = 0;
                         ph ^= 1;
@@ -613,7 +620,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_base = tmem_base + b * C::kAcc;
-                for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
                     if (!mbar_wait(smem_u32(&full[s]), ph, s_abort, kWaitLimitNs)) {
                         ok = false;
                         break;
@@ -621,17 +628,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after();
                     const uint32_t a_base = smem_u32(sA + (size_t)s * a_stage);
                     const uint32_t b_base = smem_u32(sB + (size_t)s * C::kBStage);
+                    constexpr int kBox = 64 * kBK * 2 * KPS;   // one weight box (column stride of B)
+#pragma unroll
+                    for (int k = 0; k < KPS; ++k)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
 #pragma unroll
                         for (int ms = 0; ms < MSUB; ++ms) {
-                            const uint64_t adesc = smem_desc_sw128(a_base + ms * a_box + kk * 32, 16, 1024);
+                            const uint64_t adesc =
+                                smem_desc_sw128(a_base + (k * MSUB + ms) * a_box + kk * 32, 16, 1024);
 #pragma unroll
                             for (int np = 0; np < C::kNParts; ++np) {
                                 const uint64_t bdesc = smem_desc_sw128(
-                                    b_base + np * (C::kMmaN / 64) * (64 * kBK * 2) + kk * 16 * 128, 64 * kBK * 2, 1024);
+                                    b_base + np * (C::kMmaN / 64) * kBox + k * (64 * kBK * 2) + kk * 16 * 128, kBox, 1024);
                                 umma_bf16(d_base + ms * BN + np * C::kMmaN, adesc, bdesc, idesc,
-                                          (kb > u.kb0 || kk > 0) ? 1u : 0u);
+                                          (kb > u.kb0 || k > 0 || kk > 0) ? 1u : 0u);
                             }
                         }
                     }

@@ -463,11 +463,11 @@ cudaError_t launch(Kernel k, int grid, int block, size_t smem, cudaStream_t st, 
 }
 
 // Launches one GEMM instantiation; fills in the ring depth and dynamic shared memory.
-template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0>
+template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0, int KPS = 1>
 cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         GemmArgs args, const CUtensorMap* out = nullptr) {
-    using C = GemmCfg<BN, MSUB, MAXST, OUTB>;
-    auto k = gemm_tc_kernel<BN, MSUB, MAXST, EPI, OUTB>;
+    using C = GemmCfg<BN, MSUB, MAXST, OUTB, KPS>;
+    auto k = gemm_tc_kernel<BN, MSUB, MAXST, EPI, OUTB, KPS>;
     CUtensorMap mo;
     std::memset(&mo, 0, sizeof mo);
     if (out != nullptr) mo = *out;
@@ -580,7 +580,9 @@ mla_status run(const Launched& L) {
     cudaError_t e;
 
     // The 3D map of q^C (one head's T x D slice per box) and of W^UK (one head's D x Hckv).
+    // Row tiles of 128 tokens take both k-blocks of D = 128 in one stage.
     CUtensorMap mA3, mB3;
+    const bool kps3 = !sc.q_i8 && p.g3.m_tiles > 1 && p.g3.kblocks % 2 == 0;   // 512-column int8 tiles: no room
     const uint32_t a3_rows = (uint32_t)p.g3.a_box_rows;
     {
         const uint64_t dims[3] = {(uint64_t)d.D, (uint64_t)d.N, (uint64_t)d.T};
@@ -589,7 +591,7 @@ mla_status run(const Launched& L) {
         if (!encode_map(&mA3, qc, 3, dims, strides, box)) return MLA_ERR_RUNTIME;
         const uint64_t dimsb[3] = {(uint64_t)d.Hckv, (uint64_t)d.D, (uint64_t)d.N};
         const uint64_t stridesb[2] = {(uint64_t)d.Hckv * 2, (uint64_t)d.D * d.Hckv * 2};
-        const uint32_t boxb[3] = {64, 64, 1};
+        const uint32_t boxb[3] = {64, kps3 ? 128u : 64u, 1};
         if (!encode_map(&mB3, a.wuk->data, 3, dimsb, stridesb, boxb)) return MLA_ERR_RUNTIME;
     }
 
@@ -665,8 +667,12 @@ mla_status run(const Launched& L) {
 
     // ---- K1: down-projection x . [W^DQ | W^DKV | W^KR] -> fp32 rows Y1
     CUtensorMap mA1, mB1a, mB1b;
-    if (!map_2d(&mA1, x_bf, d.T, d.He, (uint32_t)p.g1.a_box_rows) || !map_2d(&mB1a, wdq_bf, d.He, d.Hcq, 64) ||
-        !map_2d(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64))
+    // Whole-K tiles with an even number of k-blocks stream two k-blocks per stage (128-row
+    // weight boxes); k ranges (decode) keep one.
+    const bool kps1 = p.g1.ksplit == 1 && p.g1.msub == 2 && p.g1.kblocks % 2 == 0;
+    const uint32_t b1_rows = kps1 ? 128 : 64;
+    if (!map_2d(&mA1, x_bf, d.T, d.He, (uint32_t)p.g1.a_box_rows) || !map_2d(&mB1a, wdq_bf, d.He, d.Hcq, b1_rows) ||
+        !map_2d(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, b1_rows))
         return MLA_ERR_RUNTIME;
     GemmArgs g1 = gemm_args(p.g1, T, p.ncols1, status);
     g1.b_split_col = (int)d.Hcq;
@@ -676,7 +682,8 @@ mla_status run(const Launched& L) {
     if (p.g1.bn == 64)
         e = launch_gemm<64, 1, 32, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
     else
-        e = launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+        e = kps1 ? launch_gemm<192, 2, 4, EPI_F32, 0, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
+                 : launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k1_down_proj");
 
@@ -693,8 +700,9 @@ mla_status run(const Launched& L) {
 
     // ---- K2: up-projection c^Q . W^UqQr -> RoPE(q^R) and q^C
     CUtensorMap mA2, mB2;
+    const bool kps2 = p.g2.msub == 2 && p.g2.ksplit == 1 && p.g2.kblocks % 2 == 0;
     if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
-        !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64))
+        !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, kps2 ? 128 : 64))
         return MLA_ERR_RUNTIME;
     GemmArgs g2 = gemm_args(p.g2, T, p.ncols2, status);
     g2.N = (int)d.N;
@@ -707,10 +715,12 @@ mla_status run(const Launched& L) {
     g2.out_f32 = reinterpret_cast<float*>(ws + p.off_y2);
     if (p.g2_fused) {
         e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2)
-                             : launch_gemm<192, 2, 4, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2);
+                             : (kps2 ? launch_gemm<192, 2, 4, EPI_QROPE, 0, 2>(p.g2.grid, st, mA2, mB2, mB2, g2)
+                                     : launch_gemm<192, 2, 4, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2));
     } else {
         e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2)
-                             : launch_gemm<192, 2, 4, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2);
+                             : (kps2 ? launch_gemm<192, 2, 4, EPI_F32, 0, 2>(p.g2.grid, st, mA2, mB2, mB2, g2)
+                                     : launch_gemm<192, 2, 4, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2));
     }
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k2_up_proj");
@@ -763,7 +773,8 @@ mla_status run(const Launched& L) {
         e = launch_gemm<512, 1, 4, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr);
     } else {
         g3.q_out_bf16 = static_cast<__nv_bfloat16*>(a.qout->data);
-        e = launch_gemm<256, 1, 8, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr);
+        e = kps3 ? launch_gemm<256, 1, 8, EPI_QN, 2, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr)
+                 : launch_gemm<256, 1, 8, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr);
     }
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k3_absorb_uk");
