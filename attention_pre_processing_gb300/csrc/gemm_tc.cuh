@@ -354,7 +354,8 @@ struct OutStage {
     int ob;
     const CUtensorMap* map;
     int lane;
-    __device__ __forceinline__ void put(const uint32_t (&w)[32], int x, int y) {
+    __device__ __forceinline__ void put(const uint32_t (&w)[32], int x, int y) { put(w, x, y, map); }
+    __device__ __forceinline__ void put(const uint32_t (&w)[32], int x, int y, const CUtensorMap* m) {
         const uint32_t buf = smem_u32(obuf + ob * 4096);
         if (lane == 0) bulk_wait_read<OUTB - 1>();   // the store that last read this buffer
         __syncwarp();
@@ -367,7 +368,7 @@ struct OutStage {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d(map, buf, x, y);
+            tma_store_2d(m, buf, x, y);
             bulk_commit();
         }
         ob = (ob + 1 == OUTB) ? 0 : ob + 1;
@@ -377,6 +378,94 @@ struct OutStage {
         __syncwarp();
     }
 };
+
+// fp32 product rows (EPI_F32, ksplit = 1) through shared memory and TMA stores: 32-row x
+// 32-column (128-byte) boxes of the T x ncols matrix; rows and columns past its extent are not
+// written.
+template <int BN, int MSUB, int OUTB>
+__device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const Unit& u, const TmemSrc& src, int q,
+                                                 OutStage<OUTB>& out) {
+#pragma unroll 1
+    for (int ms = 0; ms < MSUB; ++ms) {
+        const int row0 = u.m_tile * MSUB * 128 + ms * 128 + q * 32;
+        if (row0 >= a.T) continue;   // warp-uniform
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+            const int col = u.n_tile * BN + ch * 32;
+            if (col >= a.ncols) break;
+            uint32_t w[32];
+            tmem_ld_32x32b_x32(src.tacc + ms * BN + ch * 32, w);
+            tmem_ld_wait();
+            out.put(w, col, row0);
+        }
+    }
+}
+
+// One head per tile (EPI_QROPE, no dequant scales): q^C (128 columns) and RoPE(q^R) (64
+// columns) through shared memory and TMA stores into the (T, N*128) and (T, N*64) views.
+template <int MSUB, int OUTB>
+__device__ __forceinline__ void epilogue_qrope_tma(const GemmArgs& a, const Unit& u, const TmemSrc& src, int q,
+                                                   OutStage<OUTB>& out, const CUtensorMap* map_c,
+                                                   const CUtensorMap* map_r) {
+    constexpr int BN = 192, D = 128, DR = 64, H = 32;
+    const int head = u.n_tile;
+#pragma unroll 1
+    for (int ms = 0; ms < MSUB; ++ms) {
+        const int row0 = u.m_tile * MSUB * 128 + ms * 128 + q * 32;
+        if (row0 >= a.T) continue;   // warp-uniform
+        const int row = row0 + out.lane;
+        const bool valid = row < a.T;
+        // this row's RoPE tables, requested before the tensor-memory reads
+        uint4 c4[8], s4[8];
+        const uint4* cp = reinterpret_cast<const uint4*>(a.rope_cos + (size_t)(valid ? row : 0) * DR);
+        const uint4* sp = reinterpret_cast<const uint4*>(a.rope_sin + (size_t)(valid ? row : 0) * DR);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c4[i] = __ldg(cp + i);
+            s4[i] = __ldg(sp + i);
+        }
+#pragma unroll 1
+        for (int j = 0; j < D / 64; ++j) {
+            uint32_t w[32];
+            float v[32];
+            src.load(ms, BN, 64 * j, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+            src.load(ms, BN, 64 * j + 32, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+            out.put(w, head * D + 64 * j, row0, map_c);
+        }
+        float x0[32], x1[32];
+        src.load(ms, BN, D, x0);
+        src.load(ms, BN, D + H, x1);
+        uint32_t w[32];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const uint32_t cw0[4] = {c4[qq].x, c4[qq].y, c4[qq].z, c4[qq].w};
+            const uint32_t cw1[4] = {c4[qq + 4].x, c4[qq + 4].y, c4[qq + 4].z, c4[qq + 4].w};
+            const uint32_t sw0[4] = {s4[qq].x, s4[qq].y, s4[qq].z, s4[qq].w};
+            const uint32_t sw1[4] = {s4[qq + 4].x, s4[qq + 4].y, s4[qq + 4].z, s4[qq + 4].w};
+            float o0[8], o1[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int jj = qq * 8 + e;
+                const float cj = (e & 1) ? bf16_hi(cw0[e >> 1]) : bf16_lo(cw0[e >> 1]);
+                const float sj = (e & 1) ? bf16_hi(sw0[e >> 1]) : bf16_lo(sw0[e >> 1]);
+                const float ch = (e & 1) ? bf16_hi(cw1[e >> 1]) : bf16_lo(cw1[e >> 1]);
+                const float sh = (e & 1) ? bf16_hi(sw1[e >> 1]) : bf16_lo(sw1[e >> 1]);
+                o0[e] = x0[jj] * cj - x1[jj] * sj;
+                o1[e] = x1[jj] * ch + x0[jj] * sh;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                w[qq * 4 + e] = pack_bf16(o0[2 * e], o0[2 * e + 1]);
+                w[16 + qq * 4 + e] = pack_bf16(o1[2 * e], o1[2 * e + 1]);
+            }
+        }
+        out.put(w, head * DR, row0, map_r);
+    }
+}
 
 template <int BN, int OUTB>
 __device__ __forceinline__ void epilogue_qn_tma(const GemmArgs& a, const Unit& u, const TmemSrc& src, int q,
@@ -488,7 +577,7 @@ template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0, int KPS = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                    const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_o,
-                   const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap map_o2, const GemmArgs args) {
     using C = GemmCfg<BN, MSUB, MAXST, OUTB, KPS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -514,7 +603,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b0);
         tma_prefetch_map(&map_b1);
-        if (OUTB > 0 && args.tma_out) tma_prefetch_map(&map_o);
+        if (OUTB > 0 && args.tma_out) {
+            tma_prefetch_map(&map_o);
+            if (EPI == EPI_QROPE) tma_prefetch_map(&map_o2);
+        }
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
@@ -700,9 +792,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const TmemSrc tsrc{tmem_base + ((uint32_t)(q * 32) << 16) + b * C::kAcc};
             const int row0 = u.m_tile * MSUB * 128 + row_in;
             if constexpr (EPI == EPI_F32) {
-                epilogue_f32<BN, MSUB>(args, row0, u.n_tile, u.ks, tsrc);
+                if constexpr (OUTB > 0) {
+                    if (args.tma_out)
+                        epilogue_f32_tma<BN, MSUB, OUTB>(args, u, tsrc, q, ostage);
+                    else
+                        epilogue_f32<BN, MSUB>(args, row0, u.n_tile, u.ks, tsrc);
+                } else {
+                    epilogue_f32<BN, MSUB>(args, row0, u.n_tile, u.ks, tsrc);
+                }
             } else if constexpr (EPI == EPI_QROPE) {
-                epilogue_qrope<MSUB>(args, row0, u.n_tile, tsrc);
+                if constexpr (OUTB > 0) {
+                    if (args.tma_out)
+                        epilogue_qrope_tma<MSUB, OUTB>(args, u, tsrc, q, ostage, &map_o, &map_o2);
+                    else
+                        epilogue_qrope<MSUB>(args, row0, u.n_tile, tsrc);
+                } else {
+                    epilogue_qrope<MSUB>(args, row0, u.n_tile, tsrc);
+                }
             } else {
                 if constexpr (OUTB > 0) {
                     if (args.tma_out)

@@ -465,18 +465,20 @@ cudaError_t launch(Kernel k, int grid, int block, size_t smem, cudaStream_t st, 
 // Launches one GEMM instantiation; fills in the ring depth and dynamic shared memory.
 template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0, int KPS = 1>
 cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                        GemmArgs args, const CUtensorMap* out = nullptr) {
+                        GemmArgs args, const CUtensorMap* out = nullptr, const CUtensorMap* out2 = nullptr) {
     using C = GemmCfg<BN, MSUB, MAXST, OUTB, KPS>;
     auto k = gemm_tc_kernel<BN, MSUB, MAXST, EPI, OUTB, KPS>;
-    CUtensorMap mo;
+    CUtensorMap mo, mo2;
     std::memset(&mo, 0, sizeof mo);
+    std::memset(&mo2, 0, sizeof mo2);
     if (out != nullptr) mo = *out;
+    if (out2 != nullptr) mo2 = *out2;
     args.stages = C::max_stages(args.a_box_rows);
     if (args.stages < 2) return cudaErrorInvalidConfiguration;
     const size_t smem = C::smem_bytes(args.stages, args.a_box_rows);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
     if (e != cudaSuccess) return e;
-    return launch(k, grid, kGemmThreads, smem, st, a, b0, b1, mo, args);
+    return launch(k, grid, kGemmThreads, smem, st, a, b0, b1, mo, mo2, args);
 }
 
 struct Launched {
@@ -667,10 +669,10 @@ mla_status run(const Launched& L) {
 
     // ---- K1: down-projection x . [W^DQ | W^DKV | W^KR] -> fp32 rows Y1
     CUtensorMap mA1, mB1a, mB1b;
-    // Whole-K tiles with an even number of k-blocks stream two k-blocks per stage (128-row
-    // weight boxes); k ranges (decode) keep one.
-    const bool kps1 = p.g1.ksplit == 1 && p.g1.msub == 2 && p.g1.kblocks % 2 == 0;
-    const uint32_t b1_rows = kps1 ? 128 : 64;
+    // Whole-K 256-row tiles store their fp32 rows through shared memory with TMA (32 x 32
+    // boxes of the T x ncols1 matrix); k ranges (decode) use plain stores into their slots.
+    const bool tma1 = p.g1.ksplit == 1 && p.g1.msub == 2 && p.ncols1 % 4 == 0;
+    const uint32_t b1_rows = 64;
     if (!map_2d(&mA1, x_bf, d.T, d.He, (uint32_t)p.g1.a_box_rows) || !map_2d(&mB1a, wdq_bf, d.He, d.Hcq, b1_rows) ||
         !map_2d(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, b1_rows))
         return MLA_ERR_RUNTIME;
@@ -678,12 +680,19 @@ mla_status run(const Launched& L) {
     g1.b_split_col = (int)d.Hcq;
     g1.clear_status = 1;
     g1.a_ready = sc.x_i8 ? 0 : 1;   // bf16 tokenX is read as passed; int8 is widened first
+    CUtensorMap mO1;
+    if (tma1) {
+        const uint64_t dims[2] = {(uint64_t)p.ncols1, (uint64_t)d.T};
+        const uint64_t strides[1] = {(uint64_t)p.ncols1 * 4};
+        const uint32_t box[2] = {32, 32};
+        g1.tma_out = encode_map(&mO1, y1, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ? 1 : 0;
+    }
     g1.out_f32 = y1;
     if (p.g1.bn == 64)
         e = launch_gemm<64, 1, 32, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
     else
-        e = kps1 ? launch_gemm<192, 2, 4, EPI_F32, 0, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
-                 : launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+        e = g1.tma_out ? launch_gemm<192, 2, 4, EPI_F32, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
+                       : launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k1_down_proj");
 
@@ -700,11 +709,21 @@ mla_status run(const Launched& L) {
 
     // ---- K2: up-projection c^Q . W^UqQr -> RoPE(q^R) and q^C
     CUtensorMap mA2, mB2;
-    const bool kps2 = p.g2.msub == 2 && p.g2.ksplit == 1 && p.g2.kblocks % 2 == 0;
+    // 256-row tiles without dequant scales store q^C and q^R through shared memory with TMA.
+    const bool tma2 = p.g2_fused && p.g2.msub == 2 && !sc.uqqr_i8;
     if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
-        !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, kps2 ? 128 : 64))
+        !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64))
         return MLA_ERR_RUNTIME;
     GemmArgs g2 = gemm_args(p.g2, T, p.ncols2, status);
+    CUtensorMap mO2c, mO2r;
+    if (tma2) {
+        const uint64_t dc[2] = {(uint64_t)d.N * d.D, (uint64_t)d.T};
+        const uint64_t sc2[1] = {(uint64_t)d.N * d.D * 2};
+        const uint64_t dr[2] = {(uint64_t)d.N * d.Dr, (uint64_t)d.T};
+        const uint64_t sr[1] = {(uint64_t)d.N * d.Dr * 2};
+        const uint32_t box[2] = {64, 32};
+        g2.tma_out = encode_map(&mO2c, qc, 2, dc, sc2, box) && encode_map(&mO2r, a.qrope->data, 2, dr, sr, box) ? 1 : 0;
+    }
     g2.N = (int)d.N;
     g2.q_c = qc;
     g2.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
@@ -715,12 +734,12 @@ mla_status run(const Launched& L) {
     g2.out_f32 = reinterpret_cast<float*>(ws + p.off_y2);
     if (p.g2_fused) {
         e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2)
-                             : (kps2 ? launch_gemm<192, 2, 4, EPI_QROPE, 0, 2>(p.g2.grid, st, mA2, mB2, mB2, g2)
-                                     : launch_gemm<192, 2, 4, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2));
+                             : (g2.tma_out ? launch_gemm<192, 2, 4, EPI_QROPE, 2>(p.g2.grid, st, mA2, mB2, mB2, g2,
+                                                                                 &mO2c, &mO2r)
+                                           : launch_gemm<192, 2, 4, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2));
     } else {
         e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2)
-                             : (kps2 ? launch_gemm<192, 2, 4, EPI_F32, 0, 2>(p.g2.grid, st, mA2, mB2, mB2, g2)
-                                     : launch_gemm<192, 2, 4, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2));
+                             : launch_gemm<192, 2, 4, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2);
     }
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k2_up_proj");
