@@ -101,10 +101,9 @@ __device__ __forceinline__ float group_reduce(float v, float* red, int tid, Sync
 // ys: Hcq + Hckv + Dr floats of shared memory; red: NT/32 + 1 floats; gcq / gckv: the gammas,
 // already staged in shared memory.  Every load that does not depend on the partial sums is
 // issued before them, and a thread's partial loads for up to kRowCols columns are in flight
-// together, so the row costs about one memory latency.
-constexpr int kRowCols = 9;
-
-template <int NT, class Sync>
+// together: with few rows (decode) the row then costs about one memory latency; with many rows a
+// small kRowCols keeps the registers, and so the rows in flight per SM, up.
+template <int NT, int kRowCols, class Sync>
 __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, float* ys, float* red,
                                          const __nv_bfloat16* gcq, const __nv_bfloat16* gckv, Sync sync) {
     const int ncols = a.Hcq + a.Hckv + a.Dr;
@@ -249,7 +248,8 @@ __host__ __device__ inline size_t down_smem_bytes(int Hcq, int Hckv, int Dr) {
     return (((size_t)(Hcq + Hckv + Dr) * 4 + 15) & ~(size_t)15) + (size_t)(Hcq + Hckv) * 2;
 }
 
-// One CTA per token (grid-stride).
+// One CTA per token (grid-stride).  ROWCOLS: columns of partial sums a thread has in flight.
+template <int ROWCOLS>
 __global__ void __launch_bounds__(kRowThreads) finalize_down_kernel(const DownArgs a) {
     extern __shared__ __align__(16) uint8_t fsm[];
     float* ys = reinterpret_cast<float*>(fsm);
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kRowThreads) finalize_down_kernel(const DownAr
     pdl_wait();
     __syncthreads();
     for (int t = blockIdx.x; t < a.T; t += gridDim.x)
-        down_row<kRowThreads>(a, t, threadIdx.x, ys, red, gcq, gckv, CtaSync{});
+        down_row<kRowThreads, ROWCOLS>(a, t, threadIdx.x, ys, red, gcq, gckv, CtaSync{});
 }
 
 struct UpArgs {

@@ -699,6 +699,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, C::kMmaN, false, true);
+            const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), 64 * kBK * 2 * KPS, 1024);
             int s = 0;
             uint32_t ph = 0, ai = 0;
             Unit u;
@@ -718,8 +720,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + (size_t)s * a_stage);
-                    const uint32_t b_base = smem_u32(sB + (size_t)s * C::kBStage);
+                    // Descriptors of this stage, advanced by constant offsets (the start-address
+                    // field counts 16-byte units): cheap enough to keep the tensor core fed.
+                    const uint64_t a_desc = a_desc0 + (uint64_t)s * (uint64_t)(a_stage >> 4);
+                    const uint64_t b_desc = b_desc0 + (uint64_t)s * (uint64_t)(C::kBStage >> 4);
                     constexpr int kBox = 64 * kBK * 2 * KPS;   // one weight box (column stride of B)
 #pragma unroll
                     for (int k = 0; k < KPS; ++k)
@@ -727,12 +731,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int kk = 0; kk < kBK / 16; ++kk) {
 #pragma unroll
                         for (int ms = 0; ms < MSUB; ++ms) {
-                            const uint64_t adesc =
-                                smem_desc_sw128(a_base + (k * MSUB + ms) * a_box + kk * 32, 16, 1024);
+                            const uint64_t adesc = a_desc + (uint64_t)((((k * MSUB + ms) * a_box) >> 4) + 2 * kk);
 #pragma unroll
                             for (int np = 0; np < C::kNParts; ++np) {
-                                const uint64_t bdesc = smem_desc_sw128(
-                                    b_base + np * (C::kMmaN / 64) * kBox + k * (64 * kBK * 2) + kk * 16 * 128, kBox, 1024);
+                                const uint64_t bdesc =
+                                    b_desc + (uint64_t)(((np * (C::kMmaN / 64) * kBox + k * (64 * kBK * 2)) >> 4) + 128 * kk);
                                 umma_bf16(d_base + ms * BN + np * C::kMmaN, adesc, bdesc, idesc,
                                           (kb > u.kb0 || k > 0 || kk > 0) ? 1u : 0u);
                             }

@@ -700,9 +700,12 @@ mla_status run(const Launched& L) {
     {
         const int grid = T < 16 * L.sms ? T : 16 * L.sms;
         const size_t fsmem = down_smem_bytes((int)d.Hcq, (int)d.Hckv, (int)d.Dr);
-        e = cudaFuncSetAttribute(finalize_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
+        // decode-sized T: every partial load of a row in flight at once; many rows: fewer, so
+        // that more rows fit on an SM
+        auto fk = T <= kDecodeRows ? finalize_down_kernel<9> : finalize_down_kernel<3>;
+        e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
         if (e != cudaSuccess) return MLA_ERR_RUNTIME;
-        e = launch(finalize_down_kernel, grid, kRowThreads, fsmem, st, f1);
+        e = launch(fk, grid, kRowThreads, fsmem, st, f1);
         if (e != cudaSuccess) return MLA_ERR_RUNTIME;
         timing_mark(st, "f1_norm_rope_cache");
     }
