@@ -273,6 +273,155 @@ __global__ void __launch_bounds__(kRowThreads) finalize_down_kernel(const DownAr
         down_row<kRowThreads, ROWCOLS>(a, t, threadIdx.x, ys, red, gcq, gckv, CtaSync{});
 }
 
+// Warp-per-token variant of the row work for many tokens (one k-range slot): each lane keeps
+// its columns of the fp32 row in registers (column pairs 2*lane + 64*k), the two sums of
+// squares and the int8 absmax are warp reductions (fixed shuffle tree), and no block barrier is
+// needed, so that every row of a large call can be in flight at once.  Limits: Hcq <= 64 *
+// kWQ, Hckv <= 64 * kWKV, Hcq and Hckv multiples of 64, Dr = 64.
+constexpr int kWQ = 32;    // column pairs per lane of c^Q: Hcq <= 2048
+constexpr int kWKV = 8;    // column pairs per lane of c^KV: Hckv <= 512
+constexpr int kWarpRowThreads = 128;
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(kWarpRowThreads) finalize_down_warp_kernel(const DownArgs a) {
+    pdl_launch_dependents();
+    prefetch_down_inputs(a, threadIdx.x, kWarpRowThreads);
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
+    if (t >= a.T) return;   // whole warp
+    const int nq = a.Hcq / 64, nkv = a.Hckv / 64, h = a.Dr / 2;
+    const float* src = a.src.p + (size_t)t * a.src.ncols;
+    const long long slot = a.nslots > 0 ? a.cache_index[t] : -1;
+    const float sx = a.scale_x ? a.scale_x[t] : 1.f;
+    // loads: the whole row of this token, every load in flight together
+    float2 yq[kWQ], ykv[kWKV];
+#pragma unroll
+    for (int k = 0; k < kWQ; ++k)
+        if (k < nq) yq[k] = __ldcs(reinterpret_cast<const float2*>(src + 2 * lane + 64 * k));
+#pragma unroll
+    for (int k = 0; k < kWKV; ++k)
+        if (k < nkv) ykv[k] = __ldcs(reinterpret_cast<const float2*>(src + a.Hcq + 2 * lane + 64 * k));
+    float kr0 = __ldcs(src + a.Hcq + a.Hckv + lane), kr1 = __ldcs(src + a.Hcq + a.Hckv + lane + h);
+    const float cos0 = __bfloat162float(a.rope_cos[(size_t)t * a.Dr + lane]);
+    const float cos1 = __bfloat162float(a.rope_cos[(size_t)t * a.Dr + lane + h]);
+    const float sin0 = __bfloat162float(a.rope_sin[(size_t)t * a.Dr + lane]);
+    const float sin1 = __bfloat162float(a.rope_sin[(size_t)t * a.Dr + lane + h]);
+    if (a.scale_x) {
+#pragma unroll
+        for (int k = 0; k < kWQ; ++k)
+            if (k < nq) {
+                const int c = 2 * lane + 64 * k;
+                yq[k].x *= sx * a.scale_w_dq[c];
+                yq[k].y *= sx * a.scale_w_dq[c + 1];
+            }
+#pragma unroll
+        for (int k = 0; k < kWKV; ++k)
+            if (k < nkv) {
+                const int c = 2 * lane + 64 * k;
+                ykv[k].x *= sx * a.scale_w_dkvkr[c];
+                ykv[k].y *= sx * a.scale_w_dkvkr[c + 1];
+            }
+        kr0 *= sx * a.scale_w_dkvkr[a.Hckv + lane];
+        kr1 *= sx * a.scale_w_dkvkr[a.Hckv + lane + h];
+    }
+    float sq = 0.f, skv = 0.f;
+#pragma unroll
+    for (int k = 0; k < kWQ; ++k)
+        if (k < nq) sq += yq[k].x * yq[k].x + yq[k].y * yq[k].y;
+#pragma unroll
+    for (int k = 0; k < kWKV; ++k)
+        if (k < nkv) skv += ykv[k].x * ykv[k].x + ykv[k].y * ykv[k].y;
+    sq = warp_sum_f(sq);
+    skv = warp_sum_f(skv);
+    // RmsNorm: gamma * y / sqrt(mean(y^2) + eps), epsilon inside the root.
+    const float inv_q = 1.f / sqrtf(sq / (float)a.Hcq + a.eps_cq);
+    const float inv_kv = 1.f / sqrtf(skv / (float)a.Hckv + a.eps_ckv);
+
+    __nv_bfloat16* cq = a.c_q + (size_t)t * a.Hcq;
+    if (!a.cq_quant) {
+#pragma unroll
+        for (int k = 0; k < kWQ; ++k)
+            if (k < nq) {
+                const int c = 2 * lane + 64 * k;
+                const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(a.gamma_cq + c);
+                *reinterpret_cast<__nv_bfloat162*>(cq + c) =
+                    __floats2bfloat162_rn(__low2float(g2) * yq[k].x * inv_q, __high2float(g2) * yq[k].y * inv_q);
+            }
+    } else {
+        // per-token dynamic int8 codes of c^Q (times the smooth scales when given)
+        float m = 0.f;
+#pragma unroll
+        for (int k = 0; k < kWQ; ++k)
+            if (k < nq) {
+                const int c = 2 * lane + 64 * k;
+                const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(a.gamma_cq + c);
+                float u0 = __low2float(g2) * yq[k].x * inv_q, u1 = __high2float(g2) * yq[k].y * inv_q;
+                if (a.smooth_cq) {
+                    u0 *= a.smooth_cq[c];
+                    u1 *= a.smooth_cq[c + 1];
+                }
+                yq[k] = make_float2(u0, u1);
+                m = fmaxf(m, fmaxf(fabsf(u0), fabsf(u1)));
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float scale = m / 127.f;
+#pragma unroll
+        for (int k = 0; k < kWQ; ++k)
+            if (k < nq) {
+                const int c = 2 * lane + 64 * k;
+                const int q0 = scale > 0.f ? quant_i8(__fdiv_rn(yq[k].x, scale)) : 0;
+                const int q1 = scale > 0.f ? quant_i8(__fdiv_rn(yq[k].y, scale)) : 0;
+                *reinterpret_cast<__nv_bfloat162*>(cq + c) = __halves2bfloat162(__int2bfloat16_rn(q0), __int2bfloat16_rn(q1));
+            }
+        if (lane == 0) a.c_q_scale[t] = scale;
+    }
+
+    if (a.nslots <= 0) return;
+    if (slot < 0 || slot >= a.nslots) {
+        if (lane == 0) atomicOr(a.status, kStatusCacheIndexRange);
+        return;
+    }
+    if (a.kv_int8) {
+        int8_t* d = reinterpret_cast<int8_t*>(a.kv_cache) + slot * a.Hckv;
+#pragma unroll
+        for (int k = 0; k < kWKV; ++k)
+            if (k < nkv) {
+                const int c = 2 * lane + 64 * k;
+                d[c] = (int8_t)quant_i8(__bfloat162float(a.gamma_ckv[c]) * ykv[k].x * inv_kv * a.quant_scale_ckv[c]);
+                d[c + 1] = (int8_t)quant_i8(__bfloat162float(a.gamma_ckv[c + 1]) * ykv[k].y * inv_kv * a.quant_scale_ckv[c + 1]);
+            }
+    } else {
+        __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(a.kv_cache) + slot * a.Hckv;
+#pragma unroll
+        for (int k = 0; k < kWKV; ++k)
+            if (k < nkv) {
+                const int c = 2 * lane + 64 * k;
+                const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(a.gamma_ckv + c);
+                *reinterpret_cast<__nv_bfloat162*>(d + c) =
+                    __floats2bfloat162_rn(__low2float(g2) * ykv[k].x * inv_kv, __high2float(g2) * ykv[k].y * inv_kv);
+            }
+    }
+    // "half" RoPE of k^R: lane j holds the pair (j, j + Dr/2)
+    const float o0 = kr0 * cos0 - kr1 * sin0;
+    const float o1 = kr1 * cos1 + kr0 * sin1;
+    if (a.kr_int8) {
+        int8_t* d = reinterpret_cast<int8_t*>(a.kr_cache) + slot * a.Dr;
+        d[lane] = (int8_t)quant_i8(o0 * a.quant_scale_ckr[lane]);
+        d[lane + h] = (int8_t)quant_i8(o1 * a.quant_scale_ckr[lane + h]);
+    } else {
+        __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(a.kr_cache) + slot * a.Dr;
+        d[lane] = __float2bfloat16_rn(o0);
+        d[lane + h] = __float2bfloat16_rn(o1);
+    }
+}
+
 struct UpArgs {
     int T, N, D, Dr;
     PartialSrc src;                     // T x N * (D + Dr)

@@ -697,7 +697,14 @@ mla_status run(const Launched& L) {
     timing_mark(st, "k1_down_proj");
 
     // ---- F1: RmsNorm, RoPE(k^R), cache writes, c^Q
-    {
+    if (T > kDecodeRows && p.g1.ksplit == 1 && d.Dr == 64 && d.Hcq % 64 == 0 && d.Hckv % 64 == 0 &&
+        d.Hcq <= 64 * kWQ && d.Hckv <= 64 * kWKV) {
+        // many tokens: one warp per token, the row in registers
+        const int wpc = kWarpRowThreads / 32;
+        e = launch(finalize_down_warp_kernel, (T + wpc - 1) / wpc, kWarpRowThreads, 0, st, f1);
+        if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+        timing_mark(st, "f1_norm_rope_cache");
+    } else {
         const int grid = T < 16 * L.sms ? T : 16 * L.sms;
         const size_t fsmem = down_smem_bytes((int)d.Hcq, (int)d.Hckv, (int)d.Dr);
         // decode-sized T: every partial load of a row in flight at once; many rows: fewer, so

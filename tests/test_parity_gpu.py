@@ -181,6 +181,19 @@ def test_tile_path_ragged(T):
     case("decode_t32", sample=24, T=T, block_num=8).check_all()
 
 
+def test_int8_full_quant_many_tokens():
+    """int8 inputs and int8 kv cache / q^N with T above the decode sizes: the warp-per-token
+    row pass with its dequant scales, int8 c^Q codes and int8 cache rows."""
+    case("int8_t64", sample=24, T=300, block_num=8).check_all()
+
+
+def test_partial_quant_many_tokens():
+    """Partial quantisation (int8 W^UqQr, smooth scales, int8 kv and kr caches) with T above the
+    decode sizes."""
+    case("decode_t32", sample=24, T=300, block_num=8, uqqr_int8=True, smooth=True, kv_int8=True,
+         kr_int8=True, ckv_reciprocal=True).check_all()
+
+
 def test_tiny_shapes_tile_path():
     """T above the split threshold with small heads: tile GEMMs, fp32 rows, row-wise finalize."""
     case("tiny", T=300, block_num=32).check_all()
