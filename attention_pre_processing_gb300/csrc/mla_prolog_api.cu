@@ -278,9 +278,10 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     const int64_t T = d.T;
     p.ncols1 = d.Hcq + d.Hckv + d.Dr;
     p.ncols2 = d.N * (d.D + d.Dr);
-    // Down-projection: at decode, 64-column tiles x k ranges; two 128-row sub-tiles or
-    // prefill use 192-column tiles.
-    plan_gemm(p.g1, T, p.ncols1, d.He, sms, T <= 128 ? 64 : 192, true);
+    // Down-projection: at decode, 64-column tiles x k ranges; two 128-row sub-tiles use
+    // 192-column tiles; prefill 256-column tiles (2112 columns: nine tiles per 256 rows, so that
+    // 8192 tokens make two waves on 152 SMs instead of three).
+    plan_gemm(p.g1, T, p.ncols1, d.He, sms, T <= 128 ? 64 : (T <= kDecodeRows ? 192 : 256), true);
     // Up-projection: one head (192 columns) per tile, full K, fused RoPE epilogue.
     plan_gemm(p.g2, T, p.ncols2, d.Hcq, sms, 192, false);
     p.g2_fused = d.D == 128 && d.Dr == 64;
@@ -691,8 +692,10 @@ mla_status run(const Launched& L) {
     if (p.g1.bn == 64)
         e = launch_gemm<64, 1, 32, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
     else
-        e = g1.tma_out ? launch_gemm<192, 2, 4, EPI_F32, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
-                       : launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+        e = p.g1.bn == 256 ? (g1.tma_out ? launch_gemm<256, 2, 4, EPI_F32, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
+                                         : launch_gemm<256, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1))
+                           : (g1.tma_out ? launch_gemm<192, 2, 4, EPI_F32, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
+                                         : launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1));
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k1_down_proj");
 
