@@ -467,6 +467,69 @@ __device__ __forceinline__ void epilogue_qrope_tma(const GemmArgs& a, const Unit
     }
 }
 
+// Up-projection tiles of BN columns that need not align with heads (D = 128, Dr = 64): the
+// 192 columns of head h are three 64-column blocks, the first two q^C, the third W^QR, so every
+// 64-column block of a tile is wholly q^C or wholly rope, and the RoPE pairs (j, j + 32) of a
+// rope block lie in the same block.  Each block goes through shared memory and a TMA store into
+// the (T, N*128) or (T, N*64) view.
+template <int BN, int MSUB, int OUTB>
+__device__ __forceinline__ void epilogue_qrope_blocks_tma(const GemmArgs& a, const Unit& u, const TmemSrc& src,
+                                                          int q, OutStage<OUTB>& out, const CUtensorMap* map_c,
+                                                          const CUtensorMap* map_r) {
+    constexpr int DR = 64;
+#pragma unroll 1
+    for (int ms = 0; ms < MSUB; ++ms) {
+        const int row0 = u.m_tile * MSUB * 128 + ms * 128 + q * 32;
+        if (row0 >= a.T) continue;   // warp-uniform
+        const int row = row0 + out.lane;
+        const bool valid = row < a.T;
+#pragma unroll 1
+        for (int blk = 0; blk < BN / 64; ++blk) {
+            const int b = (u.n_tile * BN) / 64 + blk;   // global 64-column block
+            if (b * 64 >= a.ncols) break;               // uniform across the warp
+            const int head = b / 3, part = b % 3;
+            float v0[32], v1[32];
+            src.load(ms, BN, 64 * blk, v0);
+            src.load(ms, BN, 64 * blk + 32, v1);
+            uint32_t w[32];
+            if (part < 2) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    w[i] = pack_bf16(v0[2 * i], v0[2 * i + 1]);
+                    w[16 + i] = pack_bf16(v1[2 * i], v1[2 * i + 1]);
+                }
+                out.put(w, head * 128 + part * 64, row0, map_c);
+            } else {
+                const uint4* cp = reinterpret_cast<const uint4*>(a.rope_cos + (size_t)(valid ? row : 0) * DR);
+                const uint4* sp = reinterpret_cast<const uint4*>(a.rope_sin + (size_t)(valid ? row : 0) * DR);
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const uint4 c0 = __ldg(cp + qq), c1 = __ldg(cp + qq + 4), s0 = __ldg(sp + qq), s1 = __ldg(sp + qq + 4);
+                    const uint32_t cw0[4] = {c0.x, c0.y, c0.z, c0.w}, cw1[4] = {c1.x, c1.y, c1.z, c1.w};
+                    const uint32_t sw0[4] = {s0.x, s0.y, s0.z, s0.w}, sw1[4] = {s1.x, s1.y, s1.z, s1.w};
+                    float o0[8], o1[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int jj = qq * 8 + e;
+                        const float cj = (e & 1) ? bf16_hi(cw0[e >> 1]) : bf16_lo(cw0[e >> 1]);
+                        const float sj = (e & 1) ? bf16_hi(sw0[e >> 1]) : bf16_lo(sw0[e >> 1]);
+                        const float ch = (e & 1) ? bf16_hi(cw1[e >> 1]) : bf16_lo(cw1[e >> 1]);
+                        const float sh = (e & 1) ? bf16_hi(sw1[e >> 1]) : bf16_lo(sw1[e >> 1]);
+                        o0[e] = v0[jj] * cj - v1[jj] * sj;
+                        o1[e] = v1[jj] * ch + v0[jj] * sh;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        w[qq * 4 + e] = pack_bf16(o0[2 * e], o0[2 * e + 1]);
+                        w[16 + qq * 4 + e] = pack_bf16(o1[2 * e], o1[2 * e + 1]);
+                    }
+                }
+                out.put(w, head * DR, row0, map_r);
+            }
+        }
+    }
+}
+
 template <int BN, int OUTB>
 __device__ __forceinline__ void epilogue_qn_tma(const GemmArgs& a, const Unit& u, const TmemSrc& src, int q,
                                                 OutStage<OUTB>& out) {
@@ -804,7 +867,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     epilogue_f32<BN, MSUB>(args, row0, u.n_tile, u.ks, tsrc);
                 }
             } else if constexpr (EPI == EPI_QROPE) {
-                if constexpr (OUTB > 0) {
+                if constexpr (BN != 192) {
+                    static_assert(OUTB > 0, "head-unaligned tiles store through TMA");
+                    epilogue_qrope_blocks_tma<BN, MSUB, OUTB>(args, u, tsrc, q, ostage, &map_o, &map_o2);
+                } else if constexpr (OUTB > 0) {
                     if (args.tma_out)
                         epilogue_qrope_tma<MSUB, OUTB>(args, u, tsrc, q, ostage, &map_o, &map_o2);
                     else

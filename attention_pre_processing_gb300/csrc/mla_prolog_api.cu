@@ -227,6 +227,7 @@ struct GemmPlan {
 struct Plan {
     GemmPlan g1, g2, g3;
     bool g2_fused = false;   // K2 epilogue does RoPE and q^C (no finalize_up)
+    bool g2_wide = false;    // K2 with 256-column tiles (prefill)
     bool persist = false;    // decode-sized bf16 call: the one persistent kernel of decode_persist.cuh
     int p_n1 = 0, p_s1 = 0, p_wst = 0, p_arows = 0;
     size_t p_smem = 0, off_pss = 0, off_pykv = 0, off_pbar = 0;
@@ -282,9 +283,12 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     // 192-column tiles; prefill 256-column tiles (2112 columns: nine tiles per 256 rows, so that
     // 8192 tokens make two waves on 152 SMs instead of three).
     plan_gemm(p.g1, T, p.ncols1, d.He, sms, T <= 128 ? 64 : (T <= kDecodeRows ? 192 : 256), true);
-    // Up-projection: one head (192 columns) per tile, full K, fused RoPE epilogue.
-    plan_gemm(p.g2, T, p.ncols2, d.Hcq, sms, 192, false);
+    // Up-projection: one head (192 columns) per tile, full K, fused RoPE epilogue; prefill with
+    // the 128 + 64 head layout uses 256-column tiles (their epilogue sorts 64-column blocks into
+    // q^C and rope blocks).
     p.g2_fused = d.D == 128 && d.Dr == 64;
+    p.g2_wide = p.g2_fused && T > kDecodeRows && p.ncols2 % 256 == 0 && !sc.uqqr_i8;
+    plan_gemm(p.g2, T, p.ncols2, d.Hcq, sms, p.g2_wide ? 256 : 192, false);
     // K3: per head, 128-row tiles; an int8 output needs the whole Hckv row in one tile.
     p.g3.bn = sc.q_i8 ? 512 : 256;
     p.g3.kblocks = (int)((d.D + kBK - 1) / kBK);
@@ -737,6 +741,7 @@ mla_status run(const Launched& L) {
         const uint32_t box[2] = {64, 32};
         g2.tma_out = encode_map(&mO2c, qc, 2, dc, sc2, box) && encode_map(&mO2r, a.qrope->data, 2, dr, sr, box) ? 1 : 0;
     }
+    if (p.g2_wide && !g2.tma_out) return MLA_ERR_RUNTIME;   // 256-column tiles store only through TMA
     g2.N = (int)d.N;
     g2.q_c = qc;
     g2.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
@@ -747,9 +752,11 @@ mla_status run(const Launched& L) {
     g2.out_f32 = reinterpret_cast<float*>(ws + p.off_y2);
     if (p.g2_fused) {
         e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2)
-                             : (g2.tma_out ? launch_gemm<192, 2, 4, EPI_QROPE, 2>(p.g2.grid, st, mA2, mB2, mB2, g2,
-                                                                                 &mO2c, &mO2r)
-                                           : launch_gemm<192, 2, 4, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2));
+                             : (p.g2_wide && g2.tma_out
+                                    ? launch_gemm<256, 2, 4, EPI_QROPE, 2>(p.g2.grid, st, mA2, mB2, mB2, g2, &mO2c, &mO2r)
+                                    : (g2.tma_out ? launch_gemm<192, 2, 4, EPI_QROPE, 2>(p.g2.grid, st, mA2, mB2, mB2, g2,
+                                                                                       &mO2c, &mO2r)
+                                                  : launch_gemm<192, 2, 4, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2)));
     } else {
         e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2)
                              : launch_gemm<192, 2, 4, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2);
