@@ -69,7 +69,10 @@ struct GemmArgs {
     __nv_bfloat16* q_out_bf16;     // (T, N, Hckv)
     int8_t* q_out_i8;              // (T, N, Hckv)
     float* q_scale;                // (T, N)
-    int tma_out;                   // EPI_QN: store q^N through shared memory with TMA (map_o)
+    int tma_out;                   // store the output through shared memory with TMA (map_o, map_o2)
+    int a_one_box;                 // one A box spans all MSUB x 128 rows (map_a box height MSUB*128)
+    int b_blocks;                  // the B maps are 3D (64 columns, k, 64-column blocks): one box
+                                   // brings all BN/64 column blocks of a k-block
     uint32_t* status;
 };
 
@@ -606,6 +609,15 @@ __device__ __forceinline__ void load_b(const GemmArgs& a, const Unit& u, int kb,
     } else {
         c0 = u.n_tile * BN;
     }
+    if (!a.head_mode && a.b_blocks) {
+        // one box: BN/64 column blocks of 64 x (64 * KPS), laid out block after block (a tile
+        // never straddles b_split_col)
+        if (c0 < a.b_split_col)
+            tma_load_3d(dst, b0, bar, 0, kb * kBK, c0 / 64, pol);
+        else
+            tma_load_3d(dst, b1, bar, 0, kb * kBK, (c0 - a.b_split_col) / 64, pol);
+        return;
+    }
 #pragma unroll
     for (int j = 0; j < BN / 64; ++j) {
         const int col = c0 + 64 * j;
@@ -624,6 +636,10 @@ template <int MSUB>
 __device__ __forceinline__ void load_a(const GemmArgs& a, const Unit& u, int kb, uint32_t dst, int a_box,
                                        uint32_t bar, const CUtensorMap* map, uint64_t pol) {
     const int head = a.head_mode ? u.n_tile / a.tiles_per_head : 0;
+    if (!a.head_mode && a.a_one_box) {
+        tma_load_2d(dst, map, bar, kb * kBK, u.m_tile * MSUB * 128, pol);
+        return;
+    }
 #pragma unroll
     for (int ms = 0; ms < MSUB; ++ms) {
         const int r0 = (u.m_tile * MSUB + ms) * 128;

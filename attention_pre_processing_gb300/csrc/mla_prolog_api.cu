@@ -407,6 +407,16 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint
     return encode_map(m, base, 2, dims, strides, box);
 }
 
+// Row-major (rows, cols) bf16 matrix viewed as (64 columns, rows, cols/64 column blocks): a box
+// {64, box_rows, nblk} brings nblk 64-column blocks of box_rows rows, block after block, in one
+// request (cols must be a multiple of 64).
+bool map_colblocks(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t nblk) {
+    const uint64_t dims[3] = {64, rows, cols / 64};
+    const uint64_t strides[2] = {cols * 2, 128};
+    const uint32_t box[3] = {64, box_rows, nblk};
+    return encode_map(m, base, 3, dims, strides, box);
+}
+
 // --------------------------------------------------------------------- timing
 
 struct Timing {
@@ -677,14 +687,22 @@ mla_status run(const Launched& L) {
     // Whole-K 256-row tiles store their fp32 rows through shared memory with TMA (32 x 32
     // boxes of the T x ncols1 matrix); k ranges (decode) use plain stores into their slots.
     const bool tma1 = p.g1.ksplit == 1 && p.g1.msub == 2 && p.ncols1 % 4 == 0;
-    const uint32_t b1_rows = 64;
-    if (!map_2d(&mA1, x_bf, d.T, d.He, (uint32_t)p.g1.a_box_rows) || !map_2d(&mB1a, wdq_bf, d.He, d.Hcq, b1_rows) ||
-        !map_2d(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, b1_rows))
+    // 256-column tiles: one 256-row activation box and one column-blocked weight box per k-block
+    const bool big1 = p.g1.bn == 256 && d.Hcq % 256 == 0 && (d.Hckv + d.Dr) % 64 == 0;
+    if (big1) {
+        if (!map_2d(&mA1, x_bf, d.T, d.He, 256) || !map_colblocks(&mB1a, wdq_bf, d.He, d.Hcq, 64, 4) ||
+            !map_colblocks(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64, 4))
+            return MLA_ERR_RUNTIME;
+    } else if (!map_2d(&mA1, x_bf, d.T, d.He, (uint32_t)p.g1.a_box_rows) || !map_2d(&mB1a, wdq_bf, d.He, d.Hcq, 64) ||
+               !map_2d(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64)) {
         return MLA_ERR_RUNTIME;
+    }
     GemmArgs g1 = gemm_args(p.g1, T, p.ncols1, status);
     g1.b_split_col = (int)d.Hcq;
     g1.clear_status = 1;
     g1.a_ready = sc.x_i8 ? 0 : 1;   // bf16 tokenX is read as passed; int8 is widened first
+    g1.a_one_box = big1 ? 1 : 0;
+    g1.b_blocks = big1 ? 1 : 0;
     CUtensorMap mO1;
     if (tma1) {
         const uint64_t dims[2] = {(uint64_t)p.ncols1, (uint64_t)d.T};
@@ -696,8 +714,9 @@ mla_status run(const Launched& L) {
     if (p.g1.bn == 64)
         e = launch_gemm<64, 1, 32, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
     else
-        e = p.g1.bn == 256 ? (g1.tma_out ? launch_gemm<256, 2, 4, EPI_F32, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
-                                         : launch_gemm<256, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1))
+        e = p.g1.bn == 256 ? (g1.tma_out && big1
+                                  ? launch_gemm<256, 2, 4, EPI_F32, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
+                                  : launch_gemm<256, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1))
                            : (g1.tma_out ? launch_gemm<192, 2, 4, EPI_F32, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
                                          : launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1));
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
@@ -728,10 +747,17 @@ mla_status run(const Launched& L) {
     CUtensorMap mA2, mB2;
     // 256-row tiles without dequant scales store q^C and q^R through shared memory with TMA.
     const bool tma2 = p.g2_fused && p.g2.msub == 2 && !sc.uqqr_i8;
-    if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
-        !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64))
+    // 256-column tiles: one 256-row activation box and one column-blocked weight box per k-block
+    if (p.g2_wide) {
+        if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, 256) || !map_colblocks(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64, 4))
+            return MLA_ERR_RUNTIME;
+    } else if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
+               !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64)) {
         return MLA_ERR_RUNTIME;
+    }
     GemmArgs g2 = gemm_args(p.g2, T, p.ncols2, status);
+    g2.a_one_box = p.g2_wide ? 1 : 0;
+    g2.b_blocks = p.g2_wide ? 1 : 0;
     CUtensorMap mO2c, mO2r;
     if (tma2) {
         const uint64_t dc[2] = {(uint64_t)d.N * d.D, (uint64_t)d.T};
