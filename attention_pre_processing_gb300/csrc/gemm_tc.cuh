@@ -30,7 +30,9 @@
 namespace mla {
 
 constexpr int kBK = 64;          // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 192;   // with one epilogue warp per TMEM lane quarter
+// Threads of a GEMM CTA with EPW epilogue warps per TMEM lane quarter.
+__host__ __device__ constexpr int gemm_threads(int epw) { return 64 + 128 * epw; }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr size_t kSmemLimit = 232448;             // 227 KB opt-in per CTA
 
@@ -79,9 +81,9 @@ struct GemmArgs {
 // OUTB: 4 KB staging buffers per epilogue warp for TMA stores of the output (0 = none).
 // KPS: k-blocks per pipeline stage.  With KPS = 2 a weight box spans 128 k rows (16 KB): the
 // TMA engine moves far more bytes per box request from L2 than with 64-row boxes.
-template <int BN, int MSUB, int MAXST, int OUTB = 0, int KPS = 1>
+template <int BN, int MSUB, int MAXST, int OUTB = 0, int KPS = 1, int EPW = 1>
 struct GemmCfg {
-    static constexpr int kOutBytes = 4 * OUTB * 4096;
+    static constexpr int kOutBytes = 4 * EPW * OUTB * 4096;
     static constexpr int kBStage = BN * kBK * 2 * KPS;      // BN/64 boxes of 64 cols x 64*KPS rows
     static constexpr int kAcc = MSUB * BN;                  // TMEM columns per accumulator set
     static constexpr int kNBuf = (2 * kAcc <= 512) ? 2 : 1;
@@ -146,6 +148,22 @@ __device__ __forceinline__ int quant_i8(float v) {
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// The same over the NT epilogue threads of a CTA with more than four epilogue warps.
+template <int NT>
+__device__ __forceinline__ void epi_bar_n() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
+template <int NT>
+__device__ __forceinline__ bool epi_any_n(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "n"(NT)
+        : "memory");
+    return r != 0;
+}
 
 // Barrier over the 128 epilogue threads that also ORs a flag: every thread gets the same answer.
 __device__ __forceinline__ bool epi_any(bool v) {
@@ -385,15 +403,15 @@ struct OutStage {
 // fp32 product rows (EPI_F32, ksplit = 1) through shared memory and TMA stores: 32-row x
 // 32-column (128-byte) boxes of the T x ncols matrix; rows and columns past its extent are not
 // written.
-template <int BN, int MSUB, int OUTB>
+template <int BN, int MSUB, int OUTB, int EPW = 1>
 __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const Unit& u, const TmemSrc& src, int q,
-                                                 OutStage<OUTB>& out) {
+                                                 OutStage<OUTB>& out, int part = 0) {
 #pragma unroll 1
     for (int ms = 0; ms < MSUB; ++ms) {
         const int row0 = u.m_tile * MSUB * 128 + ms * 128 + q * 32;
         if (row0 >= a.T) continue;   // warp-uniform
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
+        for (int ch = part; ch < BN / 32; ch += EPW) {   // this warp's share of the columns
             const int col = u.n_tile * BN + ch * 32;
             if (col >= a.ncols) break;
             uint32_t w[32];
@@ -475,10 +493,10 @@ __device__ __forceinline__ void epilogue_qrope_tma(const GemmArgs& a, const Unit
 // 64-column block of a tile is wholly q^C or wholly rope, and the RoPE pairs (j, j + 32) of a
 // rope block lie in the same block.  Each block goes through shared memory and a TMA store into
 // the (T, N*128) or (T, N*64) view.
-template <int BN, int MSUB, int OUTB>
+template <int BN, int MSUB, int OUTB, int EPW = 1>
 __device__ __forceinline__ void epilogue_qrope_blocks_tma(const GemmArgs& a, const Unit& u, const TmemSrc& src,
                                                           int q, OutStage<OUTB>& out, const CUtensorMap* map_c,
-                                                          const CUtensorMap* map_r) {
+                                                          const CUtensorMap* map_r, int part = 0) {
     constexpr int DR = 64;
 #pragma unroll 1
     for (int ms = 0; ms < MSUB; ++ms) {
@@ -487,7 +505,7 @@ __device__ __forceinline__ void epilogue_qrope_blocks_tma(const GemmArgs& a, con
         const int row = row0 + out.lane;
         const bool valid = row < a.T;
 #pragma unroll 1
-        for (int blk = 0; blk < BN / 64; ++blk) {
+        for (int blk = part; blk < BN / 64; blk += EPW) {   // this warp's share of the blocks
             const int b = (u.n_tile * BN) / 64 + blk;   // global 64-column block
             if (b * 64 >= a.ncols) break;               // uniform across the warp
             const int head = b / 3, part = b % 3;
@@ -652,12 +670,15 @@ __device__ __forceinline__ void load_a(const GemmArgs& a, const Unit& u, int kb,
 
 // ---------------------------------------------------------------------- kernel
 
-template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0, int KPS = 1>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0, int KPS = 1, int EPW = 1>
+__global__ void __launch_bounds__(gemm_threads(EPW), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                    const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_o,
                    const __grid_constant__ CUtensorMap map_o2, const GemmArgs args) {
-    using C = GemmCfg<BN, MSUB, MAXST, OUTB, KPS>;
+    using C = GemmCfg<BN, MSUB, MAXST, OUTB, KPS, EPW>;
+    constexpr int kEpiThreads = 128 * EPW;
+    static_assert(EPW == 1 || (OUTB > 0 && (EPI == EPI_F32 || (EPI == EPI_QROPE && BN != 192))),
+                  "split epilogues exist for TMA-stored fp32 rows and head-unaligned RoPE tiles");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -692,7 +713,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
-            mbar_init(smem_u32(&tempty[b]), 128);
+            mbar_init(smem_u32(&tempty[b]), kEpiThreads);
         }
         mbar_init(smem_u32(done), 1);
         *s_abort = 0;
@@ -840,6 +861,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue warps
         const int q = warp & 3;   // TMEM lane quarter this warp may access
+        const int part = (warp - 2) >> 2;   // which share of the columns (EPW warps per quarter)
         const int row_in = q * 32 + lane;
         OutStage<OUTB> ostage{sOut + (size_t)(warp - 2) * OUTB * 4096, 0, &map_o, lane};
         if constexpr (EPI == EPI_QROPE) {
@@ -867,14 +889,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 *s_abort = 1;
                 atomicOr(args.status, kStatusWaitTimeout);
             }
-            // The four epilogue warps stop together or not at all.
-            if (epi_any(!ok)) break;
+            // The epilogue warps stop together or not at all.
+            if (epi_any_n<kEpiThreads>(!ok)) break;
             __syncwarp();
             tc_fence_after();
             const TmemSrc tsrc{tmem_base + ((uint32_t)(q * 32) << 16) + b * C::kAcc};
             const int row0 = u.m_tile * MSUB * 128 + row_in;
             if constexpr (EPI == EPI_F32) {
-                if constexpr (OUTB > 0) {
+                if constexpr (EPW > 1) {
+                    epilogue_f32_tma<BN, MSUB, OUTB, EPW>(args, u, tsrc, q, ostage, part);
+                } else if constexpr (OUTB > 0) {
                     if (args.tma_out)
                         epilogue_f32_tma<BN, MSUB, OUTB>(args, u, tsrc, q, ostage);
                     else
@@ -885,7 +909,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             } else if constexpr (EPI == EPI_QROPE) {
                 if constexpr (BN != 192) {
                     static_assert(OUTB > 0, "head-unaligned tiles store through TMA");
-                    epilogue_qrope_blocks_tma<BN, MSUB, OUTB>(args, u, tsrc, q, ostage, &map_o, &map_o2);
+                    epilogue_qrope_blocks_tma<BN, MSUB, OUTB, EPW>(args, u, tsrc, q, ostage, &map_o, &map_o2, part);
                 } else if constexpr (OUTB > 0) {
                     if (args.tma_out)
                         epilogue_qrope_tma<MSUB, OUTB>(args, u, tsrc, q, ostage, &map_o, &map_o2);

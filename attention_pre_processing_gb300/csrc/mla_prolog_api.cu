@@ -478,11 +478,11 @@ cudaError_t launch(Kernel k, int grid, int block, size_t smem, cudaStream_t st, 
 }
 
 // Launches one GEMM instantiation; fills in the ring depth and dynamic shared memory.
-template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0, int KPS = 1>
+template <int BN, int MSUB, int MAXST, int EPI, int OUTB = 0, int KPS = 1, int EPW = 1>
 cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         GemmArgs args, const CUtensorMap* out = nullptr, const CUtensorMap* out2 = nullptr) {
-    using C = GemmCfg<BN, MSUB, MAXST, OUTB, KPS>;
-    auto k = gemm_tc_kernel<BN, MSUB, MAXST, EPI, OUTB, KPS>;
+    using C = GemmCfg<BN, MSUB, MAXST, OUTB, KPS, EPW>;
+    auto k = gemm_tc_kernel<BN, MSUB, MAXST, EPI, OUTB, KPS, EPW>;
     CUtensorMap mo, mo2;
     std::memset(&mo, 0, sizeof mo);
     std::memset(&mo2, 0, sizeof mo2);
@@ -493,7 +493,7 @@ cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const C
     const size_t smem = C::smem_bytes(args.stages, args.a_box_rows);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
     if (e != cudaSuccess) return e;
-    return launch(k, grid, kGemmThreads, smem, st, a, b0, b1, mo, mo2, args);
+    return launch(k, grid, gemm_threads(EPW), smem, st, a, b0, b1, mo, mo2, args);
 }
 
 struct Launched {
@@ -715,7 +715,7 @@ mla_status run(const Launched& L) {
         e = launch_gemm<64, 1, 32, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
     else
         e = p.g1.bn == 256 ? (g1.tma_out && big1
-                                  ? launch_gemm<256, 2, 4, EPI_F32, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
+                                  ? launch_gemm<256, 2, 4, EPI_F32, 1, 1, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
                                   : launch_gemm<256, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1))
                            : (g1.tma_out ? launch_gemm<192, 2, 4, EPI_F32, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
                                          : launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1));
@@ -779,7 +779,7 @@ mla_status run(const Launched& L) {
     if (p.g2_fused) {
         e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2)
                              : (p.g2_wide && g2.tma_out
-                                    ? launch_gemm<256, 2, 4, EPI_QROPE, 2>(p.g2.grid, st, mA2, mB2, mB2, g2, &mO2c, &mO2r)
+                                    ? launch_gemm<256, 2, 4, EPI_QROPE, 1, 1, 2>(p.g2.grid, st, mA2, mB2, mB2, g2, &mO2c, &mO2r)
                                     : (g2.tma_out ? launch_gemm<192, 2, 4, EPI_QROPE, 2>(p.g2.grid, st, mA2, mB2, mB2, g2,
                                                                                        &mO2c, &mO2r)
                                                   : launch_gemm<192, 2, 4, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2)));
