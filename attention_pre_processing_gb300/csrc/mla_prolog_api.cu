@@ -289,6 +289,15 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     p.g2_fused = d.D == 128 && d.Dr == 64;
     p.g2_wide = p.g2_fused && T > kDecodeRows && p.ncols2 % 256 == 0 && !sc.uqqr_i8;
     plan_gemm(p.g2, T, p.ncols2, d.Hcq, sms, p.g2_wide ? 256 : 192, false);
+    if (p.g2_wide) {
+        // 128-row tiles: two 256-column accumulators fit in tensor memory, so each tile's
+        // epilogue overlaps the next tile's main loop
+        p.g2.msub = 1;
+        p.g2.m_tiles = (int)((T + 127) / 128);
+        p.g2.a_box_rows = 128;
+        const long long tiles = (long long)p.g2.m_tiles * p.g2.n_tiles;
+        p.g2.grid = (int)(tiles < sms ? tiles : sms);
+    }
     // K3: per head, 128-row tiles; an int8 output needs the whole Hckv row in one tile.
     p.g3.bn = sc.q_i8 ? 512 : 256;
     p.g3.kblocks = (int)((d.D + kBK - 1) / kBK);
@@ -745,11 +754,11 @@ mla_status run(const Launched& L) {
 
     // ---- K2: up-projection c^Q . W^UqQr -> RoPE(q^R) and q^C
     CUtensorMap mA2, mB2;
-    // 256-row tiles without dequant scales store q^C and q^R through shared memory with TMA.
-    const bool tma2 = p.g2_fused && p.g2.msub == 2 && !sc.uqqr_i8;
+    // Prefill tiles without dequant scales store q^C and q^R through shared memory with TMA.
+    const bool tma2 = p.g2_fused && (p.g2.msub == 2 || p.g2_wide) && !sc.uqqr_i8;
     // 256-column tiles: one 256-row activation box and one column-blocked weight box per k-block
     if (p.g2_wide) {
-        if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, 256) || !map_colblocks(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64, 4))
+        if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, 128) || !map_colblocks(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64, 4))
             return MLA_ERR_RUNTIME;
     } else if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
                !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64)) {
@@ -777,12 +786,13 @@ mla_status run(const Launched& L) {
     g2.col_scale = col_scale;
     g2.out_f32 = reinterpret_cast<float*>(ws + p.off_y2);
     if (p.g2_fused) {
-        e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2)
-                             : (p.g2_wide && g2.tma_out
-                                    ? launch_gemm<256, 2, 4, EPI_QROPE, 1, 1, 2>(p.g2.grid, st, mA2, mB2, mB2, g2, &mO2c, &mO2r)
-                                    : (g2.tma_out ? launch_gemm<192, 2, 4, EPI_QROPE, 2>(p.g2.grid, st, mA2, mB2, mB2, g2,
-                                                                                       &mO2c, &mO2r)
-                                                  : launch_gemm<192, 2, 4, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2)));
+        if (p.g2_wide)
+            e = launch_gemm<256, 1, 4, EPI_QROPE, 1, 1, 2>(p.g2.grid, st, mA2, mB2, mB2, g2, &mO2c, &mO2r);
+        else if (p.g2.msub == 1)
+            e = launch_gemm<192, 1, 16, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2);
+        else
+            e = g2.tma_out ? launch_gemm<192, 2, 4, EPI_QROPE, 2>(p.g2.grid, st, mA2, mB2, mB2, g2, &mO2c, &mO2r)
+                           : launch_gemm<192, 2, 4, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2);
     } else {
         e = (p.g2.msub == 1) ? launch_gemm<192, 1, 16, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2)
                              : launch_gemm<192, 2, 4, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2);
