@@ -23,6 +23,7 @@
 #include "decode_persist.cuh"
 #include "finalize.cuh"
 #include "gemm_tc.cuh"
+#include "gemm_pair.cuh"
 
 using namespace mla;
 
@@ -227,7 +228,7 @@ struct GemmPlan {
 struct Plan {
     GemmPlan g1, g2, g3;
     bool g2_fused = false;   // K2 epilogue does RoPE and q^C (no finalize_up)
-    bool g2_wide = false;    // K2 with 256-column tiles (prefill)
+    bool g2_wide = false;    // K2 with 256 x 256 tiles on SM pairs (prefill)
     bool persist = false;    // decode-sized bf16 call: the one persistent kernel of decode_persist.cuh
     int p_n1 = 0, p_s1 = 0, p_wst = 0, p_arows = 0;
     size_t p_smem = 0, off_pss = 0, off_pykv = 0, off_pbar = 0;
@@ -284,19 +285,16 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     // 8192 tokens make two waves on 152 SMs instead of three).
     plan_gemm(p.g1, T, p.ncols1, d.He, sms, T <= 128 ? 64 : (T <= kDecodeRows ? 192 : 256), true);
     // Up-projection: one head (192 columns) per tile, full K, fused RoPE epilogue; prefill with
-    // the 128 + 64 head layout uses 256-column tiles (their epilogue sorts 64-column blocks into
-    // q^C and rope blocks).
+    // the 128 + 64 head layout uses 256 x 256 tiles on SM pairs (their epilogue sorts 64-column
+    // blocks into q^C and rope blocks).
     p.g2_fused = d.D == 128 && d.Dr == 64;
     p.g2_wide = p.g2_fused && T > kDecodeRows && p.ncols2 % 256 == 0 && !sc.uqqr_i8;
     plan_gemm(p.g2, T, p.ncols2, d.Hcq, sms, p.g2_wide ? 256 : 192, false);
     if (p.g2_wide) {
-        // 128-row tiles: two 256-column accumulators fit in tensor memory, so each tile's
-        // epilogue overlaps the next tile's main loop
-        p.g2.msub = 1;
-        p.g2.m_tiles = (int)((T + 127) / 128);
+        p.g2.msub = 2;
+        p.g2.m_tiles = (int)((T + 255) / 256);
         p.g2.a_box_rows = 128;
-        const long long tiles = (long long)p.g2.m_tiles * p.g2.n_tiles;
-        p.g2.grid = (int)(tiles < sms ? tiles : sms);
+        p.g2.grid = 0;   // pairs: sized at launch from the co-resident clusters
     }
     // K3: per head, 128-row tiles; an int8 output needs the whole Hckv row in one tile.
     p.g3.bn = sc.q_i8 ? 512 : 256;
@@ -504,6 +502,57 @@ cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const C
     if (e != cudaSuccess) return e;
     return launch(k, grid, gemm_threads(EPW), smem, st, a, b0, b1, mo, mo2, args);
 }
+
+// Launches one pair-CTA GEMM instantiation (clusters of two CTAs): as many pairs as the GPU
+// holds at once, at most one per 256-row tile.
+template <int BN, int MAXST, int EPI, int OUTB, int EPW, int KPS>
+cudaError_t launch_gemm_pair(cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                             GemmArgs args, const CUtensorMap& out, const CUtensorMap& out2) {
+    using C = PairCfg<BN, MAXST, OUTB, EPW, KPS>;
+    auto k = gemm_pair_kernel<BN, MAXST, EPI, OUTB, EPW, KPS>;
+    if (args.kblocks % KPS != 0) return cudaErrorInvalidValue;
+    args.stages = C::max_stages();
+    if (args.stages < 2) return cudaErrorInvalidConfiguration;
+    const size_t smem = C::smem_bytes(args.stages);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3((unsigned)gemm_threads(EPW));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_timing.enabled ? 1 : 2;
+    // co-resident pairs of this instantiation on this device (queried once per device)
+    static int s_pairs[64] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (s_pairs[dev] == 0) {
+        int clusters = 0;
+        cfg.gridDim = dim3(2);
+        e = cudaOccupancyMaxActiveClusters(&clusters, k, &cfg);
+        if (e != cudaSuccess) return e;
+        if (clusters < 1) return cudaErrorInvalidConfiguration;
+        s_pairs[dev] = clusters;
+    }
+    const long long units = (long long)args.m_tiles * args.n_tiles;
+    const int pairs = (int)(units < s_pairs[dev] ? units : s_pairs[dev]);
+    if (pairs < 1) return cudaSuccess;
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    return cudaLaunchKernelEx(&cfg, k, a, b0, b1, out, out2, args);
+}
+
+constexpr int kPairKps2 = 2;   // k-blocks per stage of the prefill up-projection on SM pairs
 
 struct Launched {
     const Args* a;
@@ -756,9 +805,11 @@ mla_status run(const Launched& L) {
     CUtensorMap mA2, mB2;
     // Prefill tiles without dequant scales store q^C and q^R through shared memory with TMA.
     const bool tma2 = p.g2_fused && (p.g2.msub == 2 || p.g2_wide) && !sc.uqqr_i8;
-    // 256-column tiles: one 256-row activation box and one column-blocked weight box per k-block
+    // SM-pair tiles: per k-block each CTA takes one 128-row activation box and one box of its
+    // 128 weight columns (two 64-column blocks)
     if (p.g2_wide) {
-        if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, 128) || !map_colblocks(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64, 4))
+        if (!map_colblocks(&mA2, ws + p.off_cq, d.T, d.Hcq, 128, kPairKps2) ||
+            !map_colblocks(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64 * kPairKps2, 2))
             return MLA_ERR_RUNTIME;
     } else if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
                !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64)) {
@@ -787,7 +838,7 @@ mla_status run(const Launched& L) {
     g2.out_f32 = reinterpret_cast<float*>(ws + p.off_y2);
     if (p.g2_fused) {
         if (p.g2_wide)
-            e = launch_gemm<256, 1, 4, EPI_QROPE, 1, 1, 2>(p.g2.grid, st, mA2, mB2, mB2, g2, &mO2c, &mO2r);
+            e = launch_gemm_pair<256, 8, EPI_QROPE, 1, 2, kPairKps2>(st, mA2, mB2, mB2, g2, mO2c, mO2r);
         else if (p.g2.msub == 1)
             e = launch_gemm<192, 1, 16, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2);
         else
