@@ -58,13 +58,18 @@ struct PairCfg {
     }
 };
 
-// The idx-th 256-row tile of this pair: row tile fastest.
+// The idx-th 256-row tile of this pair: row tile fastest, or column tile fastest (n_fastest).
 __device__ __forceinline__ bool get_pair_unit(const GemmArgs& a, int idx, Unit& u) {
     const long long npairs = gridDim.x >> 1;
     const long long i = (long long)(blockIdx.x >> 1) + (long long)idx * npairs;
     if (i >= (long long)a.m_tiles * a.n_tiles) return false;
-    u.m_tile = (int)(i % a.m_tiles);
-    u.n_tile = (int)(i / a.m_tiles);
+    if (a.n_fastest) {
+        u.n_tile = (int)(i % a.n_tiles);
+        u.m_tile = (int)(i / a.n_tiles);
+    } else {
+        u.m_tile = (int)(i % a.m_tiles);
+        u.n_tile = (int)(i / a.m_tiles);
+    }
     u.kb0 = 0;
     u.kb1 = a.kblocks;
     u.ks = 0;

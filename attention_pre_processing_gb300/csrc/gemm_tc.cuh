@@ -75,6 +75,8 @@ struct GemmArgs {
     int a_one_box;                 // one A box spans all MSUB x 128 rows (map_a box height MSUB*128)
     int b_blocks;                  // the B maps are 3D (64 columns, k, 64-column blocks): one box
                                    // brings all BN/64 column blocks of a k-block
+    int n_fastest;                 // pair tiles: column tile fastest (the row tiles of A then come
+                                   // from HBM once, shared by the pairs of all column tiles)
     uint32_t* status;
 };
 

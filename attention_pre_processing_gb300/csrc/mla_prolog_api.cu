@@ -229,6 +229,7 @@ struct Plan {
     GemmPlan g1, g2, g3;
     bool g2_fused = false;   // K2 epilogue does RoPE and q^C (no finalize_up)
     bool g2_wide = false;    // K2 with 256 x 256 tiles on SM pairs (prefill)
+    bool g1_pair = false;    // K1 with 256 x 256 tiles on SM pairs (prefill)
     bool persist = false;    // decode-sized bf16 call: the one persistent kernel of decode_persist.cuh
     int p_n1 = 0, p_s1 = 0, p_wst = 0, p_arows = 0;
     size_t p_smem = 0, off_pss = 0, off_pykv = 0, off_pbar = 0;
@@ -239,6 +240,7 @@ struct Plan {
 
 constexpr size_t kStatusBytes = 1024;
 constexpr int kDecodeRows = 256;   // up to this many tokens: one row tile, weight streaming
+constexpr int kPairKps = 2;         // k-blocks per stage of the prefill GEMMs on SM pairs
 
 size_t up1024(size_t v) { return (v + 1023) & ~size_t(1023); }
 
@@ -284,6 +286,15 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     // 192-column tiles; prefill 256-column tiles (2112 columns: nine tiles per 256 rows, so that
     // 8192 tokens make two waves on 152 SMs instead of three).
     plan_gemm(p.g1, T, p.ncols1, d.He, sms, T <= 128 ? 64 : (T <= kDecodeRows ? 192 : 256), true);
+    // prefill: 256 x 256 tiles on SM pairs (W^DQ's columns split into whole 128-column halves)
+    p.g1_pair = p.g1.bn == 256 && p.g1.ksplit == 1 && d.Hcq % 128 == 0 && (d.Hckv + d.Dr) % 64 == 0 &&
+                (d.He / 64) % kPairKps == 0 && p.ncols1 % 4 == 0;
+    if (p.g1_pair) {
+        p.g1.msub = 2;
+        p.g1.m_tiles = (int)((T + 255) / 256);
+        p.g1.a_box_rows = 128;
+        p.g1.grid = 0;   // pairs: sized at launch
+    }
     // Up-projection: one head (192 columns) per tile, full K, fused RoPE epilogue; prefill with
     // the 128 + 64 head layout uses 256 x 256 tiles on SM pairs (their epilogue sorts 64-column
     // blocks into q^C and rope blocks).
@@ -552,8 +563,6 @@ cudaError_t launch_gemm_pair(cudaStream_t st, const CUtensorMap& a, const CUtens
     return cudaLaunchKernelEx(&cfg, k, a, b0, b1, out, out2, args);
 }
 
-constexpr int kPairKps2 = 2;   // k-blocks per stage of the prefill up-projection on SM pairs
-
 struct Launched {
     const Args* a;
     Dims d;
@@ -746,8 +755,13 @@ mla_status run(const Launched& L) {
     // boxes of the T x ncols1 matrix); k ranges (decode) use plain stores into their slots.
     const bool tma1 = p.g1.ksplit == 1 && p.g1.msub == 2 && p.ncols1 % 4 == 0;
     // 256-column tiles: one 256-row activation box and one column-blocked weight box per k-block
-    const bool big1 = p.g1.bn == 256 && d.Hcq % 256 == 0 && (d.Hckv + d.Dr) % 64 == 0;
-    if (big1) {
+    const bool big1 = !p.g1_pair && p.g1.bn == 256 && d.Hcq % 256 == 0 && (d.Hckv + d.Dr) % 64 == 0;
+    if (p.g1_pair) {
+        if (!map_colblocks(&mA1, x_bf, d.T, d.He, 128, kPairKps) ||
+            !map_colblocks(&mB1a, wdq_bf, d.He, d.Hcq, 64 * kPairKps, 2) ||
+            !map_colblocks(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64 * kPairKps, 2))
+            return MLA_ERR_RUNTIME;
+    } else if (big1) {
         if (!map_2d(&mA1, x_bf, d.T, d.He, 256) || !map_colblocks(&mB1a, wdq_bf, d.He, d.Hcq, 64, 4) ||
             !map_colblocks(&mB1b, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64, 4))
             return MLA_ERR_RUNTIME;
@@ -769,7 +783,11 @@ mla_status run(const Launched& L) {
         g1.tma_out = encode_map(&mO1, y1, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ? 1 : 0;
     }
     g1.out_f32 = y1;
-    if (p.g1.bn == 64)
+    if (p.g1_pair && !g1.tma_out) return MLA_ERR_RUNTIME;   // pair tiles store only through TMA
+    g1.n_fastest = 1;   // x (T x He) is larger than the weights: read each row tile once
+    if (p.g1_pair)
+        e = launch_gemm_pair<256, 8, EPI_F32, 1, 2, kPairKps>(st, mA1, mB1a, mB1b, g1, mO1, mO1);
+    else if (p.g1.bn == 64)
         e = launch_gemm<64, 1, 32, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
     else
         e = p.g1.bn == 256 ? (g1.tma_out && big1
@@ -808,8 +826,8 @@ mla_status run(const Launched& L) {
     // SM-pair tiles: per k-block each CTA takes one 128-row activation box and one box of its
     // 128 weight columns (two 64-column blocks)
     if (p.g2_wide) {
-        if (!map_colblocks(&mA2, ws + p.off_cq, d.T, d.Hcq, 128, kPairKps2) ||
-            !map_colblocks(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64 * kPairKps2, 2))
+        if (!map_colblocks(&mA2, ws + p.off_cq, d.T, d.Hcq, 128, kPairKps) ||
+            !map_colblocks(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64 * kPairKps, 2))
             return MLA_ERR_RUNTIME;
     } else if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
                !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64)) {
@@ -838,7 +856,7 @@ mla_status run(const Launched& L) {
     g2.out_f32 = reinterpret_cast<float*>(ws + p.off_y2);
     if (p.g2_fused) {
         if (p.g2_wide)
-            e = launch_gemm_pair<256, 8, EPI_QROPE, 1, 2, kPairKps2>(st, mA2, mB2, mB2, g2, mO2c, mO2r);
+            e = launch_gemm_pair<256, 8, EPI_QROPE, 1, 2, kPairKps>(st, mA2, mB2, mB2, g2, mO2c, mO2r);
         else if (p.g2.msub == 1)
             e = launch_gemm<192, 1, 16, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2);
         else
