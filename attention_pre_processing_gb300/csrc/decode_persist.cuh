@@ -25,13 +25,12 @@
 // consumer waits for exactly the flags it reads.  Flags from another call carry another tag,
 // so the workspace needs no initialisation.
 //
-// Roles (256 threads): warp 0 streams weight stages with TMA; warp 1 allocates tensor memory
-// and issues tcgen05.mma; warp 2 loads P1's activation tiles (x) with TMA; warp 3 is idle;
-// warps 4..7 run the epilogues, the reduction, the cache rows, and load P3's
-// activation tiles (c^Q) with ordinary loads: a TMA load queues behind the weight stages the
-// SM has in flight, which would hold every P3 step for an HBM round trip.  Every wait is
-// bounded: a wait that gives up sets MLA_DEV_WAIT_TIMEOUT, the other roles stop at their next
-// wait, tensor memory is freed and the kernel returns.
+// Roles (256 threads): warp 0 streams weight stages with TMA (one 3D box of three 64-column
+// blocks per stage); warp 1 allocates tensor memory and issues tcgen05.mma; warp 2 loads the
+// activation tiles with TMA (x for P1, then c^Q for P3 once the epilogue warps have seen it
+// reduced); warp 3 is idle; warps 4..7 run the epilogues, the reduction and the cache rows.
+// Every wait is bounded: a wait that gives up sets MLA_DEV_WAIT_TIMEOUT, the other roles stop
+// at their next wait, tensor memory is freed and the kernel returns.
 
 #pragma once
 
@@ -88,7 +87,6 @@ struct PStep {
     int phase;    // 1, 3, 4
     int kb;       // k-block
     int g;        // P4: column group (0: 0..191, 1: 192..383, 2: 384..511)
-    int nbox;     // boxes in the stage
     bool first;   // overwrite the accumulator
     bool last;    // last stage of the phase: commit the accumulator
 };
@@ -104,19 +102,19 @@ __device__ __forceinline__ int p1_range(const PersistArgs& a, int* tile, int* ks
 
 __device__ __forceinline__ bool p_step(const PersistArgs& a, int i, int n1s, PStep& s) {
     if (i < n1s) {
-        s = {1, i, 0, 3, i == 0, i == n1s - 1};
+        s = {1, i, 0, i == 0, i == n1s - 1};
         return true;
     }
     i -= n1s;
     if ((int)blockIdx.x >= a.N) return false;
     if (i < a.kb2) {
-        s = {3, i, 0, 3, i == 0, i == a.kb2 - 1};
+        s = {3, i, 0, i == 0, i == a.kb2 - 1};
         return true;
     }
     i -= a.kb2;
     if (i < 6) {   // D = 128: two k-blocks x three column groups
         const int kb = i / 3, g = i % 3;
-        s = {4, kb, g, g == 2 ? 2 : 3, kb == 0, i == 5};
+        s = {4, kb, g, kb == 0, i == 5};
         return true;
     }
     return false;
@@ -177,79 +175,6 @@ __device__ __forceinline__ void chain_store(uint32_t base, int slot_bytes, int r
     }
 }
 
-// P3's activation tiles: c^Q k-blocks of T rows x 128 bytes in the 128-byte-swizzled K-major
-// layout, loaded by the 128 epilogue threads with ordinary 16-byte loads into the kPA3-slot
-// ring (so they never queue behind weight stages in the TMA engine).  The first batch fills
-// the ring; later batches of four follow as the tensor core frees slots.  Every load of a batch
-// is in flight together.  UPT: 16-byte chunks per thread and tile (T <= 16 * UPT).
-template <int FIRST, int UPT>
-__device__ __forceinline__ bool load_cq_tiles(const PersistArgs& a, uint8_t* ring, uint64_t* full, uint64_t* empty,
-                                              const volatile int* abort, int etid) {
-    const int chunks = a.T * 8;
-    int sa = 0;
-    uint32_t ph = 0;
-    for (int kb0 = 0; kb0 < a.kb2;) {
-        const int want = kb0 == 0 ? FIRST : 4;
-        const int nb = a.kb2 - kb0 < want ? a.kb2 - kb0 : want;
-        // One thread waits for the batch's slots; the others block at the named barrier (a
-        // spinning warp would take issue slots from the MMA warp on its scheduler).
-        bool ok = true;
-        if (etid == 0) {
-            int s2 = sa;
-            uint32_t p2 = ph;
-            for (int k = 0; k < nb && ok; ++k) {
-                ok = mbar_wait_sleep(smem_u32(&empty[s2]), p2 ^ 1, abort, kWaitLimitNs);
-                if (++s2 == kPA3) {
-                    s2 = 0;
-                    p2 ^= 1;
-                }
-            }
-        }
-        if (epi_any(!ok)) return false;   // all 128 threads leave together
-        uint4 v[FIRST][UPT];
-#pragma unroll
-        for (int k = 0; k < FIRST; ++k)
-#pragma unroll
-            for (int u = 0; u < UPT; ++u) {
-                const int c = etid + 128 * u;
-                v[k][u] = make_uint4(0, 0, 0, 0);
-                if (k < nb && c < chunks)
-                    v[k][u] = __ldcg(reinterpret_cast<const uint4*>(a.cq + (size_t)(c >> 3) * a.hcq + (kb0 + k) * 64 +
-                                                                   (c & 7) * 8));
-            }
-        int s3 = sa;
-#pragma unroll
-        for (int k = 0; k < FIRST; ++k) {
-            if (k >= nb) break;
-            const uint32_t slot = smem_u32(ring + (size_t)s3 * a.a_bytes);
-#pragma unroll
-            for (int u = 0; u < UPT; ++u) {
-                const int c = etid + 128 * u;
-                if (c < chunks) {
-                    const int r = c >> 3, ch = c & 7;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     slot + (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4))),
-                                 "r"(v[k][u].x), "r"(v[k][u].y), "r"(v[k][u].z), "r"(v[k][u].w)
-                                 : "memory");
-                }
-            }
-            if (++s3 == kPA3) s3 = 0;
-        }
-        // One proxy fence for the whole batch (generic writes -> tensor-core reads): the fence
-        // waits on the SM's busy async proxy, so one per tile would pace the tiles.
-        fence_proxy_async_smem();
-        for (int k = 0; k < nb; ++k) {
-            mbar_arrive(smem_u32(&full[sa]));
-            if (++sa == kPA3) {
-                sa = 0;
-                ph ^= 1;
-            }
-        }
-        kb0 += nb;
-    }
-    return true;
-}
-
 // Alignment slack, barriers and a 1 KB scratch, the activation region (P1's TMA ring, later
 // P3's ring, later P4's A operand) and the weight ring.
 __host__ __device__ inline size_t persist_smem_bytes(int a_bytes, int wst) {
@@ -274,7 +199,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint64_t* aempty3 = afull3 + kPA3;            // [kPA3]
     uint64_t* tfull = aempty3 + kPA3;             // [3]: P1, P3, P4 accumulators
     uint64_t* chain_full = tfull + 3;
-    uint64_t* done = chain_full + 1;
+    uint64_t* cq_ready = chain_full + 1;         // the epilogue saw every c^Q chunk reduced
+    uint64_t* done = cq_ready + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     float* ssum = reinterpret_cast<float*>(smem + 1024);   // 4 x 64 partial sums of squares
@@ -304,11 +230,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(smem_u32(&aempty[s]), 1);
         }
         for (int s = 0; s < kPA3; ++s) {
-            mbar_init(smem_u32(&afull3[s]), 128);
+            mbar_init(smem_u32(&afull3[s]), 1);
             mbar_init(smem_u32(&aempty3[s]), 1);
         }
         for (int p = 0; p < 3; ++p) mbar_init(smem_u32(&tfull[p]), 1);
         mbar_init(smem_u32(chain_full), 128);
+        mbar_init(smem_u32(cq_ready), 1);
         mbar_init(smem_u32(done), 1);
         *s_abort = 0;
         fence_barrier_init();
@@ -342,20 +269,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 const uint32_t fb = smem_u32(&wfull[s]);
                 const uint32_t dst = smem_u32(wring + (size_t)s * kPStage);
-                mbar_arrive_expect_tx(fb, (uint32_t)(st.nbox * kPBox));
-                for (int j = 0; j < st.nbox; ++j) {
-                    if (st.phase == 1) {
-                        const int col = tile * 192 + 64 * j;
-                        if (col < args.hcq)
-                            tma_load_2d(dst + j * kPBox, &map_wdq, fb, col, (kb0 + st.kb) * 64, pol);
-                        else
-                            tma_load_2d(dst + j * kPBox, &map_wdkvkr, fb, col - args.hcq, (kb0 + st.kb) * 64, pol);
-                    } else if (st.phase == 3) {
-                        tma_load_2d(dst + j * kPBox, &map_wuqqr, fb, (int)blockIdx.x * 192 + 64 * j, st.kb * 64, pol);
-                    } else {
-                        tma_load_3d(dst + j * kPBox, &map_wuk, fb, st.g * 192 + 64 * j, st.kb * 64, (int)blockIdx.x,
-                                    pol);
-                    }
+                // One request per stage: three 64-column blocks of 64 k rows (a block past the
+                // matrix, the fourth of W^UK's last group, is zero-filled and still counted).
+                mbar_arrive_expect_tx(fb, (uint32_t)kPStage);
+                if (st.phase == 1) {
+                    const int col = tile * 192;   // a tile never straddles W^DQ | W^DkvKr
+                    if (col < args.hcq)
+                        tma_load_3d(dst, &map_wdq, fb, 0, (kb0 + st.kb) * 64, col / 64, pol);
+                    else
+                        tma_load_3d(dst, &map_wdkvkr, fb, 0, (kb0 + st.kb) * 64, (col - args.hcq) / 64, pol);
+                } else if (st.phase == 3) {
+                    tma_load_3d(dst, &map_wuqqr, fb, 0, st.kb * 64, (int)blockIdx.x * 3, pol);
+                } else {
+                    tma_load_3d(dst, &map_wuk, fb, 0, (int)blockIdx.x * 128 + st.kb * 64, st.g * 3, pol);
                 }
                 if (++s == wst) {
                     s = 0;
@@ -378,57 +304,71 @@ __global__ void __launch_bounds__(kPThreads, 1)
             int sw = 0;
             uint32_t phw = 0;
             bool ok = true;
-            // One weight stage: K = 64 (four k16 MMAs) into accumulator columns d.
-            auto stage = [&](uint64_t adesc, uint32_t d, uint32_t idesc, bool first) -> bool {
-                if (!mbar_wait(smem_u32(&wfull[sw]), phw, s_abort, kWaitLimitNs)) return false;
+            // The next weight stage has landed.
+            auto wait_w = [&]() -> bool { return mbar_wait(smem_u32(&wfull[sw]), phw, s_abort, kWaitLimitNs); };
+            // One weight stage: K = 64 (four k16 MMAs) into accumulator columns d; returns the
+            // ring slot to release once they complete.
+            auto mma4 = [&](uint64_t adesc, uint32_t d, uint32_t idesc, bool first) -> int {
                 tc_fence_after();
                 const uint64_t bdesc = bdesc0 + (uint64_t)sw * w_unit;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     umma_bf16(d, adesc + 2 * kk, bdesc + 128 * kk, idesc, (first && kk == 0) ? 0u : 1u);
-                umma_commit(smem_u32(&wempty[sw]));
+                const int used = sw;
                 if (++sw == wst) {
                     sw = 0;
                     phw ^= 1;
                 }
-                return true;
+                return used;
             };
+            // Each loop waits for the NEXT stage's operands while the tensor core runs this
+            // stage's MMAs, and only then queues the commits that release this stage: the
+            // tcgen05 queue is short, so a wait placed after the commits would leave the tensor
+            // core idle for its duration every stage.
             // P1: activation slots filled by TMA
             {
                 int sa = 0;
                 uint32_t pha = 0;
+                if (n1s > 0) ok = mbar_wait(smem_u32(&afull[0]), 0, s_abort, kWaitLimitNs) && wait_w();
                 for (int i = 0; ok && i < n1s; ++i) {
-                    ok = mbar_wait(smem_u32(&afull[sa]), pha, s_abort, kWaitLimitNs) &&
-                         stage(adesc0 + (uint64_t)sa * a_unit, tmem_base + 256, id192, i == 0);
-                    if (!ok) break;
-                    umma_commit(smem_u32(&aempty[sa]));
+                    const int used_w = mma4(adesc0 + (uint64_t)sa * a_unit, tmem_base + 256, id192, i == 0);
+                    const int used_a = sa;
                     if (++sa == kPA) {
                         sa = 0;
                         pha ^= 1;
                     }
+                    if (i + 1 < n1s) ok = mbar_wait(smem_u32(&afull[sa]), pha, s_abort, kWaitLimitNs) && wait_w();
+                    umma_commit(smem_u32(&wempty[used_w]));
+                    umma_commit(smem_u32(&aempty[used_a]));
                 }
                 if (ok && n1s > 0) umma_commit(smem_u32(&tfull[0]));
             }
             if (head) {
-                // P3: activation slots filled by the epilogue warps
+                // P3: activation slots filled by TMA (c^Q)
                 int sa = 0;
                 uint32_t pha = 0;
+                ok = ok && mbar_wait(smem_u32(&afull3[0]), 0, s_abort, kWaitLimitNs) && wait_w();
                 for (int kb = 0; ok && kb < args.kb2; ++kb) {
-                    ok = mbar_wait(smem_u32(&afull3[sa]), pha, s_abort, kWaitLimitNs) &&
-                         stage(adesc0 + (uint64_t)sa * a_unit, tmem_base, id192, kb == 0);
-                    if (!ok) break;
-                    umma_commit(smem_u32(&aempty3[sa]));
+                    const int used_w = mma4(adesc0 + (uint64_t)sa * a_unit, tmem_base, id192, kb == 0);
+                    const int used_a = sa;
                     if (++sa == kPA3) {
                         sa = 0;
                         pha ^= 1;
                     }
+                    if (kb + 1 < args.kb2) ok = mbar_wait(smem_u32(&afull3[sa]), pha, s_abort, kWaitLimitNs) && wait_w();
+                    umma_commit(smem_u32(&wempty[used_w]));
+                    umma_commit(smem_u32(&aempty3[used_a]));
                 }
                 if (ok) umma_commit(smem_u32(&tfull[1]));
                 // P4: A = q^C in activation slots 0 and 1; three column groups per k-block
-                ok = ok && mbar_wait(smem_u32(chain_full), 0, s_abort, kWaitLimitNs);
-                for (int kb = 0; ok && kb < 2; ++kb)
-                    for (int g = 0; ok && g < 3; ++g)
-                        ok = stage(adesc0 + (uint64_t)kb * a_unit, tmem_base + 192 * g, g == 2 ? id128 : id192, kb == 0);
+                ok = ok && mbar_wait(smem_u32(chain_full), 0, s_abort, kWaitLimitNs) && wait_w();
+                for (int i = 0; ok && i < 6; ++i) {
+                    const int kb = i / 3, g = i % 3;
+                    const int used_w =
+                        mma4(adesc0 + (uint64_t)kb * a_unit, tmem_base + 192 * g, g == 2 ? id128 : id192, kb == 0);
+                    if (i + 1 < 6) ok = wait_w();
+                    umma_commit(smem_u32(&wempty[used_w]));
+                }
                 if (ok) umma_commit(smem_u32(&tfull[2]));
             }
             if (!ok) fail();
@@ -454,6 +394,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 return true;
             };
             for (int i = 0; ok && i < n1s; ++i) ok = put(&map_x, kb0 + i);
+            if (ok && head) {
+                // P3's activation tiles (c^Q k-blocks), once the epilogue warps have seen every
+                // chunk reduced.  c^Q was written by other CTAs' ordinary stores and is read here
+                // by the TMA engine: the proxy fence orders the two.
+                ok = mbar_wait_sleep(smem_u32(cq_ready), 0, s_abort, kWaitLimitNs);
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                for (int kb = 0; ok && kb < args.kb2; ++kb) {
+                    const int s3 = kb % kPA3;
+                    if (kb >= kPA3 &&
+                        !mbar_wait_sleep(smem_u32(&aempty3[s3]), ((kb / kPA3) & 1) ^ 1, s_abort, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&afull3[s3]);
+                    mbar_arrive_expect_tx(fb, (uint32_t)args.a_bytes);
+                    tma_load_2d(smem_u32(aring + (size_t)s3 * args.a_bytes), &map_cq, fb, kb * 64, 0, pol);
+                }
+            }
             if (!ok) fail();
         }
     } else if (warp == 3) {
@@ -558,14 +516,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (ok && head) {
             // Every c^Q chunk is reduced (one collective wait for all of them) ...
             ok = wait_flags(args.cflags, args.hcq / kPChunk, 1, args.tag, s_abort, etid);
-            // ... then the P3 activation tiles, with ordinary loads, the first batch filling the
-            // whole ring ...
-            if (ok) {
-                if (T <= 32)
-                    ok = load_cq_tiles<8, 2>(args, aring, afull3, aempty3, s_abort, etid);
-                else
-                    ok = load_cq_tiles<4, 4>(args, aring, afull3, aempty3, s_abort, etid);
-            }
+            // ... then the P3 activation tiles come by TMA (warp 2) ...
+            if (etid == 0) mbar_arrive(smem_u32(cq_ready));
             // ... and each row's 1 / RMS: the 128 threads split the chunk sums (a fixed order in
             // each part, the parts added in order).
             float inv = 0.f;

@@ -396,8 +396,10 @@ struct OutStage {
         }
         ob = (ob + 1 == OUTB) ? 0 : ob + 1;
     }
+    // The last stores have read their shared memory (the CTA may exit: the grid completes only
+    // once its bulk stores have landed, before any dependent grid reads them).
     __device__ __forceinline__ void drain() const {
-        if (lane == 0) bulk_wait_all();
+        if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
     }
 };
@@ -933,7 +935,7 @@ __global__ void __launch_bounds__(gemm_threads(EPW), 1)
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[b]));
         }
-        if constexpr (OUTB > 0) ostage.drain();   // stores read their shared memory and land
+        if constexpr (OUTB > 0) ostage.drain();   // the stores have read their shared memory
     }
 
     tc_fence_before();

@@ -334,7 +334,7 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
         if (s1 > kb1) s1 = kb1;
         if (s1 > kPMaxS) s1 = kPMaxS;
         if (!sc.x_i8 && !sc.uqqr_i8 && !sc.kv_i8 && !sc.kr_i8 && !sc.q_i8 && T >= 1 && T <= kPMaxT &&
-            d.D == 128 && d.Dr == 64 && d.Hckv == 512 && d.Hcq % 64 == 0 && d.He % 64 == 0 && ncols1 % 192 == 0 &&
+            d.D == 128 && d.Dr == 64 && d.Hckv == 512 && d.Hcq % 192 == 0 && d.He % 64 == 0 && ncols1 % 192 == 0 &&
             d.N >= 1 && d.N <= sms && ncols1 / kPChunk <= sms && s1 >= 1 && wst >= 4) {
             p.persist = true;
             p.p_n1 = n1;
@@ -682,14 +682,16 @@ mla_status run(const Launched& L) {
     if (p.persist) {
         // ---- the whole prolog in one persistent kernel
         const uint32_t rows = (uint32_t)p.p_arows;
-        CUtensorMap mx, mwdq, mwdkvkr, mcq, mwuqqr, mo;
+        // weights as (64 columns, k rows, 64-column blocks): one box brings a 192-column stage
+        CUtensorMap mx, mwdq, mwdkvkr, mcq, mwuqqr, mwuk, mo;
         const uint64_t ocols = (uint64_t)d.N * (uint64_t)d.Hckv;
         const uint64_t odims[2] = {ocols, (uint64_t)d.T};
         const uint64_t ostrides[1] = {ocols * 2};
         const uint32_t obox[2] = {64, 32};
-        if (!map_2d(&mx, x_bf, d.T, d.He, rows) || !map_2d(&mwdq, wdq_bf, d.He, d.Hcq, 64) ||
-            !map_2d(&mwdkvkr, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64) || !map_2d(&mcq, ws + p.off_cq, d.T, d.Hcq, rows) ||
-            !map_2d(&mwuqqr, wuqqr_bf, d.Hcq, p.ncols2, 64) ||
+        if (!map_2d(&mx, x_bf, d.T, d.He, rows) || !map_colblocks(&mwdq, wdq_bf, d.He, d.Hcq, 64, 3) ||
+            !map_colblocks(&mwdkvkr, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64, 3) ||
+            !map_2d(&mcq, ws + p.off_cq, d.T, d.Hcq, rows) || !map_colblocks(&mwuqqr, wuqqr_bf, d.Hcq, p.ncols2, 64, 3) ||
+            !map_colblocks(&mwuk, a.wuk->data, d.N * d.D, d.Hckv, 64, 3) ||
             !encode_map(&mo, a.qout->data, 2, odims, ostrides, obox))
             return MLA_ERR_RUNTIME;
         PersistArgs pa = {};
@@ -738,7 +740,7 @@ mla_status run(const Launched& L) {
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, decode_persist_kernel, mx, mwdq, mwdkvkr, mcq, mwuqqr, mB3, mo, pa);
+        e = cudaLaunchKernelEx(&cfg, decode_persist_kernel, mx, mwdq, mwdkvkr, mcq, mwuqqr, mwuk, mo, pa);
         if (e == cudaSuccess) {
             timing_mark(st, "decode_persist");
             if (g_timing.enabled) g_timing.have = true;

@@ -134,6 +134,18 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x
                  : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 (LDGSTS), tracked per thread by
+// commit groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Prefetch of one cache line into L2 (a hint: never faults, never waits).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
