@@ -418,6 +418,11 @@ def run_kernels_only(args):
     from attention_pre_processing_gb300.runner import PrologCall
     cuda_build.build()
     cfg = workloads.config(args.workload)
+    if args.T:
+        over = {"T": args.T}
+        if cfg.sequences is not None:   # same number of sequences, shorter ones
+            over["sequences"] = (cfg.sequences[0], args.T // cfg.sequences[0])
+        cfg = workloads.config(args.workload, **over)
     call = PrologCall(cfg, workloads.make_inputs(cfg))
     for _ in range(args.warmup + args.steps):
         call()
@@ -437,6 +442,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--kernels-only", action="store_true", help="only warmup+steps calls of --workload")
     ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--T", type=int, default=0, help="--kernels-only: token count other than the workload's")
     args = ap.parse_args()
     if args.kernels_only:
         run_kernels_only(args)
