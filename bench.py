@@ -369,7 +369,7 @@ def cpu_baseline(cfg, inp, budget_s=12.0, steps=None):
     oracle.build()
     threads = oracle.max_threads()
     done, elapsed, n = 0, 0.0, max(1, threads)
-    while elapsed < budget_s and done < cfg.shape.T * 8:
+    while elapsed < budget_s:
         tok = (workloads.sample_tokens(cfg.shape.T, n, seed=done + 1) if n < cfg.shape.T
                else list(range(cfg.shape.T)))
         t0 = time.perf_counter()
