@@ -1,36 +1,36 @@
 // The whole bf16 prolog for decode-sized token counts in ONE persistent kernel: one CTA per SM,
 // all CTAs co-resident (cooperative launch).  Every CTA streams its weights through one ring of
 // 24 KB stages (three 64 x 64 boxes) from the first to the last phase, so HBM never waits for a
-// kernel boundary; only the tensor-core work waits for the two grid barriers.
+// kernel boundary; only the tensor-core work waits for the data it depends on.
 //
-//   P1   x . [W^DQ | W^DkvKr]: 192-column tiles x s1 k ranges, one unit per CTA, fp32 products
-//        into slot k-range of a s1 x T x ncols1 buffer
-//   R    once the s1 CTAs of its tile have stored their products: the k-range slots added in
-//        fixed order, one 16-column chunk per CTA: for c^Q columns bf16(gamma * y) (the A
-//        operand of P3) and the chunk's sum of y^2 per token; for c^KV and k^R columns the fp32
-//        y (the RmsNorm scale needs every chunk of the row)
-//   P3   head n = CTA index, each k-block as soon as its four chunks are reduced:
-//        (gamma * y) . W^UqQr[:, head n]; the epilogue multiplies by the
-//        token's 1 / RMS (from the chunk sums), applies RoPE to the rope columns
+//   P1   x . [W^DQ | W^DkvKr]: 192-column tiles x s1 k ranges, one unit per CTA; each unit adds
+//        its fp32 product into y (T x ncols1) with vector atomics and counts itself in on its
+//        tile's counter
+//   P3   head n = CTA index, once the c^Q tiles' counters are complete: the epilogue warps turn
+//        y into bf16(gamma * y) k-block by k-block (P3's A operand, in shared memory) and sum
+//        each token's y^2; the tensor core computes (gamma * y) . W^UqQr[:, head n]; the
+//        epilogue multiplies by the token's 1 / RMS, applies RoPE to the rope columns
 //        (queryRopeOut) and writes q^C straight into shared memory as P4's A operand
 //   P4   q^C . W^UK[n] (512 columns) -> queryOut through TMA stores
-//   KV   CTAs without a head: RmsNorm of c^KV and RoPE of k^R, written to the caches at
-//        cacheIndex
+//   KV   CTAs without a head, once the c^KV / k^R tiles are complete: RmsNorm of c^KV and RoPE
+//        of k^R, written to the caches at cacheIndex
 //
 // RmsNorm(y) . W = (1 / RMS(y)) * ((gamma * y) . W): the per-token scale moves behind the
 // contraction, so no row pass sits between the reduction and P3.
 //
-// Cross-CTA dependencies are flags, not grid barriers: every producer of data (a P1 unit, a
-// reduced chunk) stores the call's tag in its own 8-byte flag after its data, and each
-// consumer waits for exactly the flags it reads.  Flags from another call carry another tag,
-// so the workspace needs no initialisation.
+// The k-range products are added with fp32 atomics, so their order follows arrival: results
+// can differ in the last bits from call to call (the kernel-per-step path adds them in fixed
+// order).  Each tile's y rows and counter are zeroed at the start of the call by the tile's
+// first k-range CTA, which then stores the call's tag in the tile's flag; the adders wait for
+// that flag, and readers wait for the flag and a complete counter.  Flags of another call hold
+// another tag, so the workspace needs no initialisation.
 //
 // Roles (256 threads): warp 0 streams weight stages with TMA (one 3D box of three 64-column
-// blocks per stage); warp 1 allocates tensor memory and issues tcgen05.mma; warp 2 loads the
-// activation tiles with TMA (x for P1, then c^Q for P3 once the epilogue warps have seen it
-// reduced); warp 3 is idle; warps 4..7 run the epilogues, the reduction and the cache rows.
-// Every wait is bounded: a wait that gives up sets MLA_DEV_WAIT_TIMEOUT, the other roles stop
-// at their next wait, tensor memory is freed and the kernel returns.
+// blocks per stage); warp 1 allocates tensor memory and issues tcgen05.mma; warp 2 loads P1's
+// activation tiles (x) with TMA; warp 3 is idle; warps 4..7 run the zeroing, the epilogues, P3's
+// activation tiles and the cache rows.  Every wait is bounded: a wait that gives up sets
+// MLA_DEV_WAIT_TIMEOUT, the other roles stop at their next wait, tensor memory is freed and the
+// kernel returns.
 
 #pragma once
 
@@ -47,8 +47,8 @@ constexpr int kPBox = 8192;                  // one 64 x 64 bf16 weight box
 constexpr int kPStage = 3 * kPBox;           // one weight stage: up to 192 columns
 constexpr int kPMaxW = 12;                   // weight stages at most
 constexpr int kPA = 4;                       // P1 activation slots (TMA)
-constexpr int kPA3 = 8;                      // P3 activation slots (loaded by the epilogue warps)
-constexpr int kPChunk = 16;                  // columns per reduction chunk
+constexpr int kPA3 = 8;                      // P3 activation slots (written by the epilogue warps)
+constexpr int kPTile = 192;                  // P1 columns per tile
 constexpr int kPMaxT = 64;                   // tokens at most
 constexpr int kPMaxS = 16;                   // k ranges at most
 
@@ -56,13 +56,14 @@ struct PersistArgs {
     int T, a_rows, a_bytes, wst;        // tokens, A box rows, A slot bytes, weight stages
     // P1
     int hcq, hckv, dr, ncols1, n1, s1, kb1;
-    float* y1;                          // s1 x T x ncols1
-    // R
+    float* y;                           // T x ncols1: the k-range products, added in
+    unsigned int* cnt;                  // n1: k ranges of the tile added in
+    unsigned long long* zflags;         // n1: the tile's y rows and counter are zeroed (call tag)
+    __nv_bfloat16* cq;                  // T x Hcq: bf16(gamma_cq * y), P3's activation
+    float* ss;                          // (Hcq / 192) x T: each c^Q tile's sum of y^2 per token
+    unsigned long long* cqflags;        // Hcq / 192: the tile's cq and ss are written (call tag)
     const __nv_bfloat16* gamma_cq;
     const __nv_bfloat16* gamma_ckv;
-    __nv_bfloat16* cq;                  // T x Hcq: bf16(gamma_cq * y)
-    float* ss;                          // (Hcq + Hckv) / 16 chunks x T
-    float* ykv;                         // T x (Hckv + Dr)
     float eps_cq, eps_ckv;
     // KV
     const long long* cache_index;
@@ -75,9 +76,6 @@ struct PersistArgs {
     int N, kb2;                         // heads, k-blocks of Hcq
     __nv_bfloat16* q_rope;              // T x N x 64
     __nv_bfloat16* q_out;               // T x N x 512
-    // dependency flags
-    unsigned long long* p1flags;        // gridDim.x: P1 product stored
-    unsigned long long* cflags;         // ncols1 / 16: chunk reduced
     unsigned long long tag;             // unique per call
     uint32_t* status;
 };
@@ -122,31 +120,38 @@ __device__ __forceinline__ bool p_step(const PersistArgs& a, int i, int n1s, PSt
 
 // ------------------------------------------------------------------ dependency flags
 
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
 
-// Waits (bounded) until flags f[0], f[stride], ..., f[(n-1) * stride] (n <= 128) all hold
-// `tag`.  Called by all 128 epilogue threads together.  One warp polls: lane l reads flags
-// l, l + 32, l + 64, l + 96 together (relaxed loads), with a short sleep between rounds so that
-// the flag lines are not hammered while the data behind them is being read; the named barrier
-// releases the other warps, and every thread then takes an acquire fence.
-__device__ __forceinline__ bool wait_flags(const unsigned long long* f, int n, int stride, unsigned long long tag,
-                                           const volatile int* abort, int etid) {
+// Waits (bounded) until tiles t0 .. t1 - 1 (at most 32) are ready: the tile's flag holds `tag`
+// (zeroed in this call) and, if `need` > 0, its counter holds `need` (every k range added in).
+// Called by all 128 epilogue threads together.  One warp polls, lane l the tile t0 + l: the flag
+// is read with acquire semantics first, so the counter read after it is this call's; a short
+// sleep between rounds keeps the lines from being hammered.  The named barrier releases the
+// other warps, and every thread then takes an acquire fence.
+__device__ __forceinline__ bool wait_tiles(const unsigned long long* zf, const unsigned int* cnt, int t0, int t1,
+                                           unsigned int need, unsigned long long tag, const volatile int* abort,
+                                           int etid) {
     bool ok = true;
     if (etid < 32) {
-        const uint64_t t0 = global_timer_ns();
+        const uint64_t start = global_timer_ns();
+        const int t = t0 + etid;
+        bool mine = t >= t1;
         while (true) {
-            bool all = true;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = etid + 32 * k;
-                if (i < n) all &= ld_relaxed_u64(f + (size_t)i * stride) == tag;
-            }
-            if (__all_sync(0xffffffffu, all)) break;
-            if (*abort || global_timer_ns() - t0 > kWaitLimitNs) {
+            if (!mine) mine = ld_acquire_u64(zf + t) == tag && (need == 0 || ld_relaxed_u32(cnt + t) == need);
+            if (__all_sync(0xffffffffu, mine)) break;
+            if (*abort || global_timer_ns() - start > kWaitLimitNs) {
                 ok = false;
                 break;
             }
@@ -154,7 +159,7 @@ __device__ __forceinline__ bool wait_flags(const unsigned long long* f, int n, i
         }
     }
     const bool bad = epi_any(!ok);
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");   // acquire: what the flags published
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");   // acquire: what the flags and counters published
     return !bad;
 }
 
@@ -199,11 +204,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint64_t* aempty3 = afull3 + kPA3;            // [kPA3]
     uint64_t* tfull = aempty3 + kPA3;             // [3]: P1, P3, P4 accumulators
     uint64_t* chain_full = tfull + 3;
-    uint64_t* cq_ready = chain_full + 1;         // the epilogue saw every c^Q chunk reduced
+    uint64_t* cq_ready = chain_full + 1;         // the epilogue saw every c^Q tile written
     uint64_t* done = cq_ready + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-    float* ssum = reinterpret_cast<float*>(smem + 1024);   // 4 x 64 partial sums of squares
+    volatile int* s_last = s_abort + 1;   // this CTA added the last k range of its P1 tile
+    float* scratch = reinterpret_cast<float*>(smem + 1024);   // 1 KB: the KV rows' warp sums
     uint8_t* aring = smem + 2048;
     uint8_t* wring = aring + (size_t)kPA3 * args.a_bytes;
     const int wst = args.wst;
@@ -217,6 +223,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&map_x);
+        tma_prefetch_map(&map_cq);
         tma_prefetch_map(&map_wdq);
         tma_prefetch_map(&map_wdkvkr);
         tma_prefetch_map(&map_wuqqr);
@@ -396,8 +403,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             for (int i = 0; ok && i < n1s; ++i) ok = put(&map_x, kb0 + i);
             if (ok && head) {
                 // P3's activation tiles (c^Q k-blocks), once the epilogue warps have seen every
-                // chunk reduced.  c^Q was written by other CTAs' ordinary stores and is read here
-                // by the TMA engine: the proxy fence orders the two.
+                // c^Q tile written.  c^Q was written by other CTAs' ordinary stores and is read
+                // here by the TMA engine: the proxy fence orders the two.
                 ok = mbar_wait_sleep(smem_u32(cq_ready), 0, s_abort, kWaitLimitNs);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 for (int kb = 0; ok && kb < args.kb2; ++kb) {
@@ -431,125 +438,112 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc_fence_after();
             return r != 0;
         };
-        // The epilogue threads' stores so far become visible, then the flag says so: the named
-        // barrier orders every thread's stores before thread 0's release store, and the release
-        // is cumulative over them.
-        auto publish = [&](unsigned long long* flag) {
-            epi_bar();
-            if (etid == 0) asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flag), "l"(args.tag) : "memory");
-        };
+        const int ncq = args.hcq / kPTile;    // P1 tiles of c^Q columns; the rest are c^KV | k^R
 
-        // ---- P1: this CTA's k-range product of one 192-column tile -> slot ks
+        // ---- zeroing: the first k-range CTA of each tile clears the tile's y rows and counter,
+        // then stores the call's tag in the tile's flag (release: cumulative over every epilogue
+        // thread's stores, which the named barrier orders before it)
+        if ((int)blockIdx.x < args.n1) {
+            const int zt = blockIdx.x;
+            for (int i = etid; i < T * (kPTile / 4); i += 128) {
+                const int r = i / (kPTile / 4), c4 = i % (kPTile / 4);
+                reinterpret_cast<float4*>(args.y + (size_t)r * args.ncols1 + zt * kPTile)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (etid == 0) *reinterpret_cast<volatile unsigned int*>(args.cnt + zt) = 0u;
+            epi_bar();
+            if (etid == 0)
+                asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(args.zflags + zt), "l"(args.tag) : "memory");
+        }
+
+        // ---- P1: this CTA's k-range product of one 192-column tile, added into y
         if (n1s > 0) {
             ok = acc_ready(0);
+            ok = !epi_any(!ok);
+            if (ok) ok = wait_tiles(args.zflags, args.cnt, tile, tile + 1, 0u, args.tag, s_abort, etid);
             if (ok && q * 32 < T) {
-                float* dst = args.y1 + ((size_t)ks * T + row) * args.ncols1 + tile * 192;
+                float* dst = args.y + (size_t)row * args.ncols1 + tile * kPTile;
 #pragma unroll 1
-                for (int ch = 0; ch < 6; ++ch) {
+                for (int ch = 0; ch < kPTile / 32; ++ch) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + 256 + ch * 32, r);
                     tmem_ld_wait();
                     if (row < T) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            reinterpret_cast<float4*>(dst + ch * 32)[i] =
-                                make_float4(bits_f(r[4 * i]), bits_f(r[4 * i + 1]), bits_f(r[4 * i + 2]), bits_f(r[4 * i + 3]));
+                            red_add_v4(dst + ch * 32 + 4 * i, bits_f(r[4 * i]), bits_f(r[4 * i + 1]), bits_f(r[4 * i + 2]),
+                                       bits_f(r[4 * i + 3]));
                     }
                 }
+            }
+            // Count this k range in: the named barrier orders every thread's additions before
+            // thread 0's release; the acquire half lets the last of the tile's k ranges read the
+            // complete sum.
+            epi_bar();
+            if (etid == 0) {
+                unsigned int old = 0;
+                if (ok) asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(args.cnt + tile) : "memory");
+                *s_last = ok && old + 1 == (unsigned int)args.s1 ? 1 : 0;
+            }
+            epi_bar();
+            if (*s_last && tile < ncq) {
+                // The last k range of a c^Q tile: bf16(gamma * y) of its 192 columns into cq, and
+                // each token's sum of y^2 over them into ss; then the tile's flag.  Sixteen
+                // threads per row, three float4 each; rows in batches of 32.
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                const int rsub = etid >> 4, c4 = (etid & 15) * 3;
+                for (int r0 = 0; r0 < T; r0 += 32) {
+                    float4 v[4][3];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int r = r0 + 8 * k + rsub;
+                        if (r < T) {
+                            const float4* src = reinterpret_cast<const float4*>(args.y + (size_t)r * args.ncols1 + tile * kPTile) + c4;
+                            v[k][0] = __ldcg(src);
+                            v[k][1] = __ldcg(src + 1);
+                            v[k][2] = __ldcg(src + 2);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int r = r0 + 8 * k + rsub;
+                        float s2 = 0.f;
+                        if (r < T) {
+#pragma unroll
+                            for (int j = 0; j < 3; ++j) {
+                                const int col = tile * kPTile + (c4 + j) * 4;
+                                const uint2 g = *reinterpret_cast<const uint2*>(args.gamma_cq + col);
+                                const float4 w = v[k][j];
+                                s2 += w.x * w.x + w.y * w.y + w.z * w.z + w.w * w.w;
+                                uint2 o;
+                                o.x = pack_bf16(bf16_lo(g.x) * w.x, bf16_hi(g.x) * w.y);
+                                o.y = pack_bf16(bf16_lo(g.y) * w.z, bf16_hi(g.y) * w.w);
+                                *reinterpret_cast<uint2*>(args.cq + (size_t)r * args.hcq + col) = o;
+                            }
+                        }
+#pragma unroll
+                        for (int o = 8; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+                        if ((etid & 15) == 0 && r < T) args.ss[(size_t)tile * T + r] = s2;
+                    }
+                }
+                epi_bar();
+                if (etid == 0)
+                    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(args.cqflags + tile), "l"(args.tag) : "memory");
             }
         }
         if (!ok) fail();
-        ok = !epi_any(!ok);   // uniform over the 128 threads: the flag waits below are collective
-        if (n1s > 0) publish(args.p1flags + blockIdx.x);
-
-        // ---- R: the k-range sum of one 16-column chunk, once its tile's s1 units are stored
-        const int nchunks = args.ncols1 / kPChunk;
-        if (ok && (int)blockIdx.x < nchunks) {
-            const int rtile = (int)blockIdx.x / (192 / kPChunk);
-            ok = wait_flags(args.p1flags + rtile, args.s1, args.n1, args.tag, s_abort, etid);
-        }
-        if (ok && (int)blockIdx.x < nchunks) {
-            const int col0 = (int)blockIdx.x * kPChunk;
-            const int cg = etid & 3;
-            const int col = col0 + 4 * cg;
-            const size_t slot_stride = (size_t)T * args.ncols1;
-            // Rows in rounds of 32; every lane runs every round (the shuffles need the whole
-            // warp), rows at or past T only skip their loads and stores.
-            for (int r0 = 0; r0 < T; r0 += 32) {
-                const int r = r0 + (etid >> 2);
-                const bool valid = r < T;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (valid) {
-                    float4 w[kPMaxS];
-#pragma unroll
-                    for (int k = 0; k < kPMaxS; ++k)
-                        if (k < args.s1)
-                            w[k] = __ldcg(reinterpret_cast<const float4*>(args.y1 + k * slot_stride + (size_t)r * args.ncols1 + col));
-                    v = w[0];
-#pragma unroll
-                    for (int k = 1; k < kPMaxS; ++k)
-                        if (k < args.s1) {
-                            v.x += w[k].x;
-                            v.y += w[k].y;
-                            v.z += w[k].z;
-                            v.w += w[k].w;
-                        }
-                }
-                float s2 = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-                s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
-                s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
-                if (!valid) continue;
-                if (col0 < args.hcq + args.hckv && cg == 0) args.ss[(size_t)blockIdx.x * T + r] = s2;
-                if (col0 < args.hcq) {
-                    const uint2 g = *reinterpret_cast<const uint2*>(args.gamma_cq + col);
-                    uint2 o;
-                    o.x = pack_bf16(bf16_lo(g.x) * v.x, bf16_hi(g.x) * v.y);
-                    o.y = pack_bf16(bf16_lo(g.y) * v.z, bf16_hi(g.y) * v.w);
-                    *reinterpret_cast<uint2*>(args.cq + (size_t)r * args.hcq + col) = o;
-                } else {
-                    *reinterpret_cast<float4*>(args.ykv + (size_t)r * (args.hckv + args.dr) + (col - args.hcq)) = v;
-                }
-            }
-        }
-        if ((int)blockIdx.x < nchunks) publish(args.cflags + blockIdx.x);
+        ok = !epi_any(!ok);   // uniform over the 128 threads: the waits below are collective
 
         if (ok && head) {
-            // Every c^Q chunk is reduced (one collective wait for all of them) ...
-            ok = wait_flags(args.cflags, args.hcq / kPChunk, 1, args.tag, s_abort, etid);
-            // ... then the P3 activation tiles come by TMA (warp 2) ...
+            // Every c^Q tile is written ...
+            ok = wait_tiles(args.cqflags, nullptr, 0, ncq, 0u, args.tag, s_abort, etid);
+            // ... then P3's activation tiles come by TMA (warp 2) ...
             if (etid == 0) mbar_arrive(smem_u32(cq_ready));
-            // ... and each row's 1 / RMS: the 128 threads split the chunk sums (a fixed order in
-            // each part, the parts added in order).
+            // ... and each row's 1 / RMS from the tiles' sums of y^2 (in tile order).
             float inv = 0.f;
-            {
-                const int nq = args.hcq / kPChunk;
-                const int rows_per = T <= 32 ? 32 : 64;
-                const int parts = 128 / rows_per;
-                const int pr = etid % rows_per, pp = etid / rows_per;
-                const int per = (nq + parts - 1) / parts;
-                float part = 0.f;
-                if (ok && pr < T) {
-                    const int c0 = pp * per, c1 = nq < c0 + per ? nq : c0 + per;
-                    const float* sp = args.ss + pr;
-                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                    int c = c0;
-#pragma unroll 2
-                    for (; c + 3 < c1; c += 4) {
-                        a0 += __ldcg(sp + (size_t)c * T);
-                        a1 += __ldcg(sp + (size_t)(c + 1) * T);
-                        a2 += __ldcg(sp + (size_t)(c + 2) * T);
-                        a3 += __ldcg(sp + (size_t)(c + 3) * T);
-                    }
-                    for (; c < c1; ++c) a0 += __ldcg(sp + (size_t)c * T);
-                    part = (a0 + a1) + (a2 + a3);
-                }
-                ssum[pp * 64 + pr] = part;
-                epi_bar();
-                if (row < T) {
-                    float s2 = 0.f;
-                    for (int k = 0; k < parts; ++k) s2 += ssum[k * 64 + row];
-                    inv = 1.f / sqrtf(s2 / (float)args.hcq + args.eps_cq);
-                }
+            if (ok && row < T) {
+                float s2 = 0.f;
+                for (int t = 0; t < ncq; ++t) s2 += __ldcg(args.ss + (size_t)t * T + row);
+                inv = 1.f / sqrtf(s2 / (float)args.hcq + args.eps_cq);
             }
             // ---- P3 epilogue: 1 / RMS per token, RoPE -> queryRopeOut, q^C -> P4's A operand
             ok = acc_ready(1);
@@ -619,42 +613,50 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
         }
 
-        // ---- KV: the cache rows, by the CTAs without a head (or by every CTA if none is free)
+        // ---- KV: the cache rows, by the CTAs without a head (or by every CTA if none is free),
+        // once the c^KV | k^R tiles are complete
         ok = !epi_any(!ok);
         if (ok && args.nslots > 0) {
             const int spare = G - args.N;
             const int first = spare > 0 ? (int)blockIdx.x - args.N : (int)blockIdx.x;
             const int step = spare > 0 ? spare : G;
-            const int ld = args.hckv + args.dr;
             const int h = args.dr / 2;
-            const int c0 = args.hcq / kPChunk, nkv = (args.hckv + args.dr) / kPChunk;
-            if (first >= 0 && first < T) ok = wait_flags(args.cflags + c0, nkv, 1, args.tag, s_abort, etid);
+            if (first >= 0 && first < T)
+                ok = wait_tiles(args.zflags, args.cnt, ncq, args.n1, (unsigned int)args.s1, args.tag, s_abort, etid);
             if (ok && first >= 0) {
+                float* wsum = scratch;   // the four warps' sums of squares
                 for (int t = first; t < T; t += step) {
                     const long long slot = args.cache_index[t];
-                    if (slot < 0 || slot >= args.nslots) {
+                    if (slot < 0 || slot >= args.nslots) {   // the same for every thread
                         if (etid == 0) atomicOr(args.status, kStatusCacheIndexRange);
                         continue;
                     }
-                    float s2 = 0.f;
-                    for (int c = 0; c < args.hckv / kPChunk; ++c) s2 += __ldcg(args.ss + (size_t)(c0 + c) * T + t);
-                    const float inv = 1.f / sqrtf(s2 / (float)args.hckv + args.eps_ckv);
-                    const float* y = args.ykv + (size_t)t * ld;
-                    __nv_bfloat16* kv = args.kv_cache + slot * args.hckv;
-                    for (int j = 2 * etid; j < args.hckv; j += 256) {
-                        const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(args.gamma_ckv + j);
-                        *reinterpret_cast<__nv_bfloat162*>(kv + j) =
-                            __floats2bfloat162_rn(__low2float(g2) * __ldcg(y + j) * inv, __high2float(g2) * __ldcg(y + j + 1) * inv);
+                    const float* yr = args.y + (size_t)t * args.ncols1 + args.hcq;
+                    // RmsNorm of c^KV: four of the Hckv = 512 values per thread
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(yr) + etid);
+                    float s2 = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+                    if (lane == 0) wsum[q] = s2;
+                    epi_bar();
+                    const float inv = 1.f / sqrtf(((wsum[0] + wsum[1]) + (wsum[2] + wsum[3])) / (float)args.hckv + args.eps_ckv);
+                    const uint2 g = *reinterpret_cast<const uint2*>(args.gamma_ckv + 4 * etid);
+                    uint2 o;
+                    o.x = pack_bf16(bf16_lo(g.x) * v.x * inv, bf16_hi(g.x) * v.y * inv);
+                    o.y = pack_bf16(bf16_lo(g.y) * v.z * inv, bf16_hi(g.y) * v.w * inv);
+                    *reinterpret_cast<uint2*>(args.kv_cache + slot * args.hckv + 4 * etid) = o;
+                    // RoPE of k^R
+                    if (etid < h) {
+                        const float* kr = yr + args.hckv;
+                        const __nv_bfloat16* cs = args.rope_cos + (size_t)t * args.dr;
+                        const __nv_bfloat16* sn = args.rope_sin + (size_t)t * args.dr;
+                        __nv_bfloat16* dkr = args.kr_cache + slot * args.dr;
+                        const float x0 = __ldcg(kr + etid), x1 = __ldcg(kr + etid + h);
+                        dkr[etid] = __float2bfloat16_rn(x0 * __bfloat162float(cs[etid]) - x1 * __bfloat162float(sn[etid]));
+                        dkr[etid + h] =
+                            __float2bfloat16_rn(x1 * __bfloat162float(cs[etid + h]) + x0 * __bfloat162float(sn[etid + h]));
                     }
-                    const float* kr = y + args.hckv;
-                    const __nv_bfloat16* cs = args.rope_cos + (size_t)t * args.dr;
-                    const __nv_bfloat16* sn = args.rope_sin + (size_t)t * args.dr;
-                    __nv_bfloat16* dkr = args.kr_cache + slot * args.dr;
-                    for (int j = etid; j < h; j += 128) {
-                        const float x0 = __ldcg(kr + j), x1 = __ldcg(kr + j + h);
-                        dkr[j] = __float2bfloat16_rn(x0 * __bfloat162float(cs[j]) - x1 * __bfloat162float(sn[j]));
-                        dkr[j + h] = __float2bfloat16_rn(x1 * __bfloat162float(cs[j + h]) + x0 * __bfloat162float(sn[j + h]));
-                    }
+                    epi_bar();   // wsum is reused by the next token
                 }
             }
         }

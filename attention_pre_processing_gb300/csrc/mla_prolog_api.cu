@@ -232,7 +232,7 @@ struct Plan {
     bool g1_pair = false;    // K1 with 256 x 256 tiles on SM pairs (prefill)
     bool persist = false;    // decode-sized bf16 call: the one persistent kernel of decode_persist.cuh
     int p_n1 = 0, p_s1 = 0, p_wst = 0, p_arows = 0;
-    size_t p_smem = 0, off_pss = 0, off_pykv = 0, off_pbar = 0;
+    size_t p_smem = 0, off_pbar = 0;
     int64_t ncols1 = 0, ncols2 = 0;
     size_t off_cq = 0, off_cqs = 0, off_qc = 0, off_y1 = 0, off_y2 = 0, off_xb = 0, off_wdq = 0, off_wdkvkr = 0,
            off_wuqqr = 0, bytes = 0;
@@ -335,7 +335,7 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
         if (s1 > kPMaxS) s1 = kPMaxS;
         if (!sc.x_i8 && !sc.uqqr_i8 && !sc.kv_i8 && !sc.kr_i8 && !sc.q_i8 && T >= 1 && T <= kPMaxT &&
             d.D == 128 && d.Dr == 64 && d.Hckv == 512 && d.Hcq % 192 == 0 && d.He % 64 == 0 && ncols1 % 192 == 0 &&
-            d.N >= 1 && d.N <= sms && ncols1 / kPChunk <= sms && s1 >= 1 && wst >= 4) {
+            d.N >= 1 && d.N <= sms && s1 >= 1 && wst >= 4) {
             p.persist = true;
             p.p_n1 = n1;
             p.p_s1 = s1;
@@ -354,13 +354,9 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     p.off_cq = take((size_t)T * d.Hcq * 2);
     p.off_cqs = take((size_t)T * 4);
     p.off_qc = take((size_t)T * d.N * d.D * 2);
-    const int y1_slots = p.persist && p.p_s1 > p.g1.ksplit ? p.p_s1 : p.g1.ksplit;
-    p.off_y1 = take((size_t)y1_slots * T * p.ncols1 * 4);
-    if (p.persist) {
-        p.off_pss = take((size_t)((d.Hcq + d.Hckv) / kPChunk) * T * 4);
-        p.off_pykv = take((size_t)T * (d.Hckv + d.Dr) * 4);
-        p.off_pbar = take((size_t)(sms + p.ncols1 / kPChunk) * 8);   // P1 and chunk flags
-    }
+    p.off_y1 = take((size_t)(p.g1.ksplit > 1 ? p.g1.ksplit : 1) * T * p.ncols1 * 4);
+    // per P1 tile: a flag and a counter; per c^Q tile: a flag and T sums of squares
+    if (p.persist) p.off_pbar = take((size_t)p.p_n1 * (8 + 4) + 8 + (size_t)(d.Hcq / kPTile) * (8 + 4 * T));
     if (!p.g2_fused) p.off_y2 = take((size_t)T * p.ncols2 * 4);
     if (sc.x_i8) {
         p.off_xb = take((size_t)T * d.He * 2);
@@ -475,11 +471,42 @@ void timing_begin(cudaStream_t st) {
 
 // --------------------------------------------------------------------- launch
 
+// cudaFuncSetAttribute only when the (kernel, attribute, device) value changes: the setting
+// persists, and the call costs microseconds of host time that a decode step cannot spare.
+cudaError_t set_attr(const void* fn, cudaFuncAttribute attr, int value) {
+    struct Entry {
+        const void* fn;
+        int attr, value, dev;
+    };
+    static std::mutex mu;
+    static Entry done[256];
+    static int ndone = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    int slot = -1;   // the entry holding the attribute's current value
+    for (int i = 0; i < ndone && slot < 0; ++i)
+        if (done[i].fn == fn && done[i].attr == (int)attr && done[i].dev == dev) slot = i;
+    if (slot >= 0 && done[slot].value == value) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, attr, value);
+    if (e != cudaSuccess) return e;
+    if (slot >= 0)
+        done[slot].value = value;
+    else if (ndone < 256)
+        done[ndone++] = {fn, (int)attr, value, dev};
+    return e;
+}
+template <typename Kernel>
+cudaError_t set_attr(Kernel* k, cudaFuncAttribute attr, int value) {
+    return set_attr(reinterpret_cast<const void*>(k), attr, value);
+}
+
 template <typename Kernel, typename... ArgsT>
 cudaError_t launch(Kernel k, int grid, int block, size_t smem, cudaStream_t st, ArgsT... args) {
     // Every kernel of the prolog runs with the same (maximum) shared-memory carve-out, so the
     // SMs never re-partition L1 / shared memory between consecutive kernels.
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+    cudaError_t e = set_attr(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -509,7 +536,7 @@ cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const C
     args.stages = C::max_stages(args.a_box_rows);
     if (args.stages < 2) return cudaErrorInvalidConfiguration;
     const size_t smem = C::smem_bytes(args.stages, args.a_box_rows);
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+    cudaError_t e = set_attr(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
     if (e != cudaSuccess) return e;
     return launch(k, grid, gemm_threads(EPW), smem, st, a, b0, b1, mo, mo2, args);
 }
@@ -525,9 +552,9 @@ cudaError_t launch_gemm_pair(cudaStream_t st, const CUtensorMap& a, const CUtens
     args.stages = C::max_stages();
     if (args.stages < 2) return cudaErrorInvalidConfiguration;
     const size_t smem = C::smem_bytes(args.stages);
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+    cudaError_t e = set_attr(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    e = set_attr(k, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3((unsigned)gemm_threads(EPW));
@@ -706,12 +733,14 @@ mla_status run(const Launched& L) {
         pa.n1 = p.p_n1;
         pa.s1 = p.p_s1;
         pa.kb1 = (int)(d.He / 64);
-        pa.y1 = y1;
+        pa.y = y1;
+        pa.zflags = reinterpret_cast<unsigned long long*>(ws + p.off_pbar);
+        pa.cnt = reinterpret_cast<unsigned int*>(ws + p.off_pbar + (size_t)p.p_n1 * 8);
+        pa.cqflags = reinterpret_cast<unsigned long long*>(ws + p.off_pbar + (((size_t)p.p_n1 * 12 + 7) & ~(size_t)7));
+        pa.ss = reinterpret_cast<float*>(pa.cqflags + d.Hcq / kPTile);
+        pa.cq = f1.c_q;
         pa.gamma_cq = f1.gamma_cq;
         pa.gamma_ckv = f1.gamma_ckv;
-        pa.cq = f1.c_q;
-        pa.ss = reinterpret_cast<float*>(ws + p.off_pss);
-        pa.ykv = reinterpret_cast<float*>(ws + p.off_pykv);
         pa.eps_cq = f1.eps_cq;
         pa.eps_ckv = f1.eps_ckv;
         pa.cache_index = f1.cache_index;
@@ -724,11 +753,9 @@ mla_status run(const Launched& L) {
         pa.kb2 = (int)(d.Hcq / 64);
         pa.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
         pa.q_out = static_cast<__nv_bfloat16*>(a.qout->data);
-        pa.p1flags = reinterpret_cast<unsigned long long*>(ws + p.off_pbar);
-        pa.cflags = pa.p1flags + L.sms;
         pa.tag = next_tag();
         pa.status = status;
-        e = cudaFuncSetAttribute(decode_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.p_smem);
+        e = set_attr(decode_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.p_smem);
         if (e != cudaSuccess) return MLA_ERR_RUNTIME;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)L.sms);
@@ -814,7 +841,7 @@ mla_status run(const Launched& L) {
         // decode-sized T: every partial load of a row in flight at once; many rows: fewer, so
         // that more rows fit on an SM
         auto fk = T <= kDecodeRows ? finalize_down_kernel<9> : finalize_down_kernel<3>;
-        e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
+        e = set_attr(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
         if (e != cudaSuccess) return MLA_ERR_RUNTIME;
         e = launch(fk, grid, kRowThreads, fsmem, st, f1);
         if (e != cudaSuccess) return MLA_ERR_RUNTIME;

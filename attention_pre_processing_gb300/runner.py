@@ -3,11 +3,12 @@ allocates outputs and the workspace with torch, and enqueues calls.  No arithmet
 prolog happens here; every step runs in libmla_prolog.so."""
 from __future__ import annotations
 
+import ctypes
 from typing import Dict, Optional
 
 import torch
 
-from . import mla_prolog, mla_prolog_device_status, mla_prolog_workspace_size
+from . import _marshal, lib, MlaError, mla_prolog_device_status, mla_prolog_workspace_size
 from .workloads import MlaConfig
 
 INPUT_KEYS = ("x", "w_dq", "w_uqqr", "w_uk", "w_dkvkr", "gamma_cq", "gamma_ckv", "rope_sin", "rope_cos",
@@ -33,9 +34,18 @@ class PrologCall:
                                               if cfg.q_int8 else None)
         self.ws_bytes = mla_prolog_workspace_size(self.t, cfg.eps_cq, cfg.eps_ckv)
         self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        # The tensors stay put between calls: their descriptors are marshalled once.
+        args, self._keep = _marshal(self.t, cfg.eps_cq, cfg.eps_ckv, "PA_BSND")
+        self._args = tuple(args) + (ctypes.c_void_p(self.workspace.data_ptr()), ctypes.c_uint64(self.ws_bytes))
+        self._fn = lib().mla_prolog
 
     def __call__(self, stream=None) -> None:
-        mla_prolog(self.t, self.cfg.eps_cq, self.cfg.eps_ckv, self.workspace, self.ws_bytes, stream=stream)
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        h = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+        rc = self._fn(*self._args, ctypes.c_void_p(h))
+        if rc != 0:
+            raise MlaError(rc, "mla_prolog")
 
     def status(self, stream=None) -> int:
         return mla_prolog_device_status(self.workspace, self.ws_bytes, stream=stream)
