@@ -404,9 +404,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (ok && head) {
                 // P3's activation tiles (c^Q k-blocks), once the epilogue warps have seen every
                 // c^Q tile written.  c^Q was written by other CTAs' ordinary stores and is read
-                // here by the TMA engine: the proxy fence orders the two.
+                // here by the TMA engine, into slots this CTA's epilogue used for staging: the
+                // proxy fence orders both.
                 ok = mbar_wait_sleep(smem_u32(cq_ready), 0, s_abort, kWaitLimitNs);
-                asm volatile("fence.proxy.async.global;" ::: "memory");
+                asm volatile("fence.proxy.async;" ::: "memory");
                 for (int kb = 0; ok && kb < args.kb2; ++kb) {
                     const int s3 = kb % kPA3;
                     if (kb >= kPA3 &&
@@ -457,11 +458,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
         // ---- P1: this CTA's k-range product of one 192-column tile, added into y
         if (n1s > 0) {
-            ok = acc_ready(0);
+            // the tile is zeroed (long before the product is ready: the wait overlaps P1)
+            ok = wait_tiles(args.zflags, args.cnt, tile, tile + 1, 0u, args.tag, s_abort, etid);
+            ok = acc_ready(0) && ok;
             ok = !epi_any(!ok);
-            if (ok) ok = wait_tiles(args.zflags, args.cnt, tile, tile + 1, 0u, args.tag, s_abort, etid);
+            // The warps whose TMEM lanes hold rows < T stage the product in shared memory (P1's
+            // activation slots: its MMAs have completed), then all 128 threads add it into y with
+            // coalesced vector atomics (a row-per-thread pattern would send one L2 request per
+            // 16 bytes).  The staging row stride (196 floats) spreads the row writes over banks.
+            constexpr int kStg = kPTile + 4;
+            float* stg = reinterpret_cast<float*>(aring);
             if (ok && q * 32 < T) {
-                float* dst = args.y + (size_t)row * args.ncols1 + tile * kPTile;
 #pragma unroll 1
                 for (int ch = 0; ch < kPTile / 32; ++ch) {
                     uint32_t r[32];
@@ -470,9 +477,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     if (row < T) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            red_add_v4(dst + ch * 32 + 4 * i, bits_f(r[4 * i]), bits_f(r[4 * i + 1]), bits_f(r[4 * i + 2]),
-                                       bits_f(r[4 * i + 3]));
+                            *reinterpret_cast<uint4*>(stg + row * kStg + ch * 32 + 4 * i) =
+                                make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
                     }
+                }
+            }
+            epi_bar();
+            if (ok) {
+                float* dst = args.y + tile * kPTile;
+                for (int i = etid; i < T * (kPTile / 4); i += 128) {
+                    const int r = i / (kPTile / 4), c4 = i % (kPTile / 4);
+                    const float4 v = *reinterpret_cast<const float4*>(stg + r * kStg + 4 * c4);
+                    red_add_v4(dst + (size_t)r * args.ncols1 + 4 * c4, v.x, v.y, v.z, v.w);
                 }
             }
             // Count this k range in: the named barrier orders every thread's additions before
@@ -488,8 +504,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (*s_last && tile < ncq) {
                 // The last k range of a c^Q tile: bf16(gamma * y) of its 192 columns into cq, and
                 // each token's sum of y^2 over them into ss; then the tile's flag.  Sixteen
-                // threads per row, three float4 each; rows in batches of 32.
-                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                // threads per row, three float4 each; rows in batches of 32.  Thread 0's acquire
+                // and the named barrier order these L2 loads after every k range's additions.
                 const int rsub = etid >> 4, c4 = (etid & 15) * 3;
                 for (int r0 = 0; r0 < T; r0 += 32) {
                     float4 v[4][3];

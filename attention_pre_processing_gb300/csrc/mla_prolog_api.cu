@@ -321,7 +321,7 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     }
 
     // The persistent decode kernel: bf16 operands and outputs, 128 + 64 head layout, 512-wide
-    // c^KV, every head and every reduction chunk on its own CTA.
+    // c^KV, every head on its own CTA.
     {
         const int64_t ncols1 = p.ncols1;
         const int n1 = (int)(ncols1 / 192);
