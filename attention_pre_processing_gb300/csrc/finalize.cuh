@@ -57,6 +57,7 @@ struct DownArgs {
     int cq_quant;                       // dynamic per-token int8 codes of c^Q
     const float* smooth_cq;             // (Hcq) or null
     float* c_q_scale;                   // (T)
+    int cq_done;                        // c^Q was written by the down-projection (rows only need c^KV | k^R)
     uint32_t* status;
 };
 
@@ -160,7 +161,8 @@ __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, floa
     const float inv_kv = 1.f / sqrtf(skv / (float)a.Hckv + a.eps_ckv);
 
     __nv_bfloat16* cq = a.c_q + (size_t)t * a.Hcq;
-    if (!a.cq_quant) {
+    if (a.cq_done) {
+    } else if (!a.cq_quant) {
         for (int j = 2 * tid; j < a.Hcq; j += 2 * NT) {
             const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(gcq + j);
             *reinterpret_cast<__nv_bfloat162*>(cq + j) =
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(kWarpRowThreads) finalize_down_warp_kernel(con
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
     if (t >= a.T) return;   // whole warp
-    const int nq = a.Hcq / 64, nkv = a.Hckv / 64, h = a.Dr / 2;
+    const int nq = a.cq_done ? 0 : a.Hcq / 64, nkv = a.Hckv / 64, h = a.Dr / 2;
     const float* src = a.src.p + (size_t)t * a.src.ncols;
     const long long slot = a.nslots > 0 ? a.cache_index[t] : -1;
     const float sx = a.scale_x ? a.scale_x[t] : 1.f;

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(gemm_threads(EPW), 1)
                      const __grid_constant__ CUtensorMap map_o2, const GemmArgs args) {
     using C = PairCfg<BN, MAXST, OUTB, EPW, KPS>;
     constexpr int kEpiThreads = 128 * EPW;
-    static_assert(OUTB > 0 && (EPI == EPI_F32 || EPI == EPI_QROPE), "pair tiles store through TMA");
+    static_assert(OUTB > 0 && (EPI == EPI_F32 || EPI == EPI_QROPE || EPI == EPI_DOWN), "pair tiles store through TMA");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(gemm_threads(EPW), 1)
         tma_prefetch_map(&map_b0);
         tma_prefetch_map(&map_b1);
         tma_prefetch_map(&map_o);
-        if (EPI == EPI_QROPE) tma_prefetch_map(&map_o2);
+        if (EPI != EPI_F32) tma_prefetch_map(&map_o2);
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
@@ -291,6 +291,8 @@ __global__ void __launch_bounds__(gemm_threads(EPW), 1)
             uh.m_tile = u.m_tile * 2 + (int)rank;
             if constexpr (EPI == EPI_F32)
                 epilogue_f32_tma<BN, 1, OUTB, EPW>(args, uh, tsrc, q, ostage, part);
+            else if constexpr (EPI == EPI_DOWN)
+                epilogue_down_tma<BN, OUTB, EPW>(args, uh, tsrc, q, ostage, &map_o, &map_o2, part);
             else
                 epilogue_qrope_blocks_tma<BN, 1, OUTB, EPW>(args, uh, tsrc, q, ostage, &map_o, &map_o2, part);
             tc_fence_before();

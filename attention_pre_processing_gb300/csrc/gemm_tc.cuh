@@ -39,7 +39,7 @@ constexpr size_t kSmemLimit = 232448;             // 227 KB opt-in per CTA
 constexpr uint32_t kStatusCacheIndexRange = 0x1u;
 constexpr uint32_t kStatusWaitTimeout = 0x2u;
 
-enum Epi : int { EPI_F32 = 0, EPI_QROPE = 1, EPI_QN = 2 };
+enum Epi : int { EPI_F32 = 0, EPI_QROPE = 1, EPI_QN = 2, EPI_DOWN = 3 };
 
 struct GemmArgs {
     int T;               // valid A rows
@@ -77,6 +77,18 @@ struct GemmArgs {
                                    // brings all BN/64 column blocks of a k-block
     int n_fastest;                 // pair tiles: column tile fastest (the row tiles of A then come
                                    // from HBM once, shared by the pairs of all column tiles)
+    // EPI_DOWN (prefill down-projection): columns below cq_cols leave as bf16(gamma_cq * y)
+    // through map_o2 with each row's sum of y^2 per (tile, epilogue part) in ss_out; the rest
+    // as fp32 through map_o
+    int cq_cols;
+    const __nv_bfloat16* gamma_cq;
+    float* ss_out;                 // T x nss
+    int nss;                       // sums per row
+    // EPI_QROPE with ss_in: the RmsNorm scale 1 / sqrt(sum(ss_in[row]) / hcq + eps_cq) of each
+    // row multiplies the product (c^Q reaches the up-projection as bf16(gamma_cq * y))
+    const float* ss_in;            // T x nss
+    int hcq;
+    float eps_cq;
     uint32_t* status;
 };
 
@@ -426,6 +438,51 @@ __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const Unit& 
     }
 }
 
+// Prefill down-projection (EPI_DOWN): a tile of c^Q columns leaves as bf16(gamma_cq * y)
+// through map_c in 64-column blocks, and each row's sum of y^2 over this warp's blocks goes to
+// ss_out[row][tile * EPW + part]; a tile of c^KV | k^R columns leaves as fp32 through map_f (the
+// row pass reads those).  A tile never straddles cq_cols.
+template <int BN, int OUTB, int EPW>
+__device__ __forceinline__ void epilogue_down_tma(const GemmArgs& a, const Unit& u, const TmemSrc& src, int q,
+                                                  OutStage<OUTB>& out, const CUtensorMap* map_f,
+                                                  const CUtensorMap* map_c, int part) {
+    const int row0 = u.m_tile * 128 + q * 32;
+    if (row0 >= a.T) return;   // warp-uniform
+    const int c0 = u.n_tile * BN;
+    if (c0 >= a.cq_cols) {
+        epilogue_f32_tma<BN, 1, OUTB, EPW>(a, u, src, q, out, part);
+        return;
+    }
+    const int row = row0 + out.lane;
+    float s2 = 0.f;
+#pragma unroll 1
+    for (int blk = part; blk < BN / 64; blk += EPW) {
+        const int col = c0 + 64 * blk;
+        float v0[32], v1[32];
+        src.load(0, BN, 64 * blk, v0);
+        src.load(0, BN, 64 * blk + 32, v1);
+        uint32_t w[32];
+        const uint4* gp = reinterpret_cast<const uint4*>(a.gamma_cq + col);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float* v = h ? v1 : v0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 g = __ldg(gp + 4 * h + k);
+                const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = v[8 * k + 2 * e], x1 = v[8 * k + 2 * e + 1];
+                    s2 += x0 * x0 + x1 * x1;
+                    w[16 * h + 4 * k + e] = pack_bf16(bf16_lo(gw[e]) * x0, bf16_hi(gw[e]) * x1);
+                }
+            }
+        }
+        out.put(w, col, row0, map_c);
+    }
+    if (row < a.T) a.ss_out[(size_t)row * a.nss + u.n_tile * EPW + part] = s2;
+}
+
 // One head per tile (EPI_QROPE, no dequant scales): q^C (128 columns) and RoPE(q^R) (64
 // columns) through shared memory and TMA stores into the (T, N*128) and (T, N*64) views.
 template <int MSUB, int OUTB>
@@ -508,6 +565,12 @@ __device__ __forceinline__ void epilogue_qrope_blocks_tma(const GemmArgs& a, con
         if (row0 >= a.T) continue;   // warp-uniform
         const int row = row0 + out.lane;
         const bool valid = row < a.T;
+        float inv = 1.f;
+        if (a.ss_in != nullptr && valid) {
+            float s2 = 0.f;
+            for (int k = 0; k < a.nss; ++k) s2 += a.ss_in[(size_t)row * a.nss + k];
+            inv = 1.f / sqrtf(s2 / (float)a.hcq + a.eps_cq);
+        }
 #pragma unroll 1
         for (int blk = part; blk < BN / 64; blk += EPW) {   // this warp's share of the blocks
             const int b = (u.n_tile * BN) / 64 + blk;   // global 64-column block
@@ -516,6 +579,11 @@ __device__ __forceinline__ void epilogue_qrope_blocks_tma(const GemmArgs& a, con
             float v0[32], v1[32];
             src.load(ms, BN, 64 * blk, v0);
             src.load(ms, BN, 64 * blk + 32, v1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                v0[i] *= inv;
+                v1[i] *= inv;
+            }
             uint32_t w[32];
             if (part < 2) {
 #pragma unroll

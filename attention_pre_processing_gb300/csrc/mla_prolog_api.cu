@@ -230,6 +230,8 @@ struct Plan {
     bool g2_fused = false;   // K2 epilogue does RoPE and q^C (no finalize_up)
     bool g2_wide = false;    // K2 with 256 x 256 tiles on SM pairs (prefill)
     bool g1_pair = false;    // K1 with 256 x 256 tiles on SM pairs (prefill)
+    bool fold_cq = false;    // K1 writes bf16(gamma_cq * y) and row sums of squares, K2 applies 1 / RMS
+    size_t off_ss = 0;       // fold_cq: T x kFoldSums row sums of squares
     bool persist = false;    // decode-sized bf16 call: the one persistent kernel of decode_persist.cuh
     int p_n1 = 0, p_s1 = 0, p_wst = 0, p_arows = 0;
     size_t p_smem = 0, off_pbar = 0;
@@ -241,6 +243,7 @@ struct Plan {
 constexpr size_t kStatusBytes = 1024;
 constexpr int kDecodeRows = 256;   // up to this many tokens: one row tile, weight streaming
 constexpr int kPairKps = 2;         // k-blocks per stage of the prefill GEMMs on SM pairs
+constexpr int kFoldSums = 16;       // row sums of squares per token in the folded c^Q RmsNorm (at most)
 
 size_t up1024(size_t v) { return (v + 1023) & ~size_t(1023); }
 
@@ -300,6 +303,10 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     // blocks into q^C and rope blocks).
     p.g2_fused = d.D == 128 && d.Dr == 64;
     p.g2_wide = p.g2_fused && T > kDecodeRows && p.ncols2 % 256 == 0 && !sc.uqqr_i8;
+    // The RmsNorm of c^Q folded into the two prefill GEMMs (bf16 operands): no row pass over c^Q.
+    // (the row pass that then handles only c^KV | k^R is the warp-per-token one)
+    p.fold_cq = p.g1_pair && p.g2_wide && !sc.x_i8 && d.Hcq % 256 == 0 && d.Hcq / 256 * 2 <= kFoldSums &&
+                d.Dr == 64 && d.Hckv % 64 == 0 && d.Hcq <= 64 * kWQ && d.Hckv <= 64 * kWKV;
     plan_gemm(p.g2, T, p.ncols2, d.Hcq, sms, p.g2_wide ? 256 : 192, false);
     if (p.g2_wide) {
         p.g2.msub = 2;
@@ -355,6 +362,7 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     p.off_cqs = take((size_t)T * 4);
     p.off_qc = take((size_t)T * d.N * d.D * 2);
     p.off_y1 = take((size_t)(p.g1.ksplit > 1 ? p.g1.ksplit : 1) * T * p.ncols1 * 4);
+    if (p.fold_cq) p.off_ss = take((size_t)T * kFoldSums * 4);
     // per P1 tile: a flag and a counter; per c^Q tile: a flag and T sums of squares
     if (p.persist) p.off_pbar = take((size_t)p.p_n1 * (8 + 4) + 8 + (size_t)(d.Hcq / kPTile) * (8 + 4 * T));
     if (!p.g2_fused) p.off_y2 = take((size_t)T * p.ncols2 * 4);
@@ -684,6 +692,7 @@ mla_status run(const Launched& L) {
     f1.cq_quant = sc.uqqr_i8;
     f1.smooth_cq = a.smooth ? static_cast<const float*>(a.smooth->data) : nullptr;
     f1.c_q_scale = reinterpret_cast<float*>(ws + p.off_cqs);
+    f1.cq_done = p.fold_cq ? 1 : 0;
     f1.status = status;
     const float* row_scale = sc.uqqr_i8 ? reinterpret_cast<const float*>(ws + p.off_cqs) : nullptr;
     const float* col_scale = sc.uqqr_i8 ? static_cast<const float*>(a.swuqqr->data) : nullptr;
@@ -814,7 +823,18 @@ mla_status run(const Launched& L) {
     g1.out_f32 = y1;
     if (p.g1_pair && !g1.tma_out) return MLA_ERR_RUNTIME;   // pair tiles store only through TMA
     g1.n_fastest = 1;   // x (T x He) is larger than the weights: read each row tile once
-    if (p.g1_pair)
+    if (p.fold_cq) {
+        CUtensorMap mCq;
+        const uint64_t dims[2] = {(uint64_t)d.Hcq, (uint64_t)d.T};
+        const uint64_t strides[1] = {(uint64_t)d.Hcq * 2};
+        const uint32_t box[2] = {64, 32};
+        if (!encode_map(&mCq, ws + p.off_cq, 2, dims, strides, box)) return MLA_ERR_RUNTIME;
+        g1.cq_cols = (int)d.Hcq;
+        g1.gamma_cq = f1.gamma_cq;
+        g1.ss_out = reinterpret_cast<float*>(ws + p.off_ss);
+        g1.nss = (int)(d.Hcq / 256) * 2;
+        e = launch_gemm_pair<256, 8, EPI_DOWN, 1, 2, kPairKps>(st, mA1, mB1a, mB1b, g1, mO1, mCq);
+    } else if (p.g1_pair)
         e = launch_gemm_pair<256, 8, EPI_F32, 1, 2, kPairKps>(st, mA1, mB1a, mB1b, g1, mO1, mO1);
     else if (p.g1.bn == 64)
         e = launch_gemm<64, 1, 32, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
@@ -880,6 +900,12 @@ mla_status run(const Launched& L) {
     g2.q_rope = static_cast<__nv_bfloat16*>(a.qrope->data);
     g2.rope_cos = f1.rope_cos;
     g2.rope_sin = f1.rope_sin;
+    if (p.fold_cq) {
+        g2.ss_in = reinterpret_cast<const float*>(ws + p.off_ss);
+        g2.nss = (int)(d.Hcq / 256) * 2;
+        g2.hcq = (int)d.Hcq;
+        g2.eps_cq = f1.eps_cq;
+    }
     g2.row_scale = row_scale;
     g2.col_scale = col_scale;
     g2.out_f32 = reinterpret_cast<float*>(ws + p.off_y2);
