@@ -598,6 +598,32 @@ cudaError_t launch_gemm_pair(cudaStream_t st, const CUtensorMap& a, const CUtens
     return cudaLaunchKernelEx(&cfg, k, a, b0, b1, out, out2, args);
 }
 
+// A second stream per device for work that nothing later in the call reads (the cache rows of
+// a folded prefill call): it runs beside the tensor-core kernels instead of between them.  The
+// fork and join are event edges, so stream capture records them as graph edges.  The mutex
+// keeps two host threads from interleaving on the shared events.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+cudaError_t side_stream(SideStream** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    SideStream& sd = g_side[dev];
+    if (sd.s == nullptr) {
+        if ((e = cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &sd;
+    return cudaSuccess;
+}
+
 struct Launched {
     const Args* a;
     Dims d;
@@ -632,6 +658,8 @@ mla_status run(const Launched& L) {
     uint32_t* status = reinterpret_cast<uint32_t*>(ws);
     const int T = (int)d.T;
     if (!get_encoder()) return MLA_ERR_RUNTIME;
+    SideStream* side = nullptr;   // set once work is forked onto the side stream
+    std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
 
     // int8 operands are widened to bf16 (exact) for the bf16 tensor-core path.
     const void* x_bf = a.x->data;
@@ -852,9 +880,22 @@ mla_status run(const Launched& L) {
         d.Hcq <= 64 * kWQ && d.Hckv <= 64 * kWKV) {
         // many tokens: one warp per token, the row in registers
         const int wpc = kWarpRowThreads / 32;
-        e = launch(finalize_down_warp_kernel, (T + wpc - 1) / wpc, kWarpRowThreads, 0, st, f1);
-        if (e != cudaSuccess) return MLA_ERR_RUNTIME;
-        timing_mark(st, "f1_norm_rope_cache");
+        if (p.fold_cq && !g_timing.enabled) {
+            // only the cache rows are left, and no later kernel of the call reads them: on the
+            // side stream, beside K2 / K3
+            SideStream* sd = nullptr;
+            if (side_stream(&sd) != cudaSuccess) return MLA_ERR_RUNTIME;
+            side_lock.lock();
+            side = sd;
+            if (cudaEventRecord(sd->fork, st) != cudaSuccess || cudaStreamWaitEvent(sd->s, sd->fork, 0) != cudaSuccess)
+                return MLA_ERR_RUNTIME;
+            e = launch(finalize_down_warp_kernel, (T + wpc - 1) / wpc, kWarpRowThreads, 0, sd->s, f1);
+            if (e != cudaSuccess || cudaEventRecord(sd->join, sd->s) != cudaSuccess) return MLA_ERR_RUNTIME;
+        } else {
+            e = launch(finalize_down_warp_kernel, (T + wpc - 1) / wpc, kWarpRowThreads, 0, st, f1);
+            if (e != cudaSuccess) return MLA_ERR_RUNTIME;
+            timing_mark(st, "f1_norm_rope_cache");
+        }
     } else {
         const int grid = T < 16 * L.sms ? T : 16 * L.sms;
         const size_t fsmem = down_smem_bytes((int)d.Hcq, (int)d.Hckv, (int)d.Dr);
@@ -977,6 +1018,7 @@ mla_status run(const Launched& L) {
     }
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k3_absorb_uk");
+    if (side != nullptr && cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return MLA_ERR_RUNTIME;
     if (g_timing.enabled) g_timing.have = true;
     return MLA_OK;
 }
