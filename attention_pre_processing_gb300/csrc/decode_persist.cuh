@@ -110,8 +110,8 @@ __device__ __forceinline__ bool p_step(const PersistArgs& a, int i, int n1s, PSt
         return true;
     }
     i -= a.kb2;
-    if (i < 6) {   // D = 128: two k-blocks x three column groups
-        const int kb = i / 3, g = i % 3;
+    if (i < 6) {   // D = 128: three column groups x two k-blocks, group by group
+        const int g = i / 2, kb = i % 2;
         s = {4, kb, g, kb == 0, i == 5};
         return true;
     }
@@ -202,8 +202,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint64_t* aempty = afull + kPA;               // [kPA]
     uint64_t* afull3 = aempty + kPA;              // [kPA3]
     uint64_t* aempty3 = afull3 + kPA3;            // [kPA3]
-    uint64_t* tfull = aempty3 + kPA3;             // [3]: P1, P3, P4 accumulators
-    uint64_t* chain_full = tfull + 3;
+    uint64_t* tfull = aempty3 + kPA3;             // [3]: P1, P3 accumulators ([2] unused)
+    uint64_t* tfull4 = tfull + 3;                 // [3]: P4 column groups
+    uint64_t* chain_full = tfull4 + 3;
     uint64_t* cq_ready = chain_full + 1;         // the epilogue saw every c^Q tile written
     uint64_t* done = cq_ready + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
@@ -240,7 +241,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(smem_u32(&afull3[s]), 1);
             mbar_init(smem_u32(&aempty3[s]), 1);
         }
-        for (int p = 0; p < 3; ++p) mbar_init(smem_u32(&tfull[p]), 1);
+        for (int p = 0; p < 3; ++p) {
+            mbar_init(smem_u32(&tfull[p]), 1);
+            mbar_init(smem_u32(&tfull4[p]), 1);
+        }
         mbar_init(smem_u32(chain_full), 128);
         mbar_init(smem_u32(cq_ready), 1);
         mbar_init(smem_u32(done), 1);
@@ -367,16 +371,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     umma_commit(smem_u32(&aempty3[used_a]));
                 }
                 if (ok) umma_commit(smem_u32(&tfull[1]));
-                // P4: A = q^C in activation slots 0 and 1; three column groups per k-block
+                // P4: A = q^C in activation slots 0 and 1; column group by column group (both
+                // k-blocks), each group's accumulator committed on its own so that its epilogue
+                // overlaps the next groups' MMAs
                 ok = ok && mbar_wait(smem_u32(chain_full), 0, s_abort, kWaitLimitNs) && wait_w();
-                for (int i = 0; ok && i < 6; ++i) {
-                    const int kb = i / 3, g = i % 3;
-                    const int used_w =
-                        mma4(adesc0 + (uint64_t)kb * a_unit, tmem_base + 192 * g, g == 2 ? id128 : id192, kb == 0);
-                    if (i + 1 < 6) ok = wait_w();
-                    umma_commit(smem_u32(&wempty[used_w]));
+                for (int g = 0; ok && g < 3; ++g) {
+                    const uint32_t id = g == 2 ? id128 : id192;
+                    const int u0 = mma4(adesc0, tmem_base + 192 * g, id, true);
+                    ok = wait_w();
+                    int u1 = -1;
+                    if (ok) u1 = mma4(adesc0 + a_unit, tmem_base + 192 * g, id, false);
+                    if (ok && g < 2) ok = wait_w();
+                    umma_commit(smem_u32(&wempty[u0]));
+                    if (u1 >= 0) umma_commit(smem_u32(&wempty[u1]));
+                    if (ok) umma_commit(smem_u32(&tfull4[g]));
                 }
-                if (ok) umma_commit(smem_u32(&tfull[2]));
             }
             if (!ok) fail();
             umma_commit(smem_u32(done));
@@ -607,25 +616,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(chain_full));
 
-            // ---- P4 epilogue: queryOut through shared memory and TMA stores
-            ok = ok && acc_ready(2);
-            if (ok && q * 32 < T) {
-                // every weight stage has been consumed: the ring is free for staging
-                OutStage<2> out{wring + (size_t)(warp - 4) * 2 * 4096, 0, &map_o, lane};
+            // ---- P4 epilogue: queryOut through shared memory and TMA stores, group by group.
+            // Staging: the ring slot of P4's first weight stage (the last phase: once group 0 is
+            // complete that slot is never loaded again); 8 KB per warp, at most two warps.
+            {
+                const int slot0 = (n1s + args.kb2) % wst;
+                OutStage<2> out{wring + (size_t)slot0 * kPStage + (size_t)(warp - 4) * 2 * 4096, 0, &map_o, lane};
                 const TmemSrc src{tmem_base + ((uint32_t)(q * 32) << 16)};
+                for (int g = 0; ok && g < 3; ++g) {
+                    int r = 1;
+                    if (lane == 0) r = mbar_wait_sleep(smem_u32(&tfull4[g]), 0, s_abort, kWaitLimitNs) ? 1 : 0;
+                    ok = __shfl_sync(0xffffffffu, r, 0) != 0;
+                    __syncwarp();
+                    tc_fence_after();
+                    if (!ok || q * 32 >= T) continue;
 #pragma unroll 1
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t w[32];
-                    float v[32];
-                    src.load(0, 0, 64 * j, v);
+                    for (int j = 3 * g; j < (g == 2 ? 8 : 3 * g + 3); ++j) {
+                        uint32_t w[32];
+                        float v[32];
+                        src.load(0, 0, 64 * j, v);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-                    src.load(0, 0, 64 * j + 32, v);
+                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+                        src.load(0, 0, 64 * j + 32, v);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-                    out.put(w, (int)blockIdx.x * 512 + 64 * j, q * 32);
+                        for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+                        out.put(w, (int)blockIdx.x * 512 + 64 * j, q * 32);
+                    }
                 }
-                out.drain();
+                if (q * 32 < T) out.drain();
             }
         }
 

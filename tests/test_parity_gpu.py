@@ -239,8 +239,8 @@ def test_persistent_decode_repeatable():
     PrologCall = _runner()
     a = PrologCall(cfg, inp)
     b = PrologCall(cfg, inp)
-    for _ in range(3):
-        a()
+    a()
+    for _ in range(20):   # many calls on b: a race in the cross-CTA hand-offs would show
         b()
     torch.cuda.synchronize()
     assert a.status() == 0 and b.status() == 0
