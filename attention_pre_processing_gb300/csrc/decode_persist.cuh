@@ -298,6 +298,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     s = 0;
                     ph ^= 1;
                 }
+                // The ring now holds the first P3 stages, which wait for the reduction: while HBM
+                // idles, the next eight P3 stages are requested into L2 (all of P3 / P4 would
+                // load L2 enough to stretch the reduction's dependency chain).
+                if (head && i == n1s + wst - 1) {
+                    const uint64_t keep = policy_evict_last();
+                    PStep pf;
+                    for (int k = i + 1; k <= i + 8 && p_step(args, k, n1s, pf); ++k)
+                        if (pf.phase == 3) tma_prefetch_l2_3d(&map_wuqqr, 0, pf.kb * 64, (int)blockIdx.x * 3, keep);
+                }
             }
         }
     } else if (warp == 1) {
@@ -355,20 +364,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (ok && n1s > 0) umma_commit(smem_u32(&tfull[0]));
             }
             if (head) {
-                // P3: activation slots filled by TMA (c^Q)
+                // P3: activation slots filled by TMA (c^Q), two k-blocks per round: eight MMAs
+                // between waits keep the tensor core's short queue from draining (kb2 is even)
                 int sa = 0;
                 uint32_t pha = 0;
-                ok = ok && mbar_wait(smem_u32(&afull3[0]), 0, s_abort, kWaitLimitNs) && wait_w();
-                for (int kb = 0; ok && kb < args.kb2; ++kb) {
-                    const int used_w = mma4(adesc0 + (uint64_t)sa * a_unit, tmem_base, id192, kb == 0);
-                    const int used_a = sa;
-                    if (++sa == kPA3) {
-                        sa = 0;
-                        pha ^= 1;
-                    }
-                    if (kb + 1 < args.kb2) ok = mbar_wait(smem_u32(&afull3[sa]), pha, s_abort, kWaitLimitNs) && wait_w();
-                    umma_commit(smem_u32(&wempty[used_w]));
-                    umma_commit(smem_u32(&aempty3[used_a]));
+                for (int kb = 0; ok && kb < args.kb2; kb += 2) {
+                    const int sa1 = sa + 1 == kPA3 ? 0 : sa + 1;
+                    const uint32_t pha1 = sa + 1 == kPA3 ? pha ^ 1 : pha;
+                    const int sw1 = sw + 1 == wst ? 0 : sw + 1;
+                    const uint32_t phw1 = sw + 1 == wst ? phw ^ 1 : phw;
+                    ok = mbar_wait(smem_u32(&afull3[sa]), pha, s_abort, kWaitLimitNs) && wait_w() &&
+                         mbar_wait(smem_u32(&afull3[sa1]), pha1, s_abort, kWaitLimitNs) &&
+                         mbar_wait(smem_u32(&wfull[sw1]), phw1, s_abort, kWaitLimitNs);
+                    if (!ok) break;
+                    const int uw0 = mma4(adesc0 + (uint64_t)sa * a_unit, tmem_base, id192, kb == 0);
+                    const int uw1 = mma4(adesc0 + (uint64_t)sa1 * a_unit, tmem_base, id192, false);
+                    umma_commit(smem_u32(&wempty[uw0]));
+                    umma_commit(smem_u32(&aempty3[sa]));
+                    umma_commit(smem_u32(&wempty[uw1]));
+                    umma_commit(smem_u32(&aempty3[sa1]));
+                    sa = sa1 + 1 == kPA3 ? 0 : sa1 + 1;
+                    pha = sa1 + 1 == kPA3 ? pha1 ^ 1 : pha1;
                 }
                 if (ok) umma_commit(smem_u32(&tfull[1]));
                 // P4: A = q^C in activation slots 0 and 1; column group by column group (both

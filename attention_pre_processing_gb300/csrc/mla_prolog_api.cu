@@ -341,7 +341,7 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
         if (s1 > kb1) s1 = kb1;
         if (s1 > kPMaxS) s1 = kPMaxS;
         if (!sc.x_i8 && !sc.uqqr_i8 && !sc.kv_i8 && !sc.kr_i8 && !sc.q_i8 && T >= 1 && T <= kPMaxT &&
-            d.D == 128 && d.Dr == 64 && d.Hckv == 512 && d.Hcq % 192 == 0 && d.He % 64 == 0 && ncols1 % 192 == 0 &&
+            d.D == 128 && d.Dr == 64 && d.Hckv == 512 && d.Hcq % 384 == 0 && d.He % 64 == 0 && ncols1 % 192 == 0 &&
             d.N >= 1 && d.N <= sms && s1 >= 1 && wst >= 6) {   // P4 staging needs its six stages in distinct slots
             p.persist = true;
             p.p_n1 = n1;
