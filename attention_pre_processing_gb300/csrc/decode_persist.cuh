@@ -3,27 +3,26 @@
 // 24 KB stages (three 64 x 64 boxes) from the first to the last phase, so HBM never waits for a
 // kernel boundary; only the tensor-core work waits for the data it depends on.
 //
-//   P1   x . [W^DQ | W^DkvKr]: 192-column tiles x s1 k ranges, one unit per CTA; each unit adds
-//        its fp32 product into y (T x ncols1) with vector atomics and counts itself in on its
-//        tile's counter
-//   P3   head n = CTA index, once the c^Q tiles' counters are complete: the epilogue warps turn
-//        y into bf16(gamma * y) k-block by k-block (P3's A operand, in shared memory) and sum
-//        each token's y^2; the tensor core computes (gamma * y) . W^UqQr[:, head n]; the
-//        epilogue multiplies by the token's 1 / RMS, applies RoPE to the rope columns
-//        (queryRopeOut) and writes q^C straight into shared memory as P4's A operand
+//   P1   x . [W^DQ | W^DkvKr]: 192-column tiles x s1 k ranges, one unit per CTA; each unit
+//        stores its fp32 product into its k-range slot of y and counts itself in on its tile's
+//        counter.  Once a c^Q tile's count is complete, its CTAs add the tile's slots in k-range
+//        order, one 16-column chunk each, and write bf16(gamma * y) (P3's activation) and each
+//        token's sum of y^2 over the chunk
+//   P3   head n = CTA index, once every c^Q chunk is written: c^Q by TMA;
+//        (gamma * y) . W^UqQr[:, head n]; the epilogue multiplies by the token's 1 / RMS,
+//        applies RoPE to the rope columns (queryRopeOut) and writes q^C straight into shared
+//        memory as P4's A operand
 //   P4   q^C . W^UK[n] (512 columns) -> queryOut through TMA stores
-//   KV   CTAs without a head, once the c^KV / k^R tiles are complete: RmsNorm of c^KV and RoPE
-//        of k^R, written to the caches at cacheIndex
+//   KV   CTAs without a head, once the c^KV / k^R tiles are complete: the slots added in
+//        k-range order, RmsNorm of c^KV and RoPE of k^R, written to the caches at cacheIndex
 //
 // RmsNorm(y) . W = (1 / RMS(y)) * ((gamma * y) . W): the per-token scale moves behind the
 // contraction, so no row pass sits between the reduction and P3.
 //
-// The k-range products are added with fp32 atomics, so their order follows arrival: results
-// can differ in the last bits from call to call (the kernel-per-step path adds them in fixed
-// order).  Each tile's y rows and counter are zeroed at the start of the call by the tile's
-// first k-range CTA, which then stores the call's tag in the tile's flag; the adders wait for
-// that flag, and readers wait for the flag and a complete counter.  Flags of another call hold
-// another tag, so the workspace needs no initialisation.
+// Every sum is taken in a fixed order, so calls are bit-reproducible.  Each tile's counter is
+// reset at the start of the call by the tile's first k-range CTA, which then stores the call's
+// tag in the tile's flag; readers wait for the flag and a complete counter.  Flags of another
+// call hold another tag, so the workspace needs no initialisation.
 //
 // Roles (256 threads): warp 0 streams weight stages with TMA (one 3D box of three 64-column
 // blocks per stage); warp 1 allocates tensor memory and issues tcgen05.mma; warp 2 loads P1's
@@ -49,6 +48,7 @@ constexpr int kPMaxW = 12;                   // weight stages at most
 constexpr int kPA = 4;                       // P1 activation slots (TMA)
 constexpr int kPA3 = 8;                      // P3 activation slots (written by the epilogue warps)
 constexpr int kPTile = 192;                  // P1 columns per tile
+constexpr int kPChunk = 16;                  // columns per c^Q reduction chunk
 constexpr int kPMaxT = 64;                   // tokens at most
 constexpr int kPMaxS = 16;                   // k ranges at most
 
@@ -56,12 +56,12 @@ struct PersistArgs {
     int T, a_rows, a_bytes, wst;        // tokens, A box rows, A slot bytes, weight stages
     // P1
     int hcq, hckv, dr, ncols1, n1, s1, kb1;
-    float* y;                           // T x ncols1: the k-range products, added in
-    unsigned int* cnt;                  // n1: k ranges of the tile added in
-    unsigned long long* zflags;         // n1: the tile's y rows and counter are zeroed (call tag)
+    float* y;                           // s1 k-range slots of T x ncols1 fp32 products
+    unsigned int* cnt;                  // n1: k ranges of the tile stored
+    unsigned long long* zflags;         // n1: the tile's counter is reset (call tag)
     __nv_bfloat16* cq;                  // T x Hcq: bf16(gamma_cq * y), P3's activation
-    float* ss;                          // (Hcq / 192) x T: each c^Q tile's sum of y^2 per token
-    unsigned long long* cqflags;        // Hcq / 192: the tile's cq and ss are written (call tag)
+    float* ss;                          // (Hcq / 16) x T: each c^Q chunk's sum of y^2 per token
+    unsigned long long* cqflags;        // Hcq / 16: the chunk's cq and ss are written (call tag)
     const __nv_bfloat16* gamma_cq;
     const __nv_bfloat16* gamma_ckv;
     float eps_cq, eps_ckv;
@@ -130,27 +130,31 @@ __device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int* p) {
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
 
-// Waits (bounded) until tiles t0 .. t1 - 1 (at most 32) are ready: the tile's flag holds `tag`
-// (zeroed in this call) and, if `need` > 0, its counter holds `need` (every k range added in).
-// Called by all 128 epilogue threads together.  One warp polls, lane l the tile t0 + l: the flag
-// is read with acquire semantics first, so the counter read after it is this call's; a short
-// sleep between rounds keeps the lines from being hammered.  The named barrier releases the
-// other warps, and every thread then takes an acquire fence.
+// Waits (bounded) until tiles t0 .. t1 - 1 are ready: the tile's flag holds `tag` and, if
+// `need` > 0, its counter holds `need` (every k range stored; at most 32 tiles then, else 128).
+// Called by all 128 epilogue threads together.  One warp polls, lane l the tiles t0 + l + 32 k:
+// the flag is read with acquire semantics first, so the counter read after it is this call's;
+// a short sleep between rounds keeps the lines from being hammered.  The named barrier releases
+// the other warps, and every thread then takes an acquire fence.
 __device__ __forceinline__ bool wait_tiles(const unsigned long long* zf, const unsigned int* cnt, int t0, int t1,
                                            unsigned int need, unsigned long long tag, const volatile int* abort,
                                            int etid) {
     bool ok = true;
     if (etid < 32) {
         const uint64_t start = global_timer_ns();
-        const int t = t0 + etid;
-        bool mine = t >= t1;
+        bool mine[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mine[k] = t0 + etid + 32 * k >= t1;
         while (true) {
-            if (!mine) mine = ld_acquire_u64(zf + t) == tag && (need == 0 || ld_relaxed_u32(cnt + t) == need);
-            if (__all_sync(0xffffffffu, mine)) break;
+            bool all = true;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int t = t0 + etid + 32 * k;
+                if (!mine[k]) mine[k] = ld_acquire_u64(zf + t) == tag && (need == 0 || ld_relaxed_u32(cnt + t) == need);
+                all &= mine[k];
+            }
+            if (__all_sync(0xffffffffu, all)) break;
             if (*abort || global_timer_ns() - start > kWaitLimitNs) {
                 ok = false;
                 break;
@@ -209,7 +213,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint64_t* done = cq_ready + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-    volatile int* s_last = s_abort + 1;   // this CTA added the last k range of its P1 tile
+    volatile int* s_last = s_abort + 1;   // this CTA stored the last k range of its P1 tile
     float* scratch = reinterpret_cast<float*>(smem + 1024);   // 1 KB: the KV rows' warp sums
     uint8_t* aring = smem + 2048;
     uint8_t* wring = aring + (size_t)kPA3 * args.a_bytes;
@@ -466,30 +470,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
         };
         const int ncq = args.hcq / kPTile;    // P1 tiles of c^Q columns; the rest are c^KV | k^R
 
-        // ---- zeroing: the first k-range CTA of each tile clears the tile's y rows and counter,
-        // then stores the call's tag in the tile's flag (release: cumulative over every epilogue
-        // thread's stores, which the named barrier orders before it)
+        // ---- counter reset: the first k-range CTA of each P1 tile zeroes the tile's counter,
+        // then stores the call's tag in the tile's flag (release: the named barrier orders the
+        // reset before it)
         if ((int)blockIdx.x < args.n1) {
             const int zt = blockIdx.x;
-            for (int i = etid; i < T * (kPTile / 4); i += 128) {
-                const int r = i / (kPTile / 4), c4 = i % (kPTile / 4);
-                reinterpret_cast<float4*>(args.y + (size_t)r * args.ncols1 + zt * kPTile)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
             if (etid == 0) *reinterpret_cast<volatile unsigned int*>(args.cnt + zt) = 0u;
             epi_bar();
             if (etid == 0)
                 asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(args.zflags + zt), "l"(args.tag) : "memory");
         }
 
-        // ---- P1: this CTA's k-range product of one 192-column tile, added into y
+        // ---- P1: this CTA's k-range product of one 192-column tile, into its k-range slot of y
         if (n1s > 0) {
-            // the tile is zeroed (long before the product is ready: the wait overlaps P1)
+            const size_t slot_stride = (size_t)T * args.ncols1;
+            // the counter is reset (long before the product is ready: the wait overlaps P1)
             ok = wait_tiles(args.zflags, args.cnt, tile, tile + 1, 0u, args.tag, s_abort, etid);
             ok = acc_ready(0) && ok;
             ok = !epi_any(!ok);
             // The warps whose TMEM lanes hold rows < T stage the product in shared memory (P1's
-            // activation slots: its MMAs have completed), then all 128 threads add it into y with
-            // coalesced vector atomics (a row-per-thread pattern would send one L2 request per
+            // activation slots: its MMAs have completed), then all 128 threads store it with
+            // coalesced 16-byte stores (a row-per-thread pattern would send one L2 request per
             // 16 bytes).  The staging row stride (196 floats) spreads the row writes over banks.
             constexpr int kStg = kPTile + 4;
             float* stg = reinterpret_cast<float*>(aring);
@@ -509,16 +510,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             epi_bar();
             if (ok) {
-                float* dst = args.y + tile * kPTile;
+                float* dst = args.y + ks * slot_stride + tile * kPTile;
                 for (int i = etid; i < T * (kPTile / 4); i += 128) {
                     const int r = i / (kPTile / 4), c4 = i % (kPTile / 4);
-                    const float4 v = *reinterpret_cast<const float4*>(stg + r * kStg + 4 * c4);
-                    red_add_v4(dst + (size_t)r * args.ncols1 + 4 * c4, v.x, v.y, v.z, v.w);
+                    *reinterpret_cast<float4*>(dst + (size_t)r * args.ncols1 + 4 * c4) =
+                        *reinterpret_cast<const float4*>(stg + r * kStg + 4 * c4);
                 }
             }
-            // Count this k range in: the named barrier orders every thread's additions before
-            // thread 0's release; the acquire half lets the last of the tile's k ranges read the
-            // complete sum.
+            // Count this k range in: the named barrier orders every thread's stores before
+            // thread 0's release.
             epi_bar();
             if (etid == 0) {
                 unsigned int old = 0;
@@ -526,64 +526,68 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 *s_last = ok && old + 1 == (unsigned int)args.s1 ? 1 : 0;
             }
             epi_bar();
-            if (*s_last && tile < ncq) {
-                // The last k range of a c^Q tile: bf16(gamma * y) of its 192 columns into cq, and
-                // each token's sum of y^2 over them into ss; then the tile's flag.  Sixteen
-                // threads per row, three float4 each; rows in batches of 32.  Thread 0's acquire
-                // and the named barrier order these L2 loads after every k range's additions.
-                const int rsub = etid >> 4, c4 = (etid & 15) * 3;
-                for (int r0 = 0; r0 < T; r0 += 32) {
-                    float4 v[4][3];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int r = r0 + 8 * k + rsub;
+            constexpr int kChunks = kPTile / kPChunk;   // chunks per tile
+            if (ok && tile < ncq && ks < kChunks) {
+                // The tile's CTAs reduce it, chunk c by the CTAs with c = ks (mod s1): once every
+                // k range is stored (the CTA that completed the count knows at once, the others
+                // wait for the counter), the chunk's slots are added in k-range order,
+                // bf16(gamma * y) goes to cq and each token's sum of y^2 over the chunk to ss;
+                // then the chunk's flag.
+                if (!*s_last) ok = wait_tiles(args.zflags, args.cnt, tile, tile + 1, (unsigned int)args.s1, args.tag, s_abort, etid);
+                else asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                for (int c = ks; ok && c < kChunks; c += args.s1) {
+                    const int col0 = tile * kPTile + c * kPChunk;
+                    // four threads per row, one float4 each; 32 rows per round
+                    const int f4 = etid & 3, rsub = etid >> 2;
+                    const int col = col0 + 4 * f4;
+                    const uint2 g = *reinterpret_cast<const uint2*>(args.gamma_cq + col);
+                    for (int r0 = 0; r0 < T; r0 += 32) {
+                        const int r = r0 + rsub;
+                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
                         if (r < T) {
-                            const float4* src = reinterpret_cast<const float4*>(args.y + (size_t)r * args.ncols1 + tile * kPTile) + c4;
-                            v[k][0] = __ldcg(src);
-                            v[k][1] = __ldcg(src + 1);
-                            v[k][2] = __ldcg(src + 2);
+                            const float* src = args.y + (size_t)r * args.ncols1 + col;
+                            float4 w[kPMaxS];
+#pragma unroll
+                            for (int j = 0; j < kPMaxS; ++j)
+                                if (j < args.s1) w[j] = __ldcg(reinterpret_cast<const float4*>(src + j * slot_stride));
+#pragma unroll
+                            for (int j = 0; j < kPMaxS; ++j)   // k-range order
+                                if (j < args.s1) {
+                                    v.x += w[j].x;
+                                    v.y += w[j].y;
+                                    v.z += w[j].z;
+                                    v.w += w[j].w;
+                                }
+                            uint2 o;
+                            o.x = pack_bf16(bf16_lo(g.x) * v.x, bf16_hi(g.x) * v.y);
+                            o.y = pack_bf16(bf16_lo(g.y) * v.z, bf16_hi(g.y) * v.w);
+                            *reinterpret_cast<uint2*>(args.cq + (size_t)r * args.hcq + col) = o;
                         }
+                        float s2 = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                        s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+                        s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+                        if (f4 == 0 && r < T) args.ss[(size_t)(col0 / kPChunk) * T + r] = s2;
                     }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int r = r0 + 8 * k + rsub;
-                        float s2 = 0.f;
-                        if (r < T) {
-#pragma unroll
-                            for (int j = 0; j < 3; ++j) {
-                                const int col = tile * kPTile + (c4 + j) * 4;
-                                const uint2 g = *reinterpret_cast<const uint2*>(args.gamma_cq + col);
-                                const float4 w = v[k][j];
-                                s2 += w.x * w.x + w.y * w.y + w.z * w.z + w.w * w.w;
-                                uint2 o;
-                                o.x = pack_bf16(bf16_lo(g.x) * w.x, bf16_hi(g.x) * w.y);
-                                o.y = pack_bf16(bf16_lo(g.y) * w.z, bf16_hi(g.y) * w.w);
-                                *reinterpret_cast<uint2*>(args.cq + (size_t)r * args.hcq + col) = o;
-                            }
-                        }
-#pragma unroll
-                        for (int o = 8; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-                        if ((etid & 15) == 0 && r < T) args.ss[(size_t)tile * T + r] = s2;
-                    }
+                    epi_bar();
+                    if (etid == 0)
+                        asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(args.cqflags + col0 / kPChunk), "l"(args.tag)
+                                     : "memory");
                 }
-                epi_bar();
-                if (etid == 0)
-                    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(args.cqflags + tile), "l"(args.tag) : "memory");
             }
         }
         if (!ok) fail();
         ok = !epi_any(!ok);   // uniform over the 128 threads: the waits below are collective
 
         if (ok && head) {
-            // Every c^Q tile is written ...
-            ok = wait_tiles(args.cqflags, nullptr, 0, ncq, 0u, args.tag, s_abort, etid);
+            // Every c^Q chunk is written ...
+            ok = wait_tiles(args.cqflags, nullptr, 0, args.hcq / kPChunk, 0u, args.tag, s_abort, etid);
             // ... then P3's activation tiles come by TMA (warp 2) ...
             if (etid == 0) mbar_arrive(smem_u32(cq_ready));
-            // ... and each row's 1 / RMS from the tiles' sums of y^2 (in tile order).
+            // ... and each row's 1 / RMS from the chunks' sums of y^2 (in chunk order).
             float inv = 0.f;
             if (ok && row < T) {
                 float s2 = 0.f;
-                for (int t = 0; t < ncq; ++t) s2 += __ldcg(args.ss + (size_t)t * T + row);
+                for (int c = 0; c < args.hcq / kPChunk; ++c) s2 += __ldcg(args.ss + (size_t)c * T + row);
                 inv = 1.f / sqrtf(s2 / (float)args.hcq + args.eps_cq);
             }
             // ---- P3 epilogue: 1 / RMS per token, RoPE -> queryRopeOut, q^C -> P4's A operand
@@ -681,9 +685,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         if (etid == 0) atomicOr(args.status, kStatusCacheIndexRange);
                         continue;
                     }
+                    // y of this token's c^KV | k^R columns: the k-range slots added in order
                     const float* yr = args.y + (size_t)t * args.ncols1 + args.hcq;
+                    const size_t slot_stride = (size_t)T * args.ncols1;
+                    float4 v = __ldcg(reinterpret_cast<const float4*>(yr) + etid);
+                    float kr0 = 0.f, kr1 = 0.f;
+                    if (etid < h) {
+                        kr0 = __ldcg(yr + args.hckv + etid);
+                        kr1 = __ldcg(yr + args.hckv + etid + h);
+                    }
+                    for (int j = 1; j < args.s1; ++j) {
+                        const float* yj = yr + j * slot_stride;
+                        const float4 w = __ldcg(reinterpret_cast<const float4*>(yj) + etid);
+                        v.x += w.x;
+                        v.y += w.y;
+                        v.z += w.z;
+                        v.w += w.w;
+                        if (etid < h) {
+                            kr0 += __ldcg(yj + args.hckv + etid);
+                            kr1 += __ldcg(yj + args.hckv + etid + h);
+                        }
+                    }
                     // RmsNorm of c^KV: four of the Hckv = 512 values per thread
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(yr) + etid);
                     float s2 = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
@@ -697,11 +720,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     *reinterpret_cast<uint2*>(args.kv_cache + slot * args.hckv + 4 * etid) = o;
                     // RoPE of k^R
                     if (etid < h) {
-                        const float* kr = yr + args.hckv;
                         const __nv_bfloat16* cs = args.rope_cos + (size_t)t * args.dr;
                         const __nv_bfloat16* sn = args.rope_sin + (size_t)t * args.dr;
                         __nv_bfloat16* dkr = args.kr_cache + slot * args.dr;
-                        const float x0 = __ldcg(kr + etid), x1 = __ldcg(kr + etid + h);
+                        const float x0 = kr0, x1 = kr1;
                         dkr[etid] = __float2bfloat16_rn(x0 * __bfloat162float(cs[etid]) - x1 * __bfloat162float(sn[etid]));
                         dkr[etid + h] =
                             __float2bfloat16_rn(x1 * __bfloat162float(cs[etid + h]) + x0 * __bfloat162float(sn[etid + h]));

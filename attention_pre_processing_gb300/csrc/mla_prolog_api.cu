@@ -342,7 +342,8 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
         if (s1 > kPMaxS) s1 = kPMaxS;
         if (!sc.x_i8 && !sc.uqqr_i8 && !sc.kv_i8 && !sc.kr_i8 && !sc.q_i8 && T >= 1 && T <= kPMaxT &&
             d.D == 128 && d.Dr == 64 && d.Hckv == 512 && d.Hcq % 384 == 0 && d.He % 64 == 0 && ncols1 % 192 == 0 &&
-            d.N >= 1 && d.N <= sms && s1 >= 1 && wst >= 6) {   // P4 staging needs its six stages in distinct slots
+            d.Hcq / kPChunk <= 128 && d.N >= 1 && d.N <= sms && s1 >= 1 &&
+            wst >= 6) {   // P4 staging needs its six stages in distinct slots
             p.persist = true;
             p.p_n1 = n1;
             p.p_s1 = s1;
@@ -361,10 +362,12 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     p.off_cq = take((size_t)T * d.Hcq * 2);
     p.off_cqs = take((size_t)T * 4);
     p.off_qc = take((size_t)T * d.N * d.D * 2);
-    p.off_y1 = take((size_t)(p.g1.ksplit > 1 ? p.g1.ksplit : 1) * T * p.ncols1 * 4);
+    int y1_slots = p.g1.ksplit > 1 ? p.g1.ksplit : 1;
+    if (p.persist && p.p_s1 > y1_slots) y1_slots = p.p_s1;
+    p.off_y1 = take((size_t)y1_slots * T * p.ncols1 * 4);
     if (p.fold_cq) p.off_ss = take((size_t)T * kFoldSums * 4);
-    // per P1 tile: a flag and a counter; per c^Q tile: a flag and T sums of squares
-    if (p.persist) p.off_pbar = take((size_t)p.p_n1 * (8 + 4) + 8 + (size_t)(d.Hcq / kPTile) * (8 + 4 * T));
+    // per P1 tile: a flag and a counter; per 16-column c^Q chunk: a flag and T sums of squares
+    if (p.persist) p.off_pbar = take((size_t)p.p_n1 * (8 + 4) + 8 + (size_t)(d.Hcq / kPChunk) * (8 + 4 * T));
     if (!p.g2_fused) p.off_y2 = take((size_t)T * p.ncols2 * 4);
     if (sc.x_i8) {
         p.off_xb = take((size_t)T * d.He * 2);
@@ -774,7 +777,7 @@ mla_status run(const Launched& L) {
         pa.zflags = reinterpret_cast<unsigned long long*>(ws + p.off_pbar);
         pa.cnt = reinterpret_cast<unsigned int*>(ws + p.off_pbar + (size_t)p.p_n1 * 8);
         pa.cqflags = reinterpret_cast<unsigned long long*>(ws + p.off_pbar + (((size_t)p.p_n1 * 12 + 7) & ~(size_t)7));
-        pa.ss = reinterpret_cast<float*>(pa.cqflags + d.Hcq / kPTile);
+        pa.ss = reinterpret_cast<float*>(pa.cqflags + d.Hcq / kPChunk);
         pa.cq = f1.c_q;
         pa.gamma_cq = f1.gamma_cq;
         pa.gamma_ckv = f1.gamma_ckv;

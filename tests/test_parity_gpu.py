@@ -214,46 +214,23 @@ def test_partial_quant_int8_caches():
     case("tiny", uqqr_int8=True, kv_int8=True, kr_int8=True, ckv_reciprocal=True).check_all()
 
 
-def test_determinism_bit_identical():
-    """The kernel-per-step paths add the down-projection's k-range products in fixed order, so
-    repeated calls are bit-identical (T=100 takes the split-K decode path)."""
-    cfg = workloads.config("decode_t32", T=100)
+@pytest.mark.parametrize("T", [48, 100])
+def test_determinism_bit_identical(T):
+    """Every sum is taken in a fixed order (the operation is deterministic by default), so
+    repeated calls are bit-identical: T=48 runs the persistent decode kernel (twenty calls, so
+    that a race in its cross-CTA hand-offs would show), T=100 the split-K decode path."""
+    cfg = workloads.config("decode_t32", T=T)
     inp = workloads.make_inputs(cfg)
     PrologCall = _runner()
     a = PrologCall(cfg, inp)
     b = PrologCall(cfg, inp)
     a()
-    b()
-    a()
-    torch.cuda.synchronize()
-    for k in ("q_out", "q_rope_out", "kv_cache", "kr_cache"):
-        assert torch.equal(_bits(a.t[k]), _bits(b.t[k])), k
-
-
-def test_persistent_decode_repeatable():
-    """The persistent decode kernel adds the k-range products with fp32 atomics in arrival
-    order: repeated calls agree within the parity tolerance, write the same cache rows, and
-    leave every other row bit-identical."""
-    cfg = workloads.config("decode_t32", T=48)
-    inp = workloads.make_inputs(cfg)
-    PrologCall = _runner()
-    a = PrologCall(cfg, inp)
-    b = PrologCall(cfg, inp)
-    a()
-    for _ in range(20):   # many calls on b: a race in the cross-CTA hand-offs would show
+    for _ in range(20):
         b()
     torch.cuda.synchronize()
     assert a.status() == 0 and b.status() == 0
-    for k in ("q_out", "q_rope_out"):
-        assert_bf16_close(bf16_to_f64(a.t[k]), bf16_to_f64(b.t[k]), k)
-    s = cfg.shape
-    idx = inp["cache_index"].cuda()
-    for k, w in (("kv_cache", s.Hckv), ("kr_cache", s.Dr)):
-        ra, rb = a.t[k].reshape(-1, w), b.t[k].reshape(-1, w)
-        assert_bf16_close(bf16_to_f64(ra[idx]), bf16_to_f64(rb[idx]), k)
-        keep = torch.ones(ra.shape[0], dtype=torch.bool, device=ra.device)
-        keep[idx] = False
-        assert torch.equal(_bits(ra[keep]), _bits(rb[keep])), f"{k}: rows outside cacheIndex differ"
+    for k in ("q_out", "q_rope_out", "kv_cache", "kr_cache"):
+        assert torch.equal(_bits(a.t[k]), _bits(b.t[k])), k
 
 
 def test_empty_tokens_is_a_no_op():
