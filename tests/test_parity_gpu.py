@@ -166,6 +166,28 @@ def test_prefill_t8192_bf16():
     case("prefill_t8192", sample=40).check_all()
 
 
+# ------------------------------------------------------------- shape space
+# The pages fix Hcq = 1536, Hckv = 512, D = 128, Dr = 64 and let He take nine values, N seven
+# powers of two and BlockSize multiples of 16 from 16 to 1024 (aclnnMlaPrologV2WeightNz, shape
+# format fields).  A few tokens of each combination against the oracle, on the persistent
+# decode kernel (T <= 64), the split-K decode path (T <= 256) and the prefill path (T > 256).
+
+@pytest.mark.parametrize("He", [1024, 3072, 7680, 8192])
+@pytest.mark.parametrize("N", [1, 16, 128])
+def test_shape_space_decode(He, N):
+    case("decode_t32", T=5, He=He, N=N, block_num=8, block_size=16).check_all()
+
+
+@pytest.mark.parametrize("He,N,T", [(2048, 8, 100), (5120, 64, 130)])
+def test_shape_space_split_k(He, N, T):
+    case("decode_t32", sample=16, T=T, He=He, N=N, block_num=4, block_size=1024).check_all()
+
+
+@pytest.mark.parametrize("He,N", [(1024, 4), (6144, 32), (8192, 2)])
+def test_shape_space_prefill(He, N):
+    case("decode_t32", sample=16, T=300, He=He, N=N, block_num=3, block_size=112).check_all()
+
+
 # --------------------------------------------------------------- edge cases
 
 @pytest.mark.parametrize("T", [1, 37, 64, 65, 129, 200])
