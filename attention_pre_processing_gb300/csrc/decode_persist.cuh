@@ -120,46 +120,59 @@ __device__ __forceinline__ bool p_step(const PersistArgs& a, int i, int n1s, PSt
 
 // ------------------------------------------------------------------ dependency flags
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
 __device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int* p) {
     unsigned int v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Polls (bounded) until every lane's entries t0 + lane + 32 k (< t1) satisfy `ready`: one
+// round issues all four relaxed loads before it looks at any, so a round costs one trip to
+// L2, not four; a short sleep between rounds keeps the lines from being hammered.
+template <typename T, typename Ready>
+__device__ __forceinline__ bool poll_lanes(const T* base, int t0, int t1, Ready ready, uint64_t start,
+                                           const volatile int* abort) {
+    const int lane = threadIdx.x & 31;
+    while (true) {
+        T v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int t = t0 + lane + 32 * k;
+            if constexpr (sizeof(T) == 8) v[k] = t < t1 ? ld_relaxed_u64(base + t) : T(0);
+            else v[k] = t < t1 ? ld_relaxed_u32(base + t) : T(0);
+        }
+        bool all = true;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) all &= t0 + lane + 32 * k >= t1 || ready(v[k]);
+        if (__all_sync(0xffffffffu, all)) return true;
+        if (*abort || global_timer_ns() - start > kWaitLimitNs) return false;
+        __nanosleep(64);
+    }
+}
+
 // Waits (bounded) until tiles t0 .. t1 - 1 are ready: the tile's flag holds `tag` and, if
-// `need` > 0, its counter holds `need` (every k range stored; at most 32 tiles then, else 128).
-// Called by all 128 epilogue threads together.  One warp polls, lane l the tiles t0 + l + 32 k:
-// the flag is read with acquire semantics first, so the counter read after it is this call's;
-// a short sleep between rounds keeps the lines from being hammered.  The named barrier releases
-// the other warps, and every thread then takes an acquire fence.
+// `need` > 0, its counter holds `need` (every k range stored; at most 128 tiles).  Called by
+// all 128 epilogue threads together; one warp polls.  Flags first, then an acquire fence, so
+// the counters read after it are this call's (the flag says the counter was reset); then the
+// counters.  The named barrier releases the other warps, and every thread then takes an
+// acquire fence for what the flags and counters published (a relaxed read that saw a release
+// write, followed by a fence, synchronises with it).
 __device__ __forceinline__ bool wait_tiles(const unsigned long long* zf, const unsigned int* cnt, int t0, int t1,
                                            unsigned int need, unsigned long long tag, const volatile int* abort,
                                            int etid) {
     bool ok = true;
     if (etid < 32) {
         const uint64_t start = global_timer_ns();
-        bool mine[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mine[k] = t0 + etid + 32 * k >= t1;
-        while (true) {
-            bool all = true;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int t = t0 + etid + 32 * k;
-                if (!mine[k]) mine[k] = ld_acquire_u64(zf + t) == tag && (need == 0 || ld_relaxed_u32(cnt + t) == need);
-                all &= mine[k];
-            }
-            if (__all_sync(0xffffffffu, all)) break;
-            if (*abort || global_timer_ns() - start > kWaitLimitNs) {
-                ok = false;
-                break;
-            }
-            __nanosleep(64);
+        ok = poll_lanes(zf, t0, t1, [tag](unsigned long long v) { return v == tag; }, start, abort);
+        if (ok && need > 0) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            ok = poll_lanes(cnt, t0, t1, [need](unsigned int v) { return v == need; }, start, abort);
         }
     }
     const bool bad = epi_any(!ok);
