@@ -24,7 +24,8 @@ from typing import Dict, Optional
 
 import torch
 
-__all__ = ["MlaShape", "MlaConfig", "CONFIGS", "config", "make_inputs", "sample_tokens"]
+__all__ = ["MlaShape", "MlaConfig", "CONFIGS", "config", "make_inputs", "sample_tokens",
+           "PpShape", "PpConfig", "PP_CONFIGS", "pp_config", "make_pp_inputs"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -275,3 +276,135 @@ def nbytes(t: Optional[torch.Tensor]) -> int:
 def flops_per_token(s: MlaShape) -> int:
     """Multiply-adds x 2 of the three contractions, per token."""
     return 2 * (s.He * (s.Hcq + s.Hckv + s.Dr) + s.Hcq * s.N * (s.D + s.Dr) + s.N * s.D * s.Hckv)
+
+
+# ------------------------------------------------------------------ the aclnnMlaPreprocess variant
+#
+# Shapes follow "aclnnMlaPreprocess" (aclnnMlaPreprocessGetWorkspaceSize: parameter table;
+# Constraints: shape fields): input (T, He); wdqkv int8 (Hcq + 576, He), one row per output
+# column ("transposeWdq" true); wuq int8 (N * (D + 64), Hcq); wuk (N, D, 512); cos/sin (T, 64);
+# slotMapping int32 (T); cacheMode 0: kvCache (blockNum, blockSize, 1, 576); cacheMode 1:
+# kvCache (..., 512) and kvCacheRope (..., 64).  The page fixes keyTotalDim = 512 + 64 and
+# qRopeDim = 64; tokenNum <= 256, blockNum 192 and blockSize 128 in its constraints.
+
+
+@dataclasses.dataclass(frozen=True)
+class PpShape:
+    T: int
+    He: int
+    Hcq: int
+    N: int
+    D: int            # qNoRopeDim
+    block_num: int
+    block_size: int
+    Hckv: int = 512   # keyTotalDim = Hckv + Dr
+    Dr: int = 64      # qRopeDim = kRopeDim
+
+
+@dataclasses.dataclass(frozen=True)
+class PpConfig:
+    """One synthetic workload of the aclnnMlaPreprocess variant."""
+    name: str
+    shape: PpShape
+    seed: int
+    dtype: str = "bf16"        # "bf16" or "fp16": input, gammas, betas, scales, cos/sin, wuk, caches, outputs
+    cache_mode: int = 0        # 0: concatenated 576-wide cache rows and q rows; 1: split
+    do_rmsnorm: bool = True    # False: the input is only quantised
+    eps: float = 1e-6
+    with_bias: bool = True     # bias0 / bias1 passed (int32)
+    pos_hi: int = 32768
+    theta: float = 1e4
+
+    @property
+    def workload(self) -> str:
+        s = self.shape
+        return (f"{self.name}: T={s.T} He={s.He} Hcq={s.Hcq} N={s.N} D={s.D} Dr={s.Dr} Hckv={s.Hckv} "
+                f"cache={s.block_num}x{s.block_size} [int8 wdqkv/wuq, {self.dtype}, cacheMode {self.cache_mode}]")
+
+
+PP_CONFIGS: Dict[str, PpConfig] = {
+    "pp_tiny": PpConfig(name="pp_tiny", shape=PpShape(T=8, He=256, Hcq=64, N=4, D=32, block_num=4, block_size=16),
+                        seed=2000),
+    # DeepSeek-V3 shapes at the page's fixed blockNum 192 and blockSize 128
+    "pp_decode_t32": PpConfig(name="pp_decode_t32",
+                              shape=PpShape(T=32, He=7168, Hcq=1536, N=128, D=128, block_num=192, block_size=128),
+                              seed=2001),
+    "pp_decode_t32_fp16": PpConfig(name="pp_decode_t32_fp16",
+                                   shape=PpShape(T=32, He=7168, Hcq=1536, N=128, D=128, block_num=192,
+                                                 block_size=128),
+                                   seed=2002, dtype="fp16"),
+    # the page's largest tokenNum
+    "pp_t256": PpConfig(name="pp_t256",
+                        shape=PpShape(T=256, He=7168, Hcq=1536, N=128, D=128, block_num=192, block_size=128),
+                        seed=2003, cache_mode=1),
+}
+
+
+def pp_config(name: str, **overrides) -> PpConfig:
+    """Return a named aclnnMlaPreprocess config, optionally with shape or other fields replaced."""
+    cfg = PP_CONFIGS[name]
+    shape_keys = {f.name for f in dataclasses.fields(PpShape)}
+    shape_over = {k: v for k, v in overrides.items() if k in shape_keys}
+    other = {k: v for k, v in overrides.items() if k not in shape_keys}
+    if shape_over:
+        other["shape"] = dataclasses.replace(cfg.shape, **shape_over)
+    return dataclasses.replace(cfg, **other) if other else cfg
+
+
+def make_pp_inputs(cfg: PpConfig, seed: Optional[int] = None) -> Dict[str, Optional[torch.Tensor]]:
+    """Draw every input of one aclnnMlaPreprocess call on the CPU, in a fixed order, from one seed.
+
+    The scale ranges keep the int8 codes of both quantisers mostly inside [-128, 127] (a few
+    saturate) and the dequantised products of order one: deScale ~ U(0.5, 1.5) / (sqrt(K) * 25 * 73),
+    25 and 73 being the rough rms of the codes and of uniform int8 weights.
+    """
+    s = cfg.shape
+    gen = torch.Generator().manual_seed(cfg.seed if seed is None else seed)
+    T, He, Hcq, N, D, Dr, Hckv = s.T, s.He, s.Hcq, s.N, s.D, s.Dr, s.Hckv
+    fdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float16
+    n1, n2 = Hcq + Hckv + Dr, N * (D + Dr)
+    out: Dict[str, Optional[torch.Tensor]] = {}
+    out["input"] = torch.randn((T, He), generator=gen, dtype=torch.float32).to(fdt)
+    out["gamma0"] = _uniform(gen, (He,), 0.8, 1.2).to(fdt)
+    out["beta0"] = _uniform(gen, (He,), -0.1, 0.1).to(fdt)
+    out["quant_scale0"] = _uniform(gen, (1,), 20.0, 30.0).to(fdt)
+    out["quant_offset0"] = torch.randint(-4, 5, (1,), generator=gen, dtype=torch.int16).to(torch.int8)
+    out["wdqkv"] = _randint8(gen, (n1, He))
+    out["de_scale0"] = (_uniform(gen, (n1,), 0.5, 1.5) / (He ** 0.5 * 25 * 73)).to(torch.float32)
+    b0 = torch.randint(-50000, 50001, (n1,), generator=gen, dtype=torch.int32)
+    out["gamma1"] = _uniform(gen, (Hcq,), 0.8, 1.2).to(fdt)
+    out["beta1"] = _uniform(gen, (Hcq,), -0.1, 0.1).to(fdt)
+    out["quant_scale1"] = _uniform(gen, (1,), 20.0, 30.0).to(fdt)
+    out["quant_offset1"] = torch.randint(-4, 5, (1,), generator=gen, dtype=torch.int16).to(torch.int8)
+    out["wuq"] = _randint8(gen, (n2, Hcq))
+    out["de_scale1"] = (_uniform(gen, (n2,), 0.5, 1.5) / (Hcq ** 0.5 * 25 * 73)).to(torch.float32)
+    b1 = torch.randint(-20000, 20001, (n2,), generator=gen, dtype=torch.int32)
+    out["bias0"] = b0 if cfg.with_bias else None
+    out["bias1"] = b1 if cfg.with_bias else None
+    out["gamma2"] = _uniform(gen, (Hckv,), 0.8, 1.2).to(fdt)
+    pos = torch.randint(0, cfg.pos_hi, (T,), generator=gen, dtype=torch.int64)
+    out["positions"] = pos
+    h = Dr // 2
+    inv = cfg.theta ** (-2.0 * torch.arange(h, dtype=torch.float64) / Dr)
+    ang = pos.to(torch.float64)[:, None] * inv[None, :]
+    out["cos"] = torch.cat([torch.cos(ang), torch.cos(ang)], dim=1).to(fdt).contiguous()
+    out["sin"] = torch.cat([torch.sin(ang), torch.sin(ang)], dim=1).to(fdt).contiguous()
+    out["wuk"] = (torch.randn((N, D, Hckv), generator=gen, dtype=torch.float32) * 0.02).to(fdt)
+    nslots = s.block_num * s.block_size
+    if nslots == 0:
+        slots = torch.zeros(T, dtype=torch.int32)
+    else:
+        assert T <= nslots
+        slots = torch.randperm(nslots, generator=gen)[:T].to(torch.int32)
+    out["slot_mapping"] = slots.contiguous()
+
+    def bits(shape):
+        return torch.randint(-32768, 32768, shape, generator=gen, dtype=torch.int16).view(fdt)
+
+    if cfg.cache_mode == 0:
+        out["kv_cache"] = bits((s.block_num, s.block_size, 1, Hckv + Dr))
+        out["kv_cache_rope"] = None
+    else:
+        out["kv_cache"] = bits((s.block_num, s.block_size, 1, Hckv))
+        out["kv_cache_rope"] = bits((s.block_num, s.block_size, 1, Dr))
+    return out
