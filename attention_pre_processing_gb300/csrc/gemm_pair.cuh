@@ -159,9 +159,11 @@ __global__ void __launch_bounds__(gemm_threads(EPW), 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            // The first ring of weight tiles goes out before the grid dependency resolves.
+            // The first ring of weight tiles goes out before the grid dependency resolves (unless
+            // an earlier kernel of the call writes them).
             int pre = 0;
             Unit u0;
+            if (args.b_late) pdl_wait();   // the weights come from an earlier kernel of the call
             if (get_pair_unit(args, 0, u0)) {
                 pre = nst < stages ? nst : stages;
                 for (int i = 0; i < pre; ++i) {

@@ -23,6 +23,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -54,6 +55,8 @@ struct GemmArgs {
     int clear_status;    // block 0 zeroes *status once earlier grids have finished
     int a_ready;         // A is a caller input (not written by an earlier kernel of the call):
                          // its tiles may be requested before the grid dependency resolves
+    int b_late;          // B is written by an earlier kernel of the call (a widened int8 weight):
+                         // no weight tile is requested before the grid dependency resolves
     int a_box_rows;      // rows of one A TMA box (multiple of 8, <= 128)
     int stages;          // ring depth actually used (<= MAXST)
     // EPI_F32: ksplit slots of T x ncols row-major fp32
@@ -68,7 +71,9 @@ struct GemmArgs {
     const float* col_scale;        // optional (ncols): per-column dequant
     // EPI_QN
     int Hckv;
-    __nv_bfloat16* q_out_bf16;     // (T, N, Hckv)
+    __nv_bfloat16* q_out_bf16;     // (T, N, q_ld), the first Hckv of each q_ld written (16-bit output)
+    int q_ld;                      // elements from one head's row to the next (0: Hckv)
+    int f16;                       // A, B and the 16-bit output are fp16 instead of bf16
     int8_t* q_out_i8;              // (T, N, Hckv)
     float* q_scale;                // (T, N)
     int tma_out;                   // store the output through shared memory with TMA (map_o, map_o2)
@@ -228,6 +233,31 @@ __device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16* dst, const float
     }
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 32 values -> fp16 (round to nearest even), as store_bf16_chunk.
+__device__ __forceinline__ void store_f16_chunk(__nv_bfloat16* dst_bits, const float (&v)[32], int nvalid) {
+    __half* dst = reinterpret_cast<__half*>(dst_bits);
+    if (nvalid >= 32 && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_f16(v[8 * i + 0], v[8 * i + 1]);
+            w.y = pack_f16(v[8 * i + 2], v[8 * i + 3]);
+            w.z = pack_f16(v[8 * i + 4], v[8 * i + 5]);
+            w.w = pack_f16(v[8 * i + 6], v[8 * i + 7]);
+            reinterpret_cast<uint4*>(dst)[i] = w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nvalid) dst[i] = __float2half_rn(v[i]);
+    }
+}
+
 __device__ __forceinline__ void store_f32_chunk(float* dst, const float (&v)[32], int nvalid) {
     if (nvalid >= 32 && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
 #pragma unroll
@@ -322,7 +352,7 @@ __device__ __forceinline__ void epilogue_qn(const GemmArgs& a, const Unit& u, co
     const int c0 = (u.n_tile % a.tiles_per_head) * BN;
     const int row = u.m_tile * 128 + row_in;
     const bool valid = row < a.T;
-    const size_t rowoff = ((size_t)row * a.N + head) * a.Hckv;
+    const size_t rowoff = ((size_t)row * a.N + head) * (a.q_ld > 0 ? a.q_ld : a.Hckv);
     if (a.q_out_i8 == nullptr) {
 #pragma unroll 1
         for (int ch = 0; ch < BN / 32; ++ch) {
@@ -330,7 +360,12 @@ __device__ __forceinline__ void epilogue_qn(const GemmArgs& a, const Unit& u, co
             if (col >= a.Hckv) break;   // uniform across the warp
             float v[32];
             src.load(0, BN, ch * 32, v);
-            if (valid) store_bf16_chunk(a.q_out_bf16 + rowoff + col, v, a.Hckv - col);
+            if (valid) {
+                if (a.f16)
+                    store_f16_chunk(a.q_out_bf16 + rowoff + col, v, a.Hckv - col);
+                else
+                    store_bf16_chunk(a.q_out_bf16 + rowoff + col, v, a.Hckv - col);
+            }
         }
         return;
     }
@@ -639,12 +674,22 @@ __device__ __forceinline__ void epilogue_qn_tma(const GemmArgs& a, const Unit& u
             uint32_t w[32];
             float v[32];
             src.load(0, BN, 64 * j, v);
+            if (a.f16) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+                for (int i = 0; i < 16; ++i) w[i] = pack_f16(v[2 * i], v[2 * i + 1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+            }
             src.load(0, BN, 64 * j + 32, v);
+            if (a.f16) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-            out.put(w, head * a.Hckv + col, row0);
+                for (int i = 0; i < 16; ++i) w[16 + i] = pack_f16(v[2 * i], v[2 * i + 1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+            }
+            out.put(w, head * (a.q_ld > 0 ? a.q_ld : a.Hckv) + col, row0);
         }
         return;
     }
@@ -680,7 +725,7 @@ __device__ __forceinline__ void epilogue_qn_tma(const GemmArgs& a, const Unit& u
                 w[8 * h + i] = packed;
             }
         }
-        out.put(w, head * a.Hckv + c0 + col, row0);
+        out.put(w, head * (a.q_ld > 0 ? a.q_ld : a.Hckv) + c0 + col, row0);
     }
     if (row < a.T) a.q_scale[(size_t)row * a.N + head] = scale;
 }
@@ -826,6 +871,7 @@ __global__ void __launch_bounds__(gemm_threads(EPW), 1)
                 for (int k = 0; k < KPS; ++k)
                     load_a<MSUB>(args, uu, kb + k, dst + k * MSUB * a_box, a_box, fb, &map_a, pol_a);
             };
+            if (args.b_late) pdl_wait();   // the weights come from an earlier kernel of the call
             if (have0) {
                 const int n0 = (u0.kb1 - u0.kb0) / KPS;
                 pre = n0 < stages ? n0 : stages;
@@ -870,7 +916,8 @@ __global__ void __launch_bounds__(gemm_threads(EPW), 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, C::kMmaN, false, true);
+            const uint32_t idesc = args.f16 ? idesc_f16_f32(128, C::kMmaN, false, true)
+                                            : idesc_bf16_f32(128, C::kMmaN, false, true);
             const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
             const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), 64 * kBK * 2 * KPS, 1024);
             int s = 0;

@@ -24,6 +24,7 @@
 #include "finalize.cuh"
 #include "gemm_tc.cuh"
 #include "gemm_pair.cuh"
+#include "preprocess.cuh"
 
 using namespace mla;
 
@@ -842,6 +843,7 @@ mla_status run(const Launched& L) {
     g1.b_split_col = (int)d.Hcq;
     g1.clear_status = 1;
     g1.a_ready = sc.x_i8 ? 0 : 1;   // bf16 tokenX is read as passed; int8 is widened first
+    g1.b_late = sc.x_i8 ? 1 : 0;    // so are int8 weights
     g1.a_one_box = big1 ? 1 : 0;
     g1.b_blocks = big1 ? 1 : 0;
     CUtensorMap mO1;
@@ -927,6 +929,7 @@ mla_status run(const Launched& L) {
         return MLA_ERR_RUNTIME;
     }
     GemmArgs g2 = gemm_args(p.g2, T, p.ncols2, status);
+    g2.b_late = sc.uqqr_i8 ? 1 : 0;   // a widened int8 W^UqQr is written by this call
     g2.a_one_box = p.g2_wide ? 1 : 0;
     g2.b_blocks = p.g2_wide ? 1 : 0;
     CUtensorMap mO2c, mO2r;
@@ -1205,3 +1208,7 @@ extern "C" const char* mla_prolog_status_string(mla_status status) {
     }
     return "unknown mla_status";
 }
+
+// ====================================================================== aclnnMlaPreprocess variant
+
+#include "preprocess_api.cuh"

@@ -274,6 +274,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// The same for fp16 A and B (format code 0 in both operand fields).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4)                       // D format: f32
+           | ((a_mn ? 1u : 0u) << 15)      // A major
+           | ((b_mn ? 1u : 0u) << 16)      // B major
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
 //   lbo: byte distance between swizzle atoms along the leading (MN for MN-major) dimension,
 //   sbo: byte distance between 8-row groups along the strided dimension.

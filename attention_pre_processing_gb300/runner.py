@@ -8,8 +8,9 @@ from typing import Dict, Optional
 
 import torch
 
-from . import _marshal, lib, MlaError, mla_prolog_device_status, mla_prolog_workspace_size
-from .workloads import MlaConfig
+from . import _marshal, _pp_marshal, lib, MlaError, mla_prolog_device_status, mla_prolog_workspace_size
+from . import mla_preprocess_workspace_size
+from .workloads import MlaConfig, PpConfig
 
 INPUT_KEYS = ("x", "w_dq", "w_uqqr", "w_uk", "w_dkvkr", "gamma_cq", "gamma_ckv", "rope_sin", "rope_cos",
               "cache_index", "kv_cache", "kr_cache", "dequant_scale_x", "dequant_scale_w_dq",
@@ -52,3 +53,44 @@ class PrologCall:
 
     def outputs(self) -> Dict[str, Optional[torch.Tensor]]:
         return {k: self.t[k] for k in ("q_out", "q_rope_out", "dequant_scale_q_nope_out", "kv_cache", "kr_cache")}
+
+
+PP_INPUT_KEYS = ("input", "gamma0", "beta0", "quant_scale0", "quant_offset0", "wdqkv", "de_scale0", "bias0",
+                 "gamma1", "beta1", "quant_scale1", "quant_offset1", "wuq", "de_scale1", "bias1", "gamma2",
+                 "cos", "sin", "wuk", "kv_cache", "kv_cache_rope", "slot_mapping")
+
+
+class PreprocessCall:
+    """One configured call of the aclnnMlaPreprocess variant, reusable across launches."""
+
+    def __init__(self, cfg: PpConfig, inputs: Dict[str, Optional[torch.Tensor]], device="cuda"):
+        s = cfg.shape
+        self.cfg = cfg
+        self.t: Dict[str, Optional[torch.Tensor]] = {}
+        for k in PP_INPUT_KEYS:
+            v = inputs.get(k)
+            self.t[k] = None if v is None else v.to(device).contiguous()
+        fdt = self.t["input"].dtype
+        qw = s.Hckv + s.Dr if cfg.cache_mode == 0 else s.Hckv
+        self.t["q_out"] = torch.empty((s.T, s.N, qw), dtype=fdt, device=device)
+        self.t["q_rope_out"] = (torch.empty((s.T, s.N, s.Dr), dtype=fdt, device=device)
+                                if cfg.cache_mode == 1 else None)
+        self._scal = dict(epsilon=cfg.eps, cache_mode=cfg.cache_mode, do_rmsnorm=cfg.do_rmsnorm, wdq_dim=None,
+                          q_rope_dim=64, k_rope_dim=64, q_rotary_coeff=2, k_rotary_coeff=2, transpose_wdq=True,
+                          transpose_wuq=True, transpose_wuk=True, quant_mode=0, wdkv_split_count=1)
+        self.ws_bytes = mla_preprocess_workspace_size(self.t, **self._scal)
+        self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        args, self._keep = _pp_marshal(self.t, **self._scal)
+        self._args = tuple(args) + (ctypes.c_void_p(self.workspace.data_ptr()), ctypes.c_uint64(self.ws_bytes))
+        self._fn = lib().mla_preprocess
+
+    def __call__(self, stream=None) -> None:
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        h = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+        rc = self._fn(*self._args, ctypes.c_void_p(h))
+        if rc != 0:
+            raise MlaError(rc, "mla_preprocess")
+
+    def status(self, stream=None) -> int:
+        return mla_prolog_device_status(self.workspace, self.ws_bytes, stream=stream)

@@ -67,7 +67,9 @@ typedef enum {
     MLA_DT_BF16 = 0,
     MLA_DT_INT8 = 1,
     MLA_DT_FP32 = 2,
-    MLA_DT_INT64 = 3
+    MLA_DT_INT64 = 3,
+    MLA_DT_FP16 = 4, /* aclnnMlaPreprocess only */
+    MLA_DT_INT32 = 5 /* aclnnMlaPreprocess only */
 } mla_dtype;
 
 /* A dense, row-major, contiguous device tensor. */

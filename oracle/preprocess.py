@@ -177,7 +177,7 @@ def preprocess(inp: Dict, *, dtype: str, cache_mode: int, do_rmsnorm: bool, eps:
 
     kv = cache_bits(inp["kv_cache"])
     nslots = kv.shape[0] * kv.shape[1]
-    kv = kv.reshape(nslots, -1)
+    kv = kv.reshape(nslots, kv.shape[-1])
     if cache_mode == 0:
         res["q_out"] = np.concatenate([q_nope, q_rope], axis=-1)
         rows = np.concatenate([k_nope, k_rope], axis=-1)
@@ -189,7 +189,8 @@ def preprocess(inp: Dict, *, dtype: str, cache_mode: int, do_rmsnorm: bool, eps:
     else:
         res["q_out"] = q_nope
         res["q_rope_out"] = q_rope
-        kr = cache_bits(inp["kv_cache_rope"]).reshape(nslots, -1)
+        kr = cache_bits(inp["kv_cache_rope"])
+        kr = kr.reshape(nslots, kr.shape[-1])
         if nslots > 0:
             assert len(set(slots.tolist())) == len(slots), "slotMapping values must be distinct"
             assert slots.min(initial=0) >= 0 and slots.max(initial=0) < nslots, "slotMapping out of range"

@@ -159,3 +159,87 @@ def test_product_has_no_cpu_fallback():
             if fn.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in text and "from oracle" not in text and "mla_oracle" not in text, fn
+
+
+# ---------------------------------------------------------- the aclnnMlaPreprocess variant
+
+F16, I32 = 4, 5
+
+
+def pp(Tk=32, dt=BF16, mode=0, **kw):
+    He, Hcq, N, D = 7168, 1536, 128, 128
+    n1, n2 = Hcq + 576, N * (D + 64)
+    kv = T(dt, 192, 128, 1, 576 if mode == 0 else 512)
+    t = dict(input=T(dt, Tk, He), gamma0=T(dt, He), beta0=T(dt, He), quant_scale0=T(dt, 1), quant_offset0=T(I8, 1),
+             wdqkv=T(I8, n1, He), de_scale0=T(F32, n1), bias0=T(I32, n1), gamma1=T(dt, Hcq), beta1=T(dt, Hcq),
+             quant_scale1=T(dt, 1), quant_offset1=T(I8, 1), wuq=T(I8, n2, Hcq), de_scale1=T(F32, n2),
+             bias1=T(I32, n2), gamma2=T(dt, 512), cos=T(dt, Tk, 64), sin=T(dt, Tk, 64), wuk=T(dt, N, D, 512),
+             kv_cache=kv, slot_mapping=T(I32, Tk), q_out=T(dt, Tk, N, 576 if mode == 0 else 512))
+    if mode == 1:
+        t.update(kv_cache_rope=T(dt, 192, 128, 1, 64), q_rope_out=T(dt, Tk, N, 64))
+    t.update(kw)
+    return t
+
+
+def pp_code(tensors, mode=0, **scal):
+    try:
+        mla.mla_preprocess_workspace_size(tensors, 1e-6, cache_mode=mode, **scal)
+        return 0
+    except mla.MlaError as e:
+        return e.code
+
+
+def test_preprocess_valid_arguments(lib):
+    assert pp_code(pp()) in (0, 361001)
+    assert pp_code(pp(dt=F16)) in (0, 361001)
+    assert pp_code(pp(mode=1), mode=1) in (0, 361001)
+    assert pp_code(pp(bias0=None, bias1=None)) in (0, 361001)           # the biases are optional
+    assert pp_code(pp(), do_rmsnorm=False) in (0, 361001)
+    assert pp_code(pp(Tk=0)) == 0                                          # empty: no device query
+
+
+def test_preprocess_nulls_and_patterns(lib):
+    assert pp_code(pp(wuq=None)) == 161001
+    assert pp_code(pp(mode=1, kv_cache_rope=None), mode=1) == 161001     # mode 1 needs the rope cache
+    assert pp_code(pp(q_rope_out=T(BF16, 32, 128, 64))) == 161002        # mode 0 has no separate q^R
+    t = pp()
+    t["kv_cache_out"] = T(BF16, 192, 128, 1, 576)                           # not the same tensor as kvCache
+    assert pp_code(t) == 161002
+    assert pp_code(pp(ctkv_scale=T(BF16, 1))) == 161002                   # cacheMode 2 only
+
+
+def test_preprocess_scalars(lib):
+    assert pp_code(pp(), mode=2) == 161002                                  # NZ cache layouts are not built
+    assert pp_code(pp(), mode=3) == 161002
+    assert pp_code(pp(), quant_mode=1) == 161002
+    assert pp_code(pp(), q_rope_dim=32) == 161002
+    assert pp_code(pp(), q_rotary_coeff=4) == 161002
+    assert pp_code(pp(), transpose_wuq=False) == 161002
+    assert pp_code(pp(), wdkv_split_count=2) == 161002
+    assert pp_code(pp(), wdq_dim=1024) == 161002
+
+
+def test_preprocess_shapes_and_dtypes(lib):
+    assert pp_code(pp(Tk=257)) == 161002                                    # tokenNum in [0, 256]
+    assert pp_code(pp(gamma0=T(F16, 7168))) == 161002                       # every F tensor in the input's dtype
+    assert pp_code(pp(wdqkv=T(BF16, 2112, 7168))) == 161002                 # int8 weights only (quantMode 0)
+    assert pp_code(pp(de_scale0=T(F32, 2111))) == 161002
+    assert pp_code(pp(slot_mapping=T(I64, 32))) == 161002                   # slotMapping is int32
+    assert pp_code(pp(bias1=T(F32, 24576))) == 161002
+    assert pp_code(pp(input=T(F32, 32, 7168))) == 161002
+    assert pp_code(pp(wuk=T(BF16, 129, 128, 512), wuq=T(I8, 129 * 192, 1536), de_scale1=T(F32, 129 * 192),
+                      bias1=T(I32, 129 * 192), q_out=T(BF16, 32, 129, 576))) == 161002   # headNum <= 128
+
+
+def test_preprocess_tiling_rules(lib):
+    Hcq = 1504                                                                # a multiple of 32, not of 64
+    t = pp(wdqkv=T(I8, Hcq + 576, 7168), de_scale0=T(F32, Hcq + 576), bias0=T(I32, Hcq + 576),
+           gamma1=T(BF16, Hcq), beta1=T(BF16, Hcq), wuq=T(I8, 128 * 192, Hcq))
+    assert pp_code(t) == 561002
+    D = 40                                                                    # not a multiple of 16
+    t = pp(wuk=T(BF16, 128, D, 512), wuq=T(I8, 128 * (D + 64), 1536), de_scale1=T(F32, 128 * (D + 64)),
+           bias1=T(I32, 128 * (D + 64)))
+    assert pp_code(t) == 561002
+    t = pp()
+    t["input"].data = t["input"].data + 2
+    assert pp_code(t) == 161002
