@@ -24,6 +24,9 @@
 namespace mla {
 
 constexpr int kPpThreads = 256;
+// The per-token row kernels (one CTA per token) run 1024 threads: at decode sizes they are
+// latency-bound, and more warps per token hide more of it.
+constexpr int kPpRowThreads = 1024;
 
 // 16-bit element <-> float for the input dtype (bf16 or fp16).
 template <bool F16>
@@ -60,20 +63,33 @@ struct Half16<true> {
 // The int8 code of the page's static asymmetric quantiser,
 //   code = clamp(round_half_away(v * qs) + qo, -128, 127),  v = (gamma * y) / r + beta  (norm)
 //                                                            v = y                     (no norm)
-// decided as in exact double arithmetic, in this operation order: the fp32 estimate decides
-// unless it lies within its error bound of a rounding boundary (a half-integer), and then the
-// double expression does.  The bound: four fp32 roundings of at most 2^-24 relative each, on
-// terms no larger than (|gamma * y / r| + |beta|) * |qs|; 1e-5 of that is a 40x margin.
-// r is sqrt(mean(y^2) + eps) in double; inv its fp32 reciprocal.
-__device__ __forceinline__ float pp_code(double y, float g, float b, bool norm, double r, float inv, float qs,
+// with r = sqrt(mean(y^2) + eps), decided as in exact double arithmetic in this operation order:
+// the fp32 estimate decides unless it lies within its error bound of a rounding boundary (a
+// half-integer), and then the double expression does.  The bound: a handful of fp32 roundings
+// of at most 2^-24 relative each, on terms no larger than (|gamma * y / r| + |beta|) * |qs|;
+// 1e-5 of that is a wide margin.  y arrives as an unevaluated float pair y = yh + yl (yl = 0
+// when y is a float), the sum of squares as the pair (sh, sl) over nfeat features; inv is the
+// fp32 estimate of 1 / r.  GB300 runs doubles at a small fraction of its float rate, so the
+// double path (r included) runs only for the rare values near a boundary.
+struct PpNorm {
+    float sh, sl;   // sum of squares, as an unevaluated float pair
+    float inv;      // fp32 estimate of 1 / r
+    int nfeat;
+    double eps;
+};
+__device__ __forceinline__ float pp_code(float yh, float yl, float g, float b, bool norm, const PpNorm& nr, float qs,
                                          int qo) {
-    const float yf = (float)y;
-    const float a = norm ? g * yf * inv : yf;
+    const float a = norm ? g * yh * nr.inv : yh;
     const float sf = (a + (norm ? b : 0.f)) * qs;
     const float margin = 1e-5f * (fabsf(a) + (norm ? fabsf(b) : 0.f)) * fabsf(qs) + 1e-30f;
     float q;
     if (fabsf(sf - floorf(sf) - 0.5f) <= margin) {
-        const double v = norm ? __dadd_rn(__ddiv_rn(__dmul_rn((double)g, y), r), (double)b) : y;
+        const double y = (double)yh + (double)yl;
+        double v = y;
+        if (norm) {
+            const double r = __dsqrt_rn(__dadd_rn(__ddiv_rn((double)nr.sh + (double)nr.sl, (double)nr.nfeat), nr.eps));
+            v = __dadd_rn(__ddiv_rn(__dmul_rn((double)g, y), r), (double)b);
+        }
         q = (float)round(__dmul_rn(v, (double)qs));   // round(): halves away from zero
     } else {
         q = roundf(sf);
@@ -81,62 +97,128 @@ __device__ __forceinline__ float pp_code(double y, float g, float b, bool norm, 
     return fminf(fmaxf(q + (float)qo, -128.f), 127.f);
 }
 
-// Deterministic double sum over the CTA (fixed shuffle tree, then the warps in order).
-__device__ __forceinline__ double pp_block_sum(double v, double* red) {
+// Error-free float transformations: s + e == a + b and p + e == a * b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+__device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
+    p = __fmul_rn(a, b);
+    e = fmaf(a, b, -p);
+}
+// (hi, lo) += v (v exact as a float pair vh + vl), keeping ~48 significant bits.
+__device__ __forceinline__ void ff_add(float& hi, float& lo, float vh, float vl) {
+    float s, e;
+    two_sum(hi, vh, s, e);
+    e = __fadd_rn(e, __fadd_rn(lo, vl));
+    hi = __fadd_rn(s, e);
+    lo = __fsub_rn(e, __fsub_rn(hi, s));
+}
+
+// Deterministic sum of float pairs over the CTA of NT threads (fixed shuffle tree, then the
+// warps in order); red holds NT / 32 + 1 pairs.
+template <int NT>
+__device__ __forceinline__ float2 pp_block_sum(float hi, float lo, float2* red) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, hi, o), ol = __shfl_xor_sync(0xffffffffu, lo, o);
+        ff_add(hi, lo, oh, ol);
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __syncthreads();
-    if (lane == 0) red[warp] = v;
+    if (lane == 0) red[warp] = make_float2(hi, lo);
     __syncthreads();
     if (warp == 0) {
-        double r = lane < kPpThreads / 32 ? red[lane] : 0.0;
+        float2 r = lane < NT / 32 ? red[lane] : make_float2(0.f, 0.f);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-        if (lane == 0) red[kPpThreads / 32] = r;
+        for (int o = 16; o > 0; o >>= 1) {
+            const float oh = __shfl_xor_sync(0xffffffffu, r.x, o), ol = __shfl_xor_sync(0xffffffffu, r.y, o);
+            ff_add(r.x, r.y, oh, ol);
+        }
+        if (lane == 0) red[NT / 32] = r;
     }
     __syncthreads();
-    return red[kPpThreads / 32];
+    return red[NT / 32];
+}
+
+// Four 16-bit values from four floats, as one 8-byte word.
+template <bool F16>
+__device__ __forceinline__ uint2 pp_pack4(float a, float b, float c, float d) {
+    if constexpr (F16)
+        return make_uint2(pack_f16(a, b), pack_f16(c, d));
+    else
+        return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
 
 // ---------------------------------------------------------------- weight widening
 
 // src: int8 (R, C), one row per output column n (R = columns, C = k).  dst0: bf16 (C, rsplit)
 // holding columns n < rsplit; dst1: bf16 (C, R - rsplit) holding the rest (may be null when
-// rsplit == R).  64 x 64 tiles through shared memory, a 1D grid of ceil(C/64) * ceil(R/64).
-// Requires C % 16 == 0, R % 8 == 0 and rsplit % 8 == 0 (16-byte loads and stores).
+// rsplit == R).  One tile of 64 rows x 256 columns per CTA and step, through shared memory:
+// the reads take 256 contiguous bytes of each row, the writes 128 contiguous bytes (64 bf16) of
+// each of the tile's 256 output rows.  A thread turns four 4-byte words of eight tile rows into
+// four 8-value output chunks.  The row pitch of 65 words makes the eight rows' words fall in
+// banks two apart.  Requires R % 8 == 0, C % 16 == 0, rsplit % 8 == 0.
+constexpr int kWtRows = 64, kWtCols = 256, kWtPitch = kWtCols + 4;   // bytes per tile row
 __global__ void __launch_bounds__(kPpThreads) pp_widen_t_kernel(const int8_t* __restrict__ src, int R, int C,
                                                                 __nv_bfloat16* __restrict__ dst0,
                                                                 __nv_bfloat16* __restrict__ dst1, int rsplit) {
-    __shared__ __align__(16) int8_t tile[64][64 + 16];
+    __shared__ __align__(16) uint32_t tile[kWtRows * kWtPitch / 4];
     pdl_launch_dependents();
     pdl_wait();
-    const int cb = (C + 63) / 64;   // one block per 64 x 64 tile, k-tile fastest
-    const int c0 = (int)(blockIdx.x % cb) * 64, r0 = (int)(blockIdx.x / cb) * 64;
     const int tid = threadIdx.x;
-    {
-        const int rr = tid >> 2, cc = (tid & 3) * 16;
-        const int r = r0 + rr, c = c0 + cc;
-        int4 v = make_int4(0, 0, 0, 0);
-        if (r < R && c < C) v = *reinterpret_cast<const int4*>(src + (size_t)r * C + c);
-        *reinterpret_cast<int4*>(&tile[rr][cc]) = v;
-    }
-    __syncthreads();
+    const int cb = (C + kWtCols - 1) / kWtCols, rb = (R + kWtRows - 1) / kWtRows;
+    for (int tt = blockIdx.x; tt < cb * rb; tt += gridDim.x) {
+        const int c0 = (tt % cb) * kWtCols, r0 = (tt / cb) * kWtRows;
+        // 64 rows x 16 chunks of 16 bytes: four per thread, all in flight together
+        int4 v[4];
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int idx = tid + it * kPpThreads;
-        const int kk = idx >> 3, nn = (idx & 7) * 8;
-        const int k = c0 + kk, n = r0 + nn;
-        if (k >= C || n >= R) continue;
-        uint32_t w[4];
+        for (int it = 0; it < 4; ++it) {
+            const int idx = tid + it * kPpThreads;
+            const int rr = idx >> 4, cc = (idx & 15) * 16;
+            const int r = r0 + rr, c = c0 + cc;
+            v[it] = (r < R && c < C) ? __ldcs(reinterpret_cast<const int4*>(src + (size_t)r * C + c))
+                                     : make_int4(0, 0, 0, 0);
+        }
+        __syncthreads();   // the previous tile's reads of shared memory are done
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16((float)tile[nn + 2 * e][kk], (float)tile[nn + 2 * e + 1][kk]);
-        const uint4 o = make_uint4(w[0], w[1], w[2], w[3]);
-        if (n < rsplit)
-            *reinterpret_cast<uint4*>(dst0 + (size_t)k * rsplit + n) = o;
-        else
-            *reinterpret_cast<uint4*>(dst1 + (size_t)k * (R - rsplit) + (n - rsplit)) = o;
+        for (int it = 0; it < 4; ++it) {
+            const int idx = tid + it * kPpThreads;
+            const int rr = idx >> 4, cc = (idx & 15) * 16;
+            uint32_t* t = tile + (rr * kWtPitch + cc) / 4;
+            t[0] = (uint32_t)v[it].x, t[1] = (uint32_t)v[it].y, t[2] = (uint32_t)v[it].z, t[3] = (uint32_t)v[it].w;
+        }
+        __syncthreads();
+        // 64 groups of four columns x 8 groups of eight rows; neighbouring lanes take
+        // neighbouring row groups, so the 8 lanes of one column write one 128-byte output row
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int idx = tid + it * kPpThreads;
+            const int ng = idx & 7, kq = idx >> 3;
+            const int n = r0 + ng * 8, k = c0 + kq * 4;
+            if (n >= R || k >= C) continue;
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = tile[((ng * 8 + e) * kWtPitch) / 4 + kq];
+            __nv_bfloat16* dst;
+            size_t ld;
+            if (n < rsplit) {
+                dst = dst0 + n;
+                ld = (size_t)rsplit;
+            } else {
+                dst = dst1 + (n - rsplit);
+                ld = (size_t)(R - rsplit);
+            }
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = (float)(int8_t)((w[e] >> (8 * b)) & 0xFFu);
+                *reinterpret_cast<uint4*>(dst + (size_t)(k + b) * ld) = make_uint4(
+                    pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+            }
+        }
     }
 }
 
@@ -156,39 +238,39 @@ struct PpQuantArgs {
 
 // One CTA per token.  He % 8 == 0.
 template <bool F16>
-__global__ void __launch_bounds__(kPpThreads) pp_quant_x_kernel(const PpQuantArgs a) {
+__global__ void __launch_bounds__(kPpRowThreads) pp_quant_x_kernel(const PpQuantArgs a) {
     using H = Half16<F16>;
-    __shared__ double red[kPpThreads / 32 + 1];
+    __shared__ float2 red[kPpRowThreads / 32 + 1];
     pdl_launch_dependents();
     pdl_wait();
     const int t = blockIdx.x, tid = threadIdx.x;
     const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)t * a.He);
     const int n8 = a.He / 8;
-    double r = 1.0;
-    float inv = 1.f;
+    PpNorm nr = {0.f, 0.f, 1.f, a.He, a.eps};
     if (a.do_norm) {
-        // squares of 16-bit values are exact in double, and so is their sum for any order
-        // (the terms span far fewer than 53 bits): r is the correctly rounded definition
-        double ss = 0.0;
-        for (int i = tid; i < n8; i += kPpThreads) {
+        // squares of 16-bit values are exact floats; each thread adds its squares as a float
+        // pair, the CTA adds the pairs in double
+        float sh = 0.f, sl = 0.f;
+        for (int i = tid; i < n8; i += kPpRowThreads) {
             const uint4 v = xr[i];
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const double lo = H::lo(w[e]), hi = H::hi(w[e]);
-                ss += lo * lo + hi * hi;
+                const float lo = H::lo(w[e]), hi = H::hi(w[e]);
+                ff_add(sh, sl, lo * lo, 0.f);
+                ff_add(sh, sl, hi * hi, 0.f);
             }
         }
-        ss = pp_block_sum(ss, red);
-        r = __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, (double)a.He), a.eps));
-        inv = (float)(1.0 / r);
+        const float2 ss = pp_block_sum<kPpRowThreads>(sh, sl, red);
+        nr.sh = ss.x, nr.sl = ss.y;
+        nr.inv = rsqrtf((ss.x + ss.y) / (float)a.He + (float)a.eps);
     }
     const float qs = H::load(a.qscale, 0);
     const int qo = (int)a.qoffset[0];
     const uint4* gr = reinterpret_cast<const uint4*>(a.gamma);
     const uint4* br = reinterpret_cast<const uint4*>(a.beta);
     uint4* outr = reinterpret_cast<uint4*>(a.out + (size_t)t * a.He);
-    for (int i = tid; i < n8; i += kPpThreads) {
+    for (int i = tid; i < n8; i += kPpRowThreads) {
         const uint4 v = xr[i];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t gw[4] = {0, 0, 0, 0}, bw[4] = {0, 0, 0, 0};
@@ -201,8 +283,8 @@ __global__ void __launch_bounds__(kPpThreads) pp_quant_x_kernel(const PpQuantArg
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const bool nm = a.do_norm != 0;
-            o[e] = pack_bf16(pp_code(H::lo(w[e]), H::lo(gw[e]), H::lo(bw[e]), nm, r, inv, qs, qo),
-                             pp_code(H::hi(w[e]), H::hi(gw[e]), H::hi(bw[e]), nm, r, inv, qs, qo));
+            o[e] = pack_bf16(pp_code(H::lo(w[e]), 0.f, H::lo(gw[e]), H::lo(bw[e]), nm, nr, qs, qo),
+                             pp_code(H::hi(w[e]), 0.f, H::hi(gw[e]), H::hi(bw[e]), nm, nr, qs, qo));
         }
         outr[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -235,43 +317,70 @@ struct PpMidArgs {
     uint32_t* status;
 };
 
-// One CTA per token; dynamic shared memory holds the token's n1 values in double.
+// One CTA per token; dynamic shared memory holds the token's n1 values as exact float pairs
+// (y = (acc + bias) * deScale has at most 48 significant bits: acc + bias is an integer below
+// 2^24 and deScale a float, so its product splits exactly into a float and the float error).
 template <bool F16>
-__global__ void __launch_bounds__(kPpThreads) pp_mid_kernel(const PpMidArgs a) {
+__global__ void __launch_bounds__(kPpRowThreads) pp_mid_kernel(const PpMidArgs a) {
     using H = Half16<F16>;
-    extern __shared__ double ys[];
-    __shared__ double red[kPpThreads / 32 + 1];
+    extern __shared__ float2 ys[];
+    __shared__ float2 red[kPpRowThreads / 32 + 1];
     pdl_launch_dependents();
     pdl_wait();
     const int t = blockIdx.x, tid = threadIdx.x;
     const float* y0 = a.y + (size_t)t * a.n1;
-    double ss1 = 0.0, ss2 = 0.0;
-    for (int j = tid; j < a.n1; j += kPpThreads) {
+    float s1h = 0.f, s1l = 0.f, s2h = 0.f, s2l = 0.f;
+    // four columns per thread and step (n1 % 4 == 0), the k-range loads unrolled so that they
+    // are in flight together
+    for (int j4 = tid; j4 < a.n1 / 4; j4 += kPpRowThreads) {
         // the k-range partials are integer-valued (int8 products), so their fp32 sum in k-range
         // order is the exact integer while it stays below 2^24; bias and scale then in double
-        float acc = 0.f;
-        for (int s = 0; s < a.ksplit; ++s) acc += __ldcg(y0 + (size_t)s * a.slot_stride + j);   // k-range order
-        double v = (double)acc;
-        if (a.bias0 != nullptr) v += (double)a.bias0[j];
-        v = __dmul_rn(v, (double)a.de0[j]);
-        ys[j] = v;
-        if (j < a.Hcq)
-            ss1 += v * v;
-        else if (j < a.Hcq + a.Hckv)
-            ss2 += v * v;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int s = 0; s < a.ksplit; ++s) {   // k-range order
+            const float4 p = __ldcg(reinterpret_cast<const float4*>(y0 + (size_t)s * a.slot_stride) + j4);
+            acc.x += p.x, acc.y += p.y, acc.z += p.z, acc.w += p.w;
+        }
+        int4 b = make_int4(0, 0, 0, 0);
+        if (a.bias0 != nullptr) b = reinterpret_cast<const int4*>(a.bias0)[j4];
+        const float4 sc = reinterpret_cast<const float4*>(a.de0)[j4];
+        const float av[4] = {acc.x, acc.y, acc.z, acc.w}, sv[4] = {sc.x, sc.y, sc.z, sc.w};
+        const int bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int j = 4 * j4 + e;
+            float yh, yl;
+            two_prod(__fadd_rn(av[e], (float)bv[e]), sv[e], yh, yl);
+            ys[j] = make_float2(yh, yl);
+            // y^2 = yh^2 + 2 yh yl (+ yl^2, below the pair's precision)
+            float ph, pl;
+            two_prod(yh, yh, ph, pl);
+            pl = fmaf(2.f * yh, yl, pl);
+            if (j < a.Hcq)
+                ff_add(s1h, s1l, ph, pl);
+            else if (j < a.Hcq + a.Hckv)
+                ff_add(s2h, s2l, ph, pl);
+        }
     }
-    ss1 = pp_block_sum(ss1, red);
-    ss2 = pp_block_sum(ss2, red);   // its barriers also publish ys
-    const double r1 = __dsqrt_rn(__dadd_rn(__ddiv_rn(ss1, (double)a.Hcq), a.eps));
-    const float inv1 = (float)(1.0 / r1);
-    const float inv2 = (float)(1.0 / __dsqrt_rn(__dadd_rn(__ddiv_rn(ss2, (double)a.Hckv), a.eps)));
+    const float2 ss1 = pp_block_sum<kPpRowThreads>(s1h, s1l, red);
+    const float2 ss2 = pp_block_sum<kPpRowThreads>(s2h, s2l, red);   // its barriers also publish ys
+    const PpNorm nr1 = {ss1.x, ss1.y, rsqrtf((ss1.x + ss1.y) / (float)a.Hcq + (float)a.eps), a.Hcq, a.eps};
+    const float inv2 = rsqrtf((ss2.x + ss2.y) / (float)a.Hckv + (float)a.eps);
     // path 1: RmsNormQuant -> the up-projection's codes
     const float qs = H::load(a.qscale1, 0);
     const int qo = (int)a.qoffset1[0];
-    for (int j = 2 * tid; j < a.Hcq; j += 2 * kPpThreads) {
-        const float c0 = pp_code(ys[j], H::load(a.gamma1, j), H::load(a.beta1, j), true, r1, inv1, qs, qo);
-        const float c1 = pp_code(ys[j + 1], H::load(a.gamma1, j + 1), H::load(a.beta1, j + 1), true, r1, inv1, qs, qo);
-        *reinterpret_cast<uint32_t*>(a.codes1 + (size_t)t * a.Hcq + j) = pack_bf16(c0, c1);
+    for (int j8 = tid; j8 < a.Hcq / 8; j8 += kPpRowThreads) {   // eight columns per thread and step
+        const uint4 g = reinterpret_cast<const uint4*>(a.gamma1)[j8];
+        const uint4 b = reinterpret_cast<const uint4*>(a.beta1)[j8];
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, bw[4] = {b.x, b.y, b.z, b.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int j = 8 * j8 + 2 * e;
+            o[e] = pack_bf16(pp_code(ys[j].x, ys[j].y, H::lo(gw[e]), H::lo(bw[e]), true, nr1, qs, qo),
+                             pp_code(ys[j + 1].x, ys[j + 1].y, H::hi(gw[e]), H::hi(bw[e]), true, nr1, qs, qo));
+        }
+        reinterpret_cast<uint4*>(a.codes1 + (size_t)t * a.Hcq)[j8] = make_uint4(o[0], o[1], o[2], o[3]);
     }
     // paths 5 and 6: the cache row
     if (a.nslots <= 0) return;
@@ -280,12 +389,17 @@ __global__ void __launch_bounds__(kPpThreads) pp_mid_kernel(const PpMidArgs a) {
         if (tid == 0) atomicOr(a.status, kStatusCacheIndexRange);
         return;
     }
-    for (int j = tid; j < a.Hckv; j += kPpThreads)
-        H::store(a.kv, (size_t)slot * a.kv_ld + j, H::load(a.gamma2, j) * ((float)ys[a.Hcq + j] * inv2));
+    for (int j4 = tid; j4 < a.Hckv / 4; j4 += kPpRowThreads) {   // Hckv % 4 == 0, kv rows 8-byte aligned
+        const uint2 g = reinterpret_cast<const uint2*>(a.gamma2)[j4];
+        const float2* yv = ys + a.Hcq + 4 * j4;
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.kv) + (size_t)slot * a.kv_ld + 4 * j4) =
+            pp_pack4<F16>(H::lo(g.x) * (yv[0].x * inv2), H::hi(g.x) * (yv[1].x * inv2),
+                          H::lo(g.y) * (yv[2].x * inv2), H::hi(g.y) * (yv[3].x * inv2));
+    }
     const int h = a.Dr / 2;
-    const double* yr = ys + a.Hcq + a.Hckv;
-    for (int j = tid; j < h; j += kPpThreads) {
-        const float v0 = (float)yr[j], v1 = (float)yr[j + h];
+    const float2* yr = ys + a.Hcq + a.Hckv;
+    for (int j = tid; j < h; j += kPpRowThreads) {
+        const float v0 = yr[j].x, v1 = yr[j + h].x;
         const size_t tr = (size_t)t * a.Dr;
         const float o0 = v0 * H::load(a.cos, tr + j) - v1 * H::load(a.sin, tr + j);
         const float o1 = v1 * H::load(a.cos, tr + j + h) + v0 * H::load(a.sin, tr + j + h);
@@ -313,36 +427,61 @@ struct PpUpArgs {
     int qr_ld;
 };
 
-// One CTA per token.
+// Heads per CTA of pp_up_kernel: the grid is T * ceil(N / kPpUpHeads).
+constexpr int kPpUpHeads = 4;
+
+// kPpUpHeads heads of one token per CTA; a thread takes four consecutive product columns
+// (all its loads are independent 16-byte loads issued together).  D % 16 == 0, Dr % 8 == 0.
 template <bool F16>
 __global__ void __launch_bounds__(kPpThreads) pp_up_kernel(const PpUpArgs a) {
     using H = Half16<F16>;
     pdl_launch_dependents();
     pdl_wait();
-    const int t = blockIdx.x, tid = threadIdx.x;
-    const int hd = a.D + a.Dr;
-    const size_t n2 = (size_t)a.N * hd;
-    const float* z = a.z + (size_t)t * n2;
-    auto deq = [&](int c) {
-        float acc = __ldcg(z + c);
-        if (a.bias1 != nullptr) acc += (float)a.bias1[c];
-        return acc * a.de1[c];
+    const int groups = (a.N + kPpUpHeads - 1) / kPpUpHeads;
+    const int t = blockIdx.x / groups, n0 = (blockIdx.x % groups) * kPpUpHeads;
+    const int nh = min(kPpUpHeads, a.N - n0);
+    const int hd = a.D + a.Dr, h = a.Dr / 2;
+    const int per_head = a.D / 4 + h / 4;
+    const float* z = a.z + (size_t)t * a.N * hd;
+    auto deq4 = [&](int c) {
+        float4 v = __ldcg(reinterpret_cast<const float4*>(z + c));
+        if (a.bias1 != nullptr) {
+            const int4 b = *reinterpret_cast<const int4*>(a.bias1 + c);
+            v.x += (float)b.x, v.y += (float)b.y, v.z += (float)b.z, v.w += (float)b.w;
+        }
+        const float4 s = *reinterpret_cast<const float4*>(a.de1 + c);
+        return make_float4(v.x * s.x, v.y * s.y, v.z * s.z, v.w * s.w);
     };
-    for (int i = tid; i < a.N * a.D; i += kPpThreads) {
-        const int n = i / a.D, d = i - n * a.D;
-        H::store(a.qc, (size_t)t * a.N * a.D + i, deq(n * hd + d));
-    }
-    const int h = a.Dr / 2;
-    const size_t tr = (size_t)t * a.Dr;
-    for (int i = tid; i < a.N * h; i += kPpThreads) {
-        const int n = i / h, j = i - n * h;
-        const int c0 = n * hd + a.D + j;
-        const float v0 = deq(c0), v1 = deq(c0 + h);
-        const float o0 = v0 * H::load(a.cos, tr + j) - v1 * H::load(a.sin, tr + j);
-        const float o1 = v1 * H::load(a.cos, tr + j + h) + v0 * H::load(a.sin, tr + j + h);
-        const size_t base = ((size_t)t * a.N + n) * a.qr_ld;
-        H::store(a.qr, base + j, o0);
-        H::store(a.qr, base + j + h, o1);
+    for (int task = threadIdx.x; task < nh * per_head; task += kPpThreads) {
+        const int n = n0 + task / per_head, r = task % per_head;
+        if (r < a.D / 4) {
+            const float4 v = deq4(n * hd + 4 * r);
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.qc) + ((size_t)t * a.N + n) * a.D + 4 * r) =
+                pp_pack4<F16>(v.x, v.y, v.z, v.w);
+        } else {
+            const int j = 4 * (r - a.D / 4);
+            const int c0 = n * hd + a.D + j;
+            const float4 v0 = deq4(c0), v1 = deq4(c0 + h);
+            const size_t tr = (size_t)t * a.Dr;
+            const uint2 cl = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.cos) + tr + j);
+            const uint2 ch = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.cos) + tr + j + h);
+            const uint2 sl = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.sin) + tr + j);
+            const uint2 sh = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.sin) + tr + j + h);
+            const float x0[4] = {v0.x, v0.y, v0.z, v0.w}, x1[4] = {v1.x, v1.y, v1.z, v1.w};
+            const float c_lo[4] = {H::lo(cl.x), H::hi(cl.x), H::lo(cl.y), H::hi(cl.y)};
+            const float c_hi[4] = {H::lo(ch.x), H::hi(ch.x), H::lo(ch.y), H::hi(ch.y)};
+            const float s_lo[4] = {H::lo(sl.x), H::hi(sl.x), H::lo(sl.y), H::hi(sl.y)};
+            const float s_hi[4] = {H::lo(sh.x), H::hi(sh.x), H::lo(sh.y), H::hi(sh.y)};
+            float o0[4], o1[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o0[e] = x0[e] * c_lo[e] - x1[e] * s_lo[e];
+                o1[e] = x1[e] * c_hi[e] + x0[e] * s_hi[e];
+            }
+            uint16_t* dst = static_cast<uint16_t*>(a.qr) + ((size_t)t * a.N + n) * a.qr_ld;
+            *reinterpret_cast<uint2*>(dst + j) = pp_pack4<F16>(o0[0], o0[1], o0[2], o0[3]);
+            *reinterpret_cast<uint2*>(dst + j + h) = pp_pack4<F16>(o1[0], o1[1], o1[2], o1[3]);
+        }
     }
 }
 

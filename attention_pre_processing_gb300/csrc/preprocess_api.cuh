@@ -161,7 +161,7 @@ PpPlan pp_plan(const PpDims& d, int sms) {
     return p;
 }
 
-mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws, cudaStream_t st) {
+mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws, cudaStream_t st, int sms) {
     if (!get_encoder()) return MLA_ERR_RUNTIME;
     uint32_t* status = reinterpret_cast<uint32_t*>(ws);
     const int T = (int)d.T;
@@ -177,8 +177,9 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
 
     // ---- W1, W2: the int8 weights as bf16 (k, n) matrices
     auto widen = [&](const mla_tensor* src, int R, int C, __nv_bfloat16* dst0, __nv_bfloat16* dst1, int rsplit) {
-        const int cb = (C + 63) / 64, rb = (R + 63) / 64;
-        return launch(pp_widen_t_kernel, cb * rb, kPpThreads, 0, st, static_cast<const int8_t*>(src->data), R, C,
+        const long long tiles = (long long)((C + kWtCols - 1) / kWtCols) * ((R + kWtRows - 1) / kWtRows);
+        const int grid = (int)(tiles < 8LL * sms ? tiles : 8LL * sms);
+        return launch(pp_widen_t_kernel, grid, kPpThreads, 0, st, static_cast<const int8_t*>(src->data), R, C,
                       dst0, dst1, rsplit);
     };
     if (widen(a.w1, (int)p.n1, (int)d.He, w1a, w1b, (int)d.Hcq) != cudaSuccess) return MLA_ERR_RUNTIME;
@@ -197,7 +198,7 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
     q.He = (int)d.He;
     q.eps = a.eps;
     q.do_norm = a.do_norm ? 1 : 0;
-    e = launch(d.f16 ? pp_quant_x_kernel<true> : pp_quant_x_kernel<false>, T, kPpThreads, 0, st, q);
+    e = launch(d.f16 ? pp_quant_x_kernel<true> : pp_quant_x_kernel<false>, T, kPpRowThreads, 0, st, q);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "pp_quant_x");
 
@@ -243,7 +244,7 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
     m.kr = d.mode == 0 ? nullptr : a.kr->data;
     m.eps = a.eps;
     m.status = status;
-    e = launch(d.f16 ? pp_mid_kernel<true> : pp_mid_kernel<false>, T, kPpThreads, (size_t)p.n1 * 8, st, m);
+    e = launch(d.f16 ? pp_mid_kernel<true> : pp_mid_kernel<false>, T, kPpRowThreads, (size_t)p.n1 * 8, st, m);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "pp_norm_quant_cache");
 
@@ -278,7 +279,8 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
         u.qr = a.qrope->data;
         u.qr_ld = (int)d.Dr;
     }
-    e = launch(d.f16 ? pp_up_kernel<true> : pp_up_kernel<false>, T, kPpThreads, 0, st, u);
+    const int up_grid = T * (int)((d.N + kPpUpHeads - 1) / kPpUpHeads);
+    e = launch(d.f16 ? pp_up_kernel<true> : pp_up_kernel<false>, up_grid, kPpThreads, 0, st, u);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "pp_dequant_rope_q");
 
@@ -417,5 +419,5 @@ extern "C" mla_status mla_preprocess(MLA_PP_PARAMS, void* workspace, uint64_t wo
     if (workspaceSize < p.bytes) return MLA_ERR_PARAM_INVALID;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     timing_begin(st);
-    return pp_run(a, d, p, static_cast<uint8_t*>(workspace), st);
+    return pp_run(a, d, p, static_cast<uint8_t*>(workspace), st, sms);
 }

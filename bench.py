@@ -26,6 +26,7 @@ sys.path.insert(0, ROOT)
 
 HEADLINE = "decode_t32"
 PREFILL = "prefill_t8192"
+PREPROCESS = "pp_decode_t32"
 METRIC = "MLA prolog tokens/s & µs/call (T=32 decode, T=8192) + % HBM/tensor roofline"
 
 
@@ -240,6 +241,10 @@ def run_cuda(args, rank, world):
     if not args.skip_prefill:
         prefill = _prefill(dev, stream, flush_l2, peaks, max(3, min(K, 10)))
 
+    pre = None
+    if not args.skip_preprocess:
+        pre = _preprocess(dev, stream, flush_l2, peaks, max(3, min(K, 20)))
+
     cpu = None
     if rank == 0 and not args.skip_cpu:
         cpu = cpu_baseline(cfg, inp, budget_s=args.cpu_budget)
@@ -259,7 +264,7 @@ def run_cuda(args, rank, world):
             "roofline": roofline, "step_roofline": step_roof, "kernels_ms": kern_ms,
             "gpu_launches": kernels_per_step * K,
             "clocks": clk.summary(), "e2e": e2e, "wall_s_timed": t_wall,
-            "cpu_baseline": cpu, "prefill": prefill,
+            "cpu_baseline": cpu, "prefill": prefill, "preprocess": pre,
         }
         print(json.dumps(line))
     if dist is not None:
@@ -352,6 +357,58 @@ def _prefill(dev, stream, flush_l2, peaks, K):
             "kernels_ms": kern, "status_clean": ok}
 
 
+def pp_bytes(cfg):
+    """Algorithmic bytes of one aclnnMlaPreprocess call: every input read once (int8 weights at one
+    byte), qOut written once, one cache row per token."""
+    s = cfg.shape
+    n1, n2 = s.Hcq + s.Hckv + s.Dr, s.N * (s.D + s.Dr)
+    e = 2   # bf16 / fp16
+    weights = n1 * s.He + n2 * s.Hcq + s.N * s.D * s.Hckv * e
+    vectors = (n1 + n2) * 4 * (2 if cfg.with_bias else 1) + (2 * s.He + 2 * s.Hcq + s.Hckv + 2) * e + 2
+    per_token = s.He * e + 2 * s.Dr * e + 4 + s.N * (s.Hckv + s.Dr) * e + (s.Hckv + s.Dr) * e
+    return weights + vectors + s.T * per_token
+
+
+def _preprocess(dev, stream, flush_l2, peaks, K):
+    """The aclnnMlaPreprocess variant at T = 32 (DeepSeek-V3 shapes, int8 weights), beside the headline."""
+    import torch
+    from attention_pre_processing_gb300 import workloads, mla_prolog_timing_enable, mla_prolog_timing_read
+    from attention_pre_processing_gb300.runner import PreprocessCall
+    cfg = workloads.pp_config(PREPROCESS)
+    s = cfg.shape
+    call = PreprocessCall(cfg, workloads.make_pp_inputs(cfg), device=dev)
+    for _ in range(3):
+        flush_l2()
+        call(stream)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush_l2()
+        starts[i].record(stream)
+        call(stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / K
+    mla_prolog_timing_enable(True)
+    per = {}
+    for _ in range(K):
+        flush_l2()
+        call(stream)
+        for name, t in mla_prolog_timing_read():
+            per.setdefault(name, []).append(t)
+    mla_prolog_timing_enable(False)
+    kern = {k: statistics.mean(v) for k, v in per.items()}
+    b = pp_bytes(cfg)
+    ok = call.status(stream) == 0
+    del call
+    torch.cuda.empty_cache()
+    return {"workload": cfg.workload, "us_per_call": ms * 1e3, "tokens_per_s": s.T / (ms / 1e3),
+            "algorithmic_bytes": b, "achieved_gbs": b / (ms / 1e3) / 1e9,
+            "frac_of_measured_hbm": b / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "kernels_ms": kern, "gpu_launches_per_call": len(kern), "status_clean": ok}
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 def cpu_baseline(cfg, inp, budget_s=12.0, steps=None):
@@ -438,6 +495,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-preprocess", action="store_true", help="skip the aclnnMlaPreprocess variant's line")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--kernels-only", action="store_true", help="only warmup+steps calls of --workload")
