@@ -60,43 +60,6 @@ struct Half16<true> {
     }
 };
 
-// The int8 code of the page's static asymmetric quantiser,
-//   code = clamp(round_half_away(v * qs) + qo, -128, 127),  v = (gamma * y) / r + beta  (norm)
-//                                                            v = y                     (no norm)
-// with r = sqrt(mean(y^2) + eps), decided as in exact double arithmetic in this operation order:
-// the fp32 estimate decides unless it lies within its error bound of a rounding boundary (a
-// half-integer), and then the double expression does.  The bound: a handful of fp32 roundings
-// of at most 2^-24 relative each, on terms no larger than (|gamma * y / r| + |beta|) * |qs|;
-// 1e-5 of that is a wide margin.  y arrives as an unevaluated float pair y = yh + yl (yl = 0
-// when y is a float), the sum of squares as the pair (sh, sl) over nfeat features; inv is the
-// fp32 estimate of 1 / r.  GB300 runs doubles at a small fraction of its float rate, so the
-// double path (r included) runs only for the rare values near a boundary.
-struct PpNorm {
-    float sh, sl;   // sum of squares, as an unevaluated float pair
-    float inv;      // fp32 estimate of 1 / r
-    int nfeat;
-    double eps;
-};
-__device__ __forceinline__ float pp_code(float yh, float yl, float g, float b, bool norm, const PpNorm& nr, float qs,
-                                         int qo) {
-    const float a = norm ? g * yh * nr.inv : yh;
-    const float sf = (a + (norm ? b : 0.f)) * qs;
-    const float margin = 1e-5f * (fabsf(a) + (norm ? fabsf(b) : 0.f)) * fabsf(qs) + 1e-30f;
-    float q;
-    if (fabsf(sf - floorf(sf) - 0.5f) <= margin) {
-        const double y = (double)yh + (double)yl;
-        double v = y;
-        if (norm) {
-            const double r = __dsqrt_rn(__dadd_rn(__ddiv_rn((double)nr.sh + (double)nr.sl, (double)nr.nfeat), nr.eps));
-            v = __dadd_rn(__ddiv_rn(__dmul_rn((double)g, y), r), (double)b);
-        }
-        q = (float)round(__dmul_rn(v, (double)qs));   // round(): halves away from zero
-    } else {
-        q = roundf(sf);
-    }
-    return fminf(fmaxf(q + (float)qo, -128.f), 127.f);
-}
-
 // Error-free float transformations: s + e == a + b and p + e == a * b exactly.
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     s = __fadd_rn(a, b);
@@ -107,13 +70,97 @@ __device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
     p = __fmul_rn(a, b);
     e = fmaf(a, b, -p);
 }
-// (hi, lo) += v (v exact as a float pair vh + vl), keeping ~48 significant bits.
+// Float pairs (hi + lo, |lo| <= ulp(hi) / 2) carry ~48 significant bits.
+__device__ __forceinline__ void ff_norm(float& hi, float& lo) {
+    const float s = __fadd_rn(hi, lo);
+    lo = __fsub_rn(lo, __fsub_rn(s, hi));
+    hi = s;
+}
+// (hi, lo) += (vh, vl)
 __device__ __forceinline__ void ff_add(float& hi, float& lo, float vh, float vl) {
     float s, e;
     two_sum(hi, vh, s, e);
     e = __fadd_rn(e, __fadd_rn(lo, vl));
-    hi = __fadd_rn(s, e);
-    lo = __fsub_rn(e, __fsub_rn(hi, s));
+    hi = s;
+    lo = e;
+    ff_norm(hi, lo);
+}
+// (ah, al) * f
+__device__ __forceinline__ void ff_mul_f(float ah, float al, float f, float& h, float& l) {
+    two_prod(ah, f, h, l);
+    l = fmaf(al, f, l);
+    ff_norm(h, l);
+}
+// (ah, al) / (bh, bl); the residual a - q * b is formed exactly from the product's error term
+__device__ __forceinline__ void ff_div(float ah, float al, float bh, float bl, float& h, float& l) {
+    h = __fdiv_rn(ah, bh);
+    float p, e;
+    two_prod(h, bh, p, e);
+    const float rem = __fsub_rn(__fadd_rn(__fsub_rn(__fsub_rn(ah, p), e), al), __fmul_rn(h, bl));
+    l = __fdiv_rn(rem, bh);
+    ff_norm(h, l);
+}
+// sqrt(ah + al)
+__device__ __forceinline__ void ff_sqrt(float ah, float al, float& h, float& l) {
+    h = __fsqrt_rn(ah);
+    float p, e;
+    two_prod(h, h, p, e);
+    l = __fdiv_rn(__fadd_rn(__fsub_rn(__fsub_rn(ah, p), e), al), __fmul_rn(2.f, h));
+    ff_norm(h, l);
+}
+
+// The int8 code of the page's static asymmetric quantiser,
+//   code = clamp(round_half_away(v * qs) + qo, -128, 127),  v = (gamma * y) / r + beta  (norm)
+//                                                            v = y                     (no norm)
+// with r = sqrt(mean(y^2) + eps), evaluated in the definition's operation order.  The fp32
+// estimate decides unless it lies within its error bound of a rounding boundary (a
+// half-integer); the bound is a few fp32 roundings (2^-24 relative each) of terms no larger than
+// (|gamma * y / r| + |beta|) * |qs|, and 1e-5 of that is a wide margin.  Near a boundary the same
+// expression is evaluated in float pairs (~48 bits), which decide like exact arithmetic unless the
+// value lies within ~1e-13 of the half-integer (GB300 runs doubles at a small fraction of its
+// float rate, and a double path there cost microseconds per kernel).  y arrives as a float pair
+// (yl = 0 when y is a float); PpNorm holds r as a float pair and its fp32 reciprocal.
+struct PpNorm {
+    float rh, rl;   // r = sqrt(sum / nfeat + eps) as a float pair
+    float inv;      // fp32 estimate of 1 / r
+};
+// r from the sum of squares (sh, sl) over nfeat features and eps = eh + el.
+__device__ __forceinline__ PpNorm pp_norm(float sh, float sl, int nfeat, float eh, float el) {
+    float mh, ml;
+    ff_div(sh, sl, (float)nfeat, 0.f, mh, ml);   // nfeat <= 2^24: exact as a float
+    ff_add(mh, ml, eh, el);
+    PpNorm n;
+    ff_sqrt(mh, ml, n.rh, n.rl);
+    n.inv = __fdiv_rn(1.f, n.rh);
+    return n;
+}
+__device__ __forceinline__ float pp_code(float yh, float yl, float g, float b, bool norm, const PpNorm& nr, float qs,
+                                         int qo) {
+    const float a = norm ? g * yh * nr.inv : yh;
+    const float sf = (a + (norm ? b : 0.f)) * qs;
+    const float margin = 1e-5f * (fabsf(a) + (norm ? fabsf(b) : 0.f)) * fabsf(qs) + 1e-30f;
+    float q;
+    if (fabsf(sf - floorf(sf) - 0.5f) <= margin) {
+        float vh = yh, vl = yl;
+        if (norm) {
+            float ph, pl;
+            ff_mul_f(yh, yl, g, ph, pl);
+            ff_div(ph, pl, nr.rh, nr.rl, vh, vl);
+            ff_add(vh, vl, b, 0.f);
+        }
+        float sh, sl;
+        ff_mul_f(vh, vl, qs, sh, sl);
+        // round half away from zero: compare |s| with the half-integer next to it
+        const float sg = sh < 0.f ? -1.f : 1.f;
+        sh *= sg;
+        sl *= sg;
+        const float m = floorf(sh);
+        const float d = __fadd_rn(__fsub_rn(sh, m + 0.5f), sl);
+        q = sg * (m + (d >= 0.f ? 1.f : 0.f));
+    } else {
+        q = roundf(sf);
+    }
+    return fminf(fmaxf(q + (float)qo, -128.f), 127.f);
 }
 
 // Deterministic sum of float pairs over the CTA of NT threads (fixed shuffle tree, then the
@@ -232,7 +279,7 @@ struct PpQuantArgs {
     const int8_t* qoffset;  // (1)
     __nv_bfloat16* out;     // (T, He): codes as bf16
     int He;
-    double eps;
+    float eps_h, eps_l;     // epsilon as a float pair
     int do_norm;
 };
 
@@ -246,7 +293,7 @@ __global__ void __launch_bounds__(kPpRowThreads) pp_quant_x_kernel(const PpQuant
     const int t = blockIdx.x, tid = threadIdx.x;
     const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)t * a.He);
     const int n8 = a.He / 8;
-    PpNorm nr = {0.f, 0.f, 1.f, a.He, a.eps};
+    PpNorm nr = {1.f, 0.f, 1.f};
     if (a.do_norm) {
         // squares of 16-bit values are exact floats; each thread adds its squares as a float
         // pair, the CTA adds the pairs in double
@@ -262,8 +309,7 @@ __global__ void __launch_bounds__(kPpRowThreads) pp_quant_x_kernel(const PpQuant
             }
         }
         const float2 ss = pp_block_sum<kPpRowThreads>(sh, sl, red);
-        nr.sh = ss.x, nr.sl = ss.y;
-        nr.inv = rsqrtf((ss.x + ss.y) / (float)a.He + (float)a.eps);
+        nr = pp_norm(ss.x, ss.y, a.He, a.eps_h, a.eps_l);
     }
     const float qs = H::load(a.qscale, 0);
     const int qo = (int)a.qoffset[0];
@@ -313,7 +359,7 @@ struct PpMidArgs {
     void* kv;                  // (nslots, kv_ld) F
     int kv_ld;                 // Hckv + Dr (cacheMode 0) or Hckv (1)
     void* kr;                  // cacheMode 1: (nslots, Dr) F; cacheMode 0: null (k^R after k^N in kv)
-    double eps;
+    float eps_h, eps_l;        // epsilon as a float pair
     uint32_t* status;
 };
 
@@ -364,8 +410,8 @@ __global__ void __launch_bounds__(kPpRowThreads) pp_mid_kernel(const PpMidArgs a
     }
     const float2 ss1 = pp_block_sum<kPpRowThreads>(s1h, s1l, red);
     const float2 ss2 = pp_block_sum<kPpRowThreads>(s2h, s2l, red);   // its barriers also publish ys
-    const PpNorm nr1 = {ss1.x, ss1.y, rsqrtf((ss1.x + ss1.y) / (float)a.Hcq + (float)a.eps), a.Hcq, a.eps};
-    const float inv2 = rsqrtf((ss2.x + ss2.y) / (float)a.Hckv + (float)a.eps);
+    const PpNorm nr1 = pp_norm(ss1.x, ss1.y, a.Hcq, a.eps_h, a.eps_l);
+    const float inv2 = pp_norm(ss2.x, ss2.y, a.Hckv, a.eps_h, a.eps_l).inv;
     // path 1: RmsNormQuant -> the up-projection's codes
     const float qs = H::load(a.qscale1, 0);
     const int qo = (int)a.qoffset1[0];

@@ -196,7 +196,8 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
     q.qoffset = static_cast<const int8_t*>(a.qo0->data);
     q.out = a0;
     q.He = (int)d.He;
-    q.eps = a.eps;
+    q.eps_h = (float)a.eps;
+    q.eps_l = (float)(a.eps - (double)q.eps_h);
     q.do_norm = a.do_norm ? 1 : 0;
     e = launch(d.f16 ? pp_quant_x_kernel<true> : pp_quant_x_kernel<false>, T, kPpRowThreads, 0, st, q);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
@@ -242,7 +243,8 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
     m.kv = a.kv->data;
     m.kv_ld = (int)(d.mode == 0 ? d.Hckv + d.Dr : d.Hckv);
     m.kr = d.mode == 0 ? nullptr : a.kr->data;
-    m.eps = a.eps;
+    m.eps_h = (float)a.eps;
+    m.eps_l = (float)(a.eps - (double)m.eps_h);
     m.status = status;
     e = launch(d.f16 ? pp_mid_kernel<true> : pp_mid_kernel<false>, T, kPpRowThreads, (size_t)p.n1 * 8, st, m);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
