@@ -1,0 +1,324 @@
+// GEMM with int8 weights streamed as int8 and widened in shared memory (decode-sized calls of the
+// aclnnMlaPreprocess variant): out = A . W^T with A fp16 (T, K) row-major (int8 codes held as
+// fp16, exact) and W int8 (ncols, K) row-major, one row per output column ("transposeWdq/Wuq"
+// true).
+//
+// GB300's int8 tensor rate is far below its fp16 rate, so the contraction runs as fp16 MMAs with
+// fp32 accumulation (exact for these integer products while the sums stay below 2^24).  fp16
+// rather than bf16 because a byte fits its 10-bit mantissa: placing the biased byte under the
+// exponent of 1024 (one byte permute) and subtracting 1152 (one paired half subtraction) widens
+// two weights, where int-to-float conversions run at a quarter of the ALU rate and were the
+// bottleneck (0.8 us per 12 KB stage, measured).  Widening
+// the weights in global memory first would move three bytes per weight through HBM more than
+// needed; here the int8 tile crosses HBM once:
+//   warp 0      TMA producer: A tiles (128-byte swizzle) and int8 weight tiles (BN rows x 64 k,
+//               plain rows of 64 bytes) into a ring of stages
+//   warp 1      TMEM allocation and the tcgen05.mma issuer (B K-major, 128-byte swizzle)
+//   warps 2-5   epilogue: TMEM -> fp32 k-range slots (split-K), as gemm_tc's EPI_F32
+//   warps 6-13  converters: each 16-byte int8 chunk of a weight row -> two 16-byte fp16 chunks
+//               of the K-major swizzled B tile (chunk c of row r at (c ^ (r % 8)) * 16), then a
+//               proxy fence and an arrival on the stage's "B ready" barrier
+// The int8 and A tiles run in a deep ring of stages (the weight stream's latency hiding); the
+// fp16 B tiles in a ring of two slots only (the converters stay at most one k-block ahead of the
+// tensor core), so that the shared memory goes to int8 stages in flight.  Stage s is reused only
+// after the MMAs that read it commit (empty[s]), which follows its conversion; slot j only after
+// the MMAs that read it commit (bempty[j]).  Every wait is bounded and sets kStatusWaitTimeout.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "gemm_tc.cuh"
+#include "ptx.cuh"
+
+namespace mla {
+
+// Converter threads: eight warps, two per scheduler, so that one warp's shared-memory latency
+// hides behind the other's arithmetic (with four, a 24 KB stage took ~1 us to convert, measured).
+constexpr int kW8Conv = 256;
+constexpr int kW8Threads = 64 + 128 + kW8Conv;
+
+// k-blocks of 64 per int8 stage: one TMA box of 64 * kW8Kb bytes per weight row.  The TMA
+// engine moves a box row by row, at a per-SM rate of rows, so longer rows move more bytes.
+constexpr int kW8Kb = 2;
+
+template <int BN, int MSUB, int MAXST>
+struct W8Cfg {
+    static constexpr int kKb = kW8Kb;
+    static constexpr int kB8Row = kBK * kKb;         // bytes per weight row per stage
+    static constexpr int kB8Stage = BN * kB8Row;     // int8: BN rows x 64 * kKb k
+    static constexpr int kBStage = BN * kBK * 2;     // fp16: BN rows x 128 bytes
+    static constexpr int kBSlots = 2;
+    static constexpr int kAcc = MSUB * BN;
+    static constexpr int kNBuf = (2 * kAcc <= 512) ? 2 : 1;
+    static constexpr int kTmemCols = (kNBuf * kAcc <= 32) ? 32 : (kNBuf * kAcc <= 64) ? 64
+                                     : (kNBuf * kAcc <= 128) ? 128 : (kNBuf * kAcc <= 256) ? 256 : 512;
+    static constexpr int kBarBytes = 1024;
+    static_assert(8 * (3 * MAXST + 9) + 16 <= kBarBytes, "barrier area");
+    static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
+    static_assert(kAcc <= 512, "accumulator exceeds TMEM");
+    static __host__ __device__ int a_stage_bytes(int a_box_rows) { return kKb * MSUB * a_box_rows * 128; }
+    static __host__ __device__ int stage_bytes(int a_box_rows) { return a_stage_bytes(a_box_rows) + kB8Stage; }
+    // Layout: barriers | A ring | fp16 B slots | int8 ring.  A 128-row MMA read of a short A box
+    // runs at most 16 KB past its stage, into the B slots (>= 16 KB), inside the block.
+    static __host__ __device__ size_t smem_bytes(int stages, int a_box_rows) {
+        return 1024 + kBarBytes + (size_t)kBSlots * kBStage + (size_t)stages * stage_bytes(a_box_rows);
+    }
+    static __host__ int max_stages(int a_box_rows) {
+        int s = (int)((kSmemLimit - 1024 - kBarBytes - kBSlots * kBStage) / stage_bytes(a_box_rows));
+        return s < MAXST ? s : MAXST;
+    }
+    static_assert(kBSlots * kBStage >= 16384, "the B slots must cover the A over-read");
+};
+
+template <int BN, int MSUB, int MAXST>
+__global__ void __launch_bounds__(kW8Threads, 1)
+    gemm_w8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b8,
+                   const GemmArgs args) {
+    using C = W8Cfg<BN, MSUB, MAXST>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* full = bars;                 // A tile landed (TMA)
+    uint64_t* empty = bars + MAXST;        // the stage's MMAs completed
+    uint64_t* full8 = bars + 2 * MAXST;    // int8 weight tile landed (TMA)
+    uint64_t* bfull = bars + 3 * MAXST;    // fp16 slot written by the converters (2)
+    uint64_t* bempty = bfull + 2;          // fp16 slot's MMAs completed (2)
+    uint64_t* tfull = bempty + 2;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done = tempty + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    const int stages = args.stages;
+    const int a_stage = C::a_stage_bytes(args.a_box_rows);
+    const int a_box = args.a_box_rows * 128;
+    uint8_t* sA = smem + C::kBarBytes;
+    uint8_t* sB = sA + (size_t)stages * a_stage;
+    uint8_t* sB8 = sB + (size_t)C::kBSlots * C::kBStage;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_b8);
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&full8[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bfull[b]), kW8Conv);
+            mbar_init(smem_u32(&bempty[b]), 1);
+            mbar_init(smem_u32(&tfull[b]), 1);
+            mbar_init(smem_u32(&tempty[b]), 128);
+        }
+        mbar_init(smem_u32(done), 1);
+        *s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+
+    pdl_launch_dependents();
+    pdl_wait();   // A and W are both written by earlier kernels of the call
+    if (args.clear_status && blockIdx.x == 0 && threadIdx.x == 64) *args.status = 0u;
+
+    auto fail = [&]() {
+        *s_abort = 1;
+        atomicOr(args.status, kStatusWaitTimeout);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_a = policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            Unit u;
+            bool ok = true;
+            for (int idx = 0; ok && get_unit(args, idx, u); ++idx) {
+                for (int kb = u.kb0; kb < u.kb1; kb += C::kKb) {
+                    if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, s_abort, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const int nkb = min(C::kKb, u.kb1 - kb);   // the unit's last stage may be short
+                    const uint32_t fa = smem_u32(&full[s]), f8 = smem_u32(&full8[s]);
+                    mbar_arrive_expect_tx(f8, (uint32_t)C::kB8Stage);   // the whole box lands (zeros past K)
+                    tma_load_2d(smem_u32(sB8 + (size_t)s * C::kB8Stage), &map_b8, f8, kb * kBK, u.n_tile * BN, pol_w);
+                    mbar_arrive_expect_tx(fa, (uint32_t)(nkb * MSUB * a_box));
+                    for (int i = 0; i < nkb; ++i)
+                        load_a<MSUB>(args, u, kb + i, smem_u32(sA + (size_t)s * a_stage + i * MSUB * a_box), a_box, fa,
+                                     &map_a, pol_a);
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok) fail();
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(128, BN, false, false);   // fp16, A and B K-major
+            const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), 16, 1024);
+            int s = 0;
+            uint32_t ph = 0, ai = 0, gi = 0;   // gi: k-blocks so far (fp16 slot gi & 1, use gi >> 1)
+            Unit u;
+            bool ok = true;
+            for (int idx = 0; ok && get_unit(args, idx, u); ++idx, ++ai) {
+                const int b = ai % C::kNBuf;
+                const uint32_t aph = (ai / C::kNBuf) & 1;
+                if (!mbar_wait(smem_u32(&tempty[b]), aph ^ 1, s_abort, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_base = tmem_base + b * C::kAcc;
+                for (int kb = u.kb0; ok && kb < u.kb1; kb += C::kKb) {
+                    const int nkb = min(C::kKb, u.kb1 - kb);
+                    if (!mbar_wait(smem_u32(&full[s]), ph, s_abort, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int i = 0; i < nkb; ++i, ++gi) {
+                        const int j = (int)(gi & 1u);
+                        if (!mbar_wait(smem_u32(&bfull[j]), (gi >> 1) & 1u, s_abort, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t a_desc =
+                            a_desc0 + (uint64_t)(((size_t)s * a_stage + (size_t)i * MSUB * a_box) >> 4);
+                        const uint64_t b_desc = b_desc0 + (uint64_t)j * (uint64_t)(C::kBStage >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+#pragma unroll
+                            for (int ms = 0; ms < MSUB; ++ms)
+                                umma_bf16(d_base + ms * BN, a_desc + (uint64_t)(((ms * a_box) >> 4) + 2 * kk),
+                                          b_desc + (uint64_t)(2 * kk), idesc, (kb + i > u.kb0 || kk > 0) ? 1u : 0u);
+                        umma_commit(smem_u32(&bempty[j]));
+                    }
+                    if (!ok) break;
+                    umma_commit(smem_u32(&empty[s]));
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&tfull[b]));
+            }
+            if (!ok) fail();
+            umma_commit(smem_u32(done));
+            mbar_wait(smem_u32(done), 0, s_abort, kWaitLimitNs / 4);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ epilogue warps
+        const int q = warp & 3;
+        const int row_in = q * 32 + lane;
+        uint32_t ai = 0;
+        Unit u;
+        for (int idx = 0; get_unit(args, idx, u); ++idx, ++ai) {
+            const int b = ai % C::kNBuf;
+            const uint32_t aph = (ai / C::kNBuf) & 1;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(smem_u32(&tfull[b]), aph, s_abort, kWaitLimitNs) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok && lane == 0) fail();
+            if (epi_any_n<128>(!ok)) break;
+            __syncwarp();
+            tc_fence_after();
+            const TmemSrc tsrc{tmem_base + ((uint32_t)(q * 32) << 16) + b * C::kAcc};
+            epilogue_f32<BN, MSUB>(args, u.m_tile * MSUB * 128 + row_in, u.n_tile, u.ks, tsrc);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&tempty[b]));
+        }
+    } else {
+        // ------------------------------------------------------------ converters
+        const int ct = threadIdx.x - 192;   // 0 .. kW8Conv - 1
+        int s = 0;
+        uint32_t ph = 0, gi = 0;
+        Unit u;
+        bool ok = true;
+        for (int idx = 0; ok && get_unit(args, idx, u); ++idx) {
+            for (int kb = u.kb0; ok && kb < u.kb1; kb += C::kKb) {
+                const int nkb = min(C::kKb, u.kb1 - kb);
+                if (!mbar_wait(smem_u32(&full8[s]), ph, s_abort, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                for (int i = 0; i < nkb; ++i, ++gi) {
+                    const int j = (int)(gi & 1u);
+                    if (!mbar_wait(smem_u32(&bempty[j]), ((gi >> 1) & 1u) ^ 1u, s_abort, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* src = sB8 + (size_t)s * C::kB8Stage + i * kBK;
+                    const uint32_t dst = smem_u32(sB + (size_t)j * C::kBStage);
+#pragma unroll 2
+                    for (int task = ct; task < BN * 4; task += kW8Conv) {
+                        const int r = task >> 2, c = task & 3;   // row r, 16-byte int8 chunk c (k 16c .. 16c+15)
+                        const int4 v = *reinterpret_cast<const int4*>(src + r * C::kB8Row + c * 16);
+                        const uint32_t w[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+                        uint32_t o[8];
+                        const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t ub = w[e] ^ 0x80808080u;   // bytes b + 128, in 0..255
+                            // (1024 + byte) as fp16: the byte under the exponent bits 0x64
+                            uint32_t lo = __byte_perm(ub, 0x64646464u, 0x4140u), hi = __byte_perm(ub, 0x64646464u, 0x4342u);
+                            __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
+                            __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
+                            o[2 * e] = *reinterpret_cast<uint32_t*>(&hl);
+                            o[2 * e + 1] = *reinterpret_cast<uint32_t*>(&hh);
+                        }
+                        const uint32_t row = dst + (uint32_t)(r * 128);
+                        const uint32_t sw = (uint32_t)(r & 7);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((2u * c) ^ sw) << 4)),
+                                     "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((2u * c + 1) ^ sw) << 4)),
+                                     "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                                     : "memory");
+                    }
+                    fence_proxy_async_smem();   // the tensor core reads what these threads wrote
+                    mbar_arrive(smem_u32(&bfull[j]));
+                }
+                if (!ok) break;
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
+        if (!ok) fail();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*s_abort) {
+        // A wait gave up: give copies that may still be in flight time to land.
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 20000000ull) {
+        }
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+}  // namespace mla

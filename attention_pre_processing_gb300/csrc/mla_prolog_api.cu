@@ -25,6 +25,7 @@
 #include "gemm_tc.cuh"
 #include "gemm_pair.cuh"
 #include "preprocess.cuh"
+#include "gemm_w8.cuh"
 
 using namespace mla;
 

@@ -1,8 +1,7 @@
-// Row kernels of the "aclnnMlaPreprocess" variant (the three contractions run on gemm_tc):
-//   pp_widen_t_kernel   int8 weight stored one row per output column -> bf16 (k, n) for the
-//                       GEMMs (exact: |v| <= 128 has at most 8 significant bits)
+// Row kernels of the "aclnnMlaPreprocess" variant (the two int8 contractions run on gemm_w8,
+// the W^UK contraction on gemm_tc):
 //   pp_quant_x_kernel   RmsNormQuant of the input (or the quantiser alone) -> int8 codes held
-//                       as bf16, the A operand of the down-projection
+//                       as fp16, the A operand of the down-projection
 //   pp_mid_kernel       per token after the down-projection: add the k-range slots, + bias0,
 //                       * deScale0; RmsNormQuant of the c^Q part -> codes (A of the
 //                       up-projection); RmsNorm of the kv part and RoPE of the rope part ->
@@ -198,77 +197,6 @@ __device__ __forceinline__ uint2 pp_pack4(float a, float b, float c, float d) {
         return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
 
-// ---------------------------------------------------------------- weight widening
-
-// src: int8 (R, C), one row per output column n (R = columns, C = k).  dst0: bf16 (C, rsplit)
-// holding columns n < rsplit; dst1: bf16 (C, R - rsplit) holding the rest (may be null when
-// rsplit == R).  One tile of 64 rows x 256 columns per CTA and step, through shared memory:
-// the reads take 256 contiguous bytes of each row, the writes 128 contiguous bytes (64 bf16) of
-// each of the tile's 256 output rows.  A thread turns four 4-byte words of eight tile rows into
-// four 8-value output chunks.  The row pitch of 65 words makes the eight rows' words fall in
-// banks two apart.  Requires R % 8 == 0, C % 16 == 0, rsplit % 8 == 0.
-constexpr int kWtRows = 64, kWtCols = 256, kWtPitch = kWtCols + 4;   // bytes per tile row
-__global__ void __launch_bounds__(kPpThreads) pp_widen_t_kernel(const int8_t* __restrict__ src, int R, int C,
-                                                                __nv_bfloat16* __restrict__ dst0,
-                                                                __nv_bfloat16* __restrict__ dst1, int rsplit) {
-    __shared__ __align__(16) uint32_t tile[kWtRows * kWtPitch / 4];
-    pdl_launch_dependents();
-    pdl_wait();
-    const int tid = threadIdx.x;
-    const int cb = (C + kWtCols - 1) / kWtCols, rb = (R + kWtRows - 1) / kWtRows;
-    for (int tt = blockIdx.x; tt < cb * rb; tt += gridDim.x) {
-        const int c0 = (tt % cb) * kWtCols, r0 = (tt / cb) * kWtRows;
-        // 64 rows x 16 chunks of 16 bytes: four per thread, all in flight together
-        int4 v[4];
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int idx = tid + it * kPpThreads;
-            const int rr = idx >> 4, cc = (idx & 15) * 16;
-            const int r = r0 + rr, c = c0 + cc;
-            v[it] = (r < R && c < C) ? __ldcs(reinterpret_cast<const int4*>(src + (size_t)r * C + c))
-                                     : make_int4(0, 0, 0, 0);
-        }
-        __syncthreads();   // the previous tile's reads of shared memory are done
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int idx = tid + it * kPpThreads;
-            const int rr = idx >> 4, cc = (idx & 15) * 16;
-            uint32_t* t = tile + (rr * kWtPitch + cc) / 4;
-            t[0] = (uint32_t)v[it].x, t[1] = (uint32_t)v[it].y, t[2] = (uint32_t)v[it].z, t[3] = (uint32_t)v[it].w;
-        }
-        __syncthreads();
-        // 64 groups of four columns x 8 groups of eight rows; neighbouring lanes take
-        // neighbouring row groups, so the 8 lanes of one column write one 128-byte output row
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int idx = tid + it * kPpThreads;
-            const int ng = idx & 7, kq = idx >> 3;
-            const int n = r0 + ng * 8, k = c0 + kq * 4;
-            if (n >= R || k >= C) continue;
-            uint32_t w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = tile[((ng * 8 + e) * kWtPitch) / 4 + kq];
-            __nv_bfloat16* dst;
-            size_t ld;
-            if (n < rsplit) {
-                dst = dst0 + n;
-                ld = (size_t)rsplit;
-            } else {
-                dst = dst1 + (n - rsplit);
-                ld = (size_t)(R - rsplit);
-            }
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = (float)(int8_t)((w[e] >> (8 * b)) & 0xFFu);
-                *reinterpret_cast<uint4*>(dst + (size_t)(k + b) * ld) = make_uint4(
-                    pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-            }
-        }
-    }
-}
-
 // ---------------------------------------------------------------- input quantisation
 
 struct PpQuantArgs {
@@ -277,7 +205,7 @@ struct PpQuantArgs {
     const void* beta;       // (He) F
     const void* qscale;     // (1) F
     const int8_t* qoffset;  // (1)
-    __nv_bfloat16* out;     // (T, He): codes as bf16
+    __nv_bfloat16* out;     // (T, He): codes as fp16 (exact), the A operand of gemm_w8
     int He;
     float eps_h, eps_l;     // epsilon as a float pair
     int do_norm;
@@ -329,8 +257,8 @@ __global__ void __launch_bounds__(kPpRowThreads) pp_quant_x_kernel(const PpQuant
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const bool nm = a.do_norm != 0;
-            o[e] = pack_bf16(pp_code(H::lo(w[e]), 0.f, H::lo(gw[e]), H::lo(bw[e]), nm, nr, qs, qo),
-                             pp_code(H::hi(w[e]), 0.f, H::hi(gw[e]), H::hi(bw[e]), nm, nr, qs, qo));
+            o[e] = pack_f16(pp_code(H::lo(w[e]), 0.f, H::lo(gw[e]), H::lo(bw[e]), nm, nr, qs, qo),
+                            pp_code(H::hi(w[e]), 0.f, H::hi(gw[e]), H::hi(bw[e]), nm, nr, qs, qo));
         }
         outr[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -350,7 +278,7 @@ struct PpMidArgs {
     const void* beta1;         // (Hcq) F
     const void* qscale1;       // (1) F
     const int8_t* qoffset1;    // (1)
-    __nv_bfloat16* codes1;     // (T, Hcq): codes as bf16
+    __nv_bfloat16* codes1;     // (T, Hcq): codes as fp16 (exact), the A operand of gemm_w8
     const void* gamma2;        // (Hckv) F
     const void* cos;           // (T, Dr) F
     const void* sin;           // (T, Dr) F
@@ -423,8 +351,8 @@ __global__ void __launch_bounds__(kPpRowThreads) pp_mid_kernel(const PpMidArgs a
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int j = 8 * j8 + 2 * e;
-            o[e] = pack_bf16(pp_code(ys[j].x, ys[j].y, H::lo(gw[e]), H::lo(bw[e]), true, nr1, qs, qo),
-                             pp_code(ys[j + 1].x, ys[j + 1].y, H::hi(gw[e]), H::hi(bw[e]), true, nr1, qs, qo));
+            o[e] = pack_f16(pp_code(ys[j].x, ys[j].y, H::lo(gw[e]), H::lo(bw[e]), true, nr1, qs, qo),
+                            pp_code(ys[j + 1].x, ys[j + 1].y, H::hi(gw[e]), H::hi(bw[e]), true, nr1, qs, qo));
         }
         reinterpret_cast<uint4*>(a.codes1 + (size_t)t * a.Hcq)[j8] = make_uint4(o[0], o[1], o[2], o[3]);
     }

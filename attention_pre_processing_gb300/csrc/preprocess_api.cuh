@@ -3,13 +3,12 @@
 // mla_prolog_api.cu (it uses that file's launch helpers and tensor-map encoders).
 //
 // Pipeline of one call (the caller's stream, programmatic dependent launch between kernels):
-//   W1  wdqkv int8 (Hcq+576, He) -> bf16 (He, Hcq) | (He, 576)      [workspace]
-//   W2  wuq   int8 (n2, Hcq)     -> bf16 (Hcq, n2)                  [workspace]
-//   Q0  RmsNormQuant(x) -> int8 codes as bf16 (T, He)
-//   G1  codes . W1 -> fp32 k-range partials (T, Hcq + 576)           (gemm_tc, split-K)
-//   M1  + bias0, * deScale0; RmsNormQuant(c^Q part) -> codes (T, Hcq); RmsNorm(kv) and
+//   Q0  RmsNormQuant(x) -> int8 codes as fp16 (T, He)
+//   G1  codes . wdqkv^T -> fp32 k-range partials (T, Hcq + 576)      (gemm_w8: int8 weights
+//       widened in shared memory, split-K)
+//   M1  + bias0, * deScale0; RmsNormQuant(c^Q part) -> fp16 codes (T, Hcq); RmsNorm(kv) and
 //       RoPE(kr) -> cache row at slotMapping[t]
-//   G2  codes . W2 -> fp32 (T, n2)                                    (gemm_tc)
+//   G2  codes . wuq^T -> fp32 (T, n2)                                 (gemm_w8)
 //   U2  + bias1, * deScale1 -> q^C (T, N, D) 16-bit; RoPE(q^R) -> q output
 //   G3  q^C[:, n, :] . W^UK[n] -> q^N into qOut (row stride 576 or 512 per head)
 
@@ -40,10 +39,33 @@ struct PpPlan {
     GemmPlan g1, g2, g3;
     int64_t n1 = 0, n2 = 0;
     bool kps3 = false;
-    size_t off_a0 = 0, off_y1 = 0, off_a1 = 0, off_y2 = 0, off_qc = 0, off_w1a = 0, off_w1b = 0, off_w2 = 0, bytes = 0;
+    size_t off_a0 = 0, off_y1 = 0, off_a1 = 0, off_y2 = 0, off_qc = 0, bytes = 0;
 };
 
 bool pp_absent(const mla_tensor* t) { return t == nullptr || numel(t) == 0; }
+
+// int8 (rows, K) row-major weight, one row per output column: boxes of 64 * kW8Kb k (no
+// swizzle) x box_rows rows; rows and columns past the end read as zero.
+bool map_w8_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
+    const cuuint64_t gd[2] = {K, rows};
+    const cuuint64_t gs[1] = {K};
+    const cuuint32_t bx[2] = {(cuuint32_t)(64 * kW8Kb), box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gd, gs, bx, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int MSUB, int MAXST>
+cudaError_t launch_gemm_w8(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b8, GemmArgs args) {
+    using C = W8Cfg<BN, MSUB, MAXST>;
+    auto k = gemm_w8_kernel<BN, MSUB, MAXST>;
+    args.stages = C::max_stages(args.a_box_rows);
+    if (args.stages < 2) return cudaErrorInvalidConfiguration;
+    cudaError_t e = set_attr(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+    if (e != cudaSuccess) return e;
+    return launch(k, grid, kW8Threads, C::smem_bytes(args.stages, args.a_box_rows), st, a, b8, args);
+}
 
 mla_status pp_validate(const PpArgs& a, PpDims& d) {
     const mla_tensor* req[] = {a.x,  a.g0,  a.b0, a.qs0, a.qo0, a.w1,  a.de0,   a.g1,   a.b1,    a.qs1,
@@ -154,14 +176,11 @@ PpPlan pp_plan(const PpDims& d, int sms) {
     p.off_a1 = take((size_t)T * d.Hcq * 2);
     p.off_y2 = take((size_t)T * p.n2 * 4);
     p.off_qc = take((size_t)T * d.N * d.D * 2);
-    p.off_w1a = take((size_t)d.He * d.Hcq * 2);
-    p.off_w1b = take((size_t)d.He * (d.Hckv + d.Dr) * 2);
-    p.off_w2 = take((size_t)d.Hcq * p.n2 * 2);
     p.bytes = off;
     return p;
 }
 
-mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws, cudaStream_t st, int sms) {
+mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws, cudaStream_t st) {
     if (!get_encoder()) return MLA_ERR_RUNTIME;
     uint32_t* status = reinterpret_cast<uint32_t*>(ws);
     const int T = (int)d.T;
@@ -170,22 +189,7 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
     auto* a1 = reinterpret_cast<__nv_bfloat16*>(ws + p.off_a1);
     auto* y2 = reinterpret_cast<float*>(ws + p.off_y2);
     uint8_t* qc = ws + p.off_qc;
-    auto* w1a = reinterpret_cast<__nv_bfloat16*>(ws + p.off_w1a);
-    auto* w1b = reinterpret_cast<__nv_bfloat16*>(ws + p.off_w1b);
-    auto* w2 = reinterpret_cast<__nv_bfloat16*>(ws + p.off_w2);
     cudaError_t e;
-
-    // ---- W1, W2: the int8 weights as bf16 (k, n) matrices
-    auto widen = [&](const mla_tensor* src, int R, int C, __nv_bfloat16* dst0, __nv_bfloat16* dst1, int rsplit) {
-        const long long tiles = (long long)((C + kWtCols - 1) / kWtCols) * ((R + kWtRows - 1) / kWtRows);
-        const int grid = (int)(tiles < 8LL * sms ? tiles : 8LL * sms);
-        return launch(pp_widen_t_kernel, grid, kPpThreads, 0, st, static_cast<const int8_t*>(src->data), R, C,
-                      dst0, dst1, rsplit);
-    };
-    if (widen(a.w1, (int)p.n1, (int)d.He, w1a, w1b, (int)d.Hcq) != cudaSuccess) return MLA_ERR_RUNTIME;
-    timing_mark(st, "pp_widen_wdqkv");
-    if (widen(a.w2, (int)p.n2, (int)d.Hcq, w2, nullptr, (int)p.n2) != cudaSuccess) return MLA_ERR_RUNTIME;
-    timing_mark(st, "pp_widen_wuq");
 
     // ---- Q0: the input's int8 codes
     PpQuantArgs q = {};
@@ -204,18 +208,15 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
     timing_mark(st, "pp_quant_x");
 
     // ---- G1: down-projection
-    CUtensorMap mA1, mB1a, mB1b;
-    if (!map_2d(&mA1, a0, d.T, d.He, (uint32_t)p.g1.a_box_rows) || !map_2d(&mB1a, w1a, d.He, d.Hcq, 64) ||
-        !map_2d(&mB1b, w1b, d.He, d.Hckv + d.Dr, 64))
+    CUtensorMap mA1, mB1;
+    if (!map_2d(&mA1, a0, d.T, d.He, (uint32_t)p.g1.a_box_rows) ||
+        !map_w8_rows(&mB1, a.w1->data, p.n1, d.He, (uint32_t)p.g1.bn))
         return MLA_ERR_RUNTIME;
     GemmArgs g1 = gemm_args(p.g1, T, p.n1, status);
-    g1.b_split_col = (int)d.Hcq;
     g1.clear_status = 1;
-    g1.a_ready = 0;
-    g1.b_late = 1;
     g1.out_f32 = y1;
-    e = p.g1.bn == 64 ? launch_gemm<64, 1, 32, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
-                      : launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+    e = p.g1.bn == 64 ? launch_gemm_w8<64, 1, 16>(p.g1.grid, st, mA1, mB1, g1)
+                      : launch_gemm_w8<192, 2, 16>(p.g1.grid, st, mA1, mB1, g1);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "pp_down_proj");
 
@@ -252,14 +253,13 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
 
     // ---- G2: up-projection
     CUtensorMap mA2, mB2;
-    if (!map_2d(&mA2, a1, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) || !map_2d(&mB2, w2, d.Hcq, p.n2, 64))
+    if (!map_2d(&mA2, a1, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
+        !map_w8_rows(&mB2, a.w2->data, p.n2, d.Hcq, (uint32_t)p.g2.bn))
         return MLA_ERR_RUNTIME;
     GemmArgs g2 = gemm_args(p.g2, T, p.n2, status);
-    g2.a_ready = 0;
-    g2.b_late = 1;
     g2.out_f32 = y2;
-    e = p.g2.msub == 1 ? launch_gemm<192, 1, 16, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2)
-                       : launch_gemm<192, 2, 4, EPI_F32>(p.g2.grid, st, mA2, mB2, mB2, g2);
+    e = p.g2.msub == 1 ? launch_gemm_w8<192, 1, 16>(p.g2.grid, st, mA2, mB2, g2)
+                       : launch_gemm_w8<192, 2, 16>(p.g2.grid, st, mA2, mB2, g2);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "pp_up_proj");
 
@@ -421,5 +421,5 @@ extern "C" mla_status mla_preprocess(MLA_PP_PARAMS, void* workspace, uint64_t wo
     if (workspaceSize < p.bytes) return MLA_ERR_PARAM_INVALID;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     timing_begin(st);
-    return pp_run(a, d, p, static_cast<uint8_t*>(workspace), st, sms);
+    return pp_run(a, d, p, static_cast<uint8_t*>(workspace), st);
 }
