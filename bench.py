@@ -133,6 +133,20 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ multi-rank timing
+
+def job_rate(total_ms_local, tokens_per_rank, world, dist=None, device=None):
+    """Whole-job throughput of N replicas (weak scaling: every rank runs the full workload):
+    the units all ranks processed divided by the slowest rank's time (MAX over ranks).
+    Returns (max total ms, tokens/s)."""
+    import torch
+    t = torch.tensor([float(total_ms_local)], dtype=torch.float64, device=device)
+    if dist is not None and world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total = float(t.item())
+    return total, tokens_per_rank * world / (total / 1e3)
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_cuda(args, rank, world):
@@ -195,14 +209,8 @@ def run_cuda(args, rank, world):
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     if call.status(stream) != 0:
         raise RuntimeError("device status bits set during the timed region")
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = job_rate(sum(step_ms), s.T * K, world, dist, dev)
     ms_per_step = total_ms / K
-    tokens = s.T * K * world
-    value = tokens / (total_ms / 1e3)
 
     # per-kernel durations (each kernel alone, events between kernels) for the roofline
     mla_prolog_timing_enable(True)
