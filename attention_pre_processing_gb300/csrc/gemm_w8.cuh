@@ -8,16 +8,16 @@
 // rather than bf16 because a byte fits its 10-bit mantissa: placing the biased byte under the
 // exponent of 1024 (one byte permute) and subtracting 1152 (one paired half subtraction) widens
 // two weights, where int-to-float conversions run at a quarter of the ALU rate and were the
-// bottleneck (0.8 us per 12 KB stage, measured).  Widening
-// the weights in global memory first would move three bytes per weight through HBM more than
-// needed; here the int8 tile crosses HBM once:
-//   warp 0      TMA producer: A tiles (128-byte swizzle) and int8 weight tiles (BN rows x 64 k,
-//               plain rows of 64 bytes) into a ring of stages
+// bottleneck (0.8 us per 12 KB stage, measured).  Widening the weights in global memory first
+// would move three bytes per weight through HBM more than needed; here the int8 tile crosses HBM
+// once:
+//   warp 0      TMA producer: per stage, kW8Kb k-blocks of A tiles (128-byte swizzle) and one
+//               int8 weight box of BN rows x 64 * kW8Kb k (plain rows)
 //   warp 1      TMEM allocation and the tcgen05.mma issuer (B K-major, 128-byte swizzle)
 //   warps 2-5   epilogue: TMEM -> fp32 k-range slots (split-K), as gemm_tc's EPI_F32
-//   warps 6-13  converters: each 16-byte int8 chunk of a weight row -> two 16-byte fp16 chunks
-//               of the K-major swizzled B tile (chunk c of row r at (c ^ (r % 8)) * 16), then a
-//               proxy fence and an arrival on the stage's "B ready" barrier
+//   warps 6-13  converters: per k-block, each 16-byte int8 chunk of a weight row -> two 16-byte
+//               fp16 chunks of the K-major swizzled B slot (chunk c of row r at (c ^ (r % 8)) * 16),
+//               then a proxy fence and an arrival on the slot's "B full" barrier
 // The int8 and A tiles run in a deep ring of stages (the weight stream's latency hiding); the
 // fp16 B tiles in a ring of two slots only (the converters stay at most one k-block ahead of the
 // tensor core), so that the shared memory goes to int8 stages in flight.  Stage s is reused only
