@@ -154,11 +154,12 @@ PpPlan pp_plan(const PpDims& d, int sms) {
     plan_gemm(p.g1, T, p.n1, d.He, sms, T <= 128 ? 64 : 192, true);
     // the up-projection: 192-column tiles, whole K
     plan_gemm(p.g2, T, p.n2, d.Hcq, sms, 192, false);
-    // W^UK: per head two 256-column tiles of 128 rows
-    p.g3.bn = 256;
-    p.g3.kblocks = (int)((d.D + kBK - 1) / kBK);
-    p.g3.n_tiles = (int)(d.N * 2);
+    // W^UK: up to 128 tokens one 512-column tile per head (N tiles: one wave on the SMs for
+    // N <= 152), above that two 256-column tiles per head and row tile
     p.g3.m_tiles = (int)((T + 127) / 128);
+    p.g3.bn = p.g3.m_tiles == 1 ? 512 : 256;
+    p.g3.kblocks = (int)((d.D + kBK - 1) / kBK);
+    p.g3.n_tiles = (int)(d.N * (512 / p.g3.bn));
     p.g3.msub = 1;
     p.g3.a_box_rows = T < 128 ? (int)((T + 7) / 8 * 8) : 128;
     const long long tiles = (long long)p.g3.m_tiles * p.g3.n_tiles;
@@ -302,7 +303,7 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
     const int64_t q_ld = d.mode == 0 ? d.Hckv + d.Dr : d.Hckv;
     GemmArgs g3 = gemm_args(p.g3, T, d.Hckv, status);
     g3.head_mode = 1;
-    g3.tiles_per_head = 2;
+    g3.tiles_per_head = 512 / p.g3.bn;
     g3.N = (int)d.N;
     g3.Hckv = (int)d.Hckv;
     g3.q_ld = (int)q_ld;
@@ -315,7 +316,8 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
         const uint32_t box[2] = {64, 32};
         g3.tma_out = encode_map(&mO3, a.qout->data, 2, dims, strides, box, tdt) ? 1 : 0;
     }
-    e = p.kps3 ? launch_gemm<256, 1, 8, EPI_QN, 2, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr)
+    e = p.g3.bn == 512 ? launch_gemm<512, 1, 4, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr)
+        : p.kps3 ? launch_gemm<256, 1, 8, EPI_QN, 2, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr)
                : launch_gemm<256, 1, 8, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "pp_absorb_uk");
