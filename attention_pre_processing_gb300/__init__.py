@@ -18,7 +18,7 @@ __all__ = [
     "mla_prolog_device_status", "mla_prolog_status_string", "STATUS", "DEV_CACHE_INDEX_RANGE",
     "DEV_WAIT_TIMEOUT", "library_path", "mla_prolog_timing_enable", "mla_prolog_timing_read",
     "mla_prolog_no_alloc", "NO_ALLOC_SCRATCH_BYTES", "PP_TENSOR_ARGS", "PP_OUTPUT_ARGS",
-    "mla_preprocess_workspace_size", "mla_preprocess",
+    "mla_preprocess_workspace_size", "mla_preprocess", "mla_prolog_debug_wait_probe",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -83,6 +83,8 @@ def lib():
         L.mla_prolog_device_status.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
                                                ctypes.POINTER(ctypes.c_uint32)]
         L.mla_prolog_device_status.restype = ctypes.c_int
+        L.mla_prolog_debug_wait_probe.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p]
+        L.mla_prolog_debug_wait_probe.restype = ctypes.c_int
         L.mla_prolog_timing_enable.argtypes = [ctypes.c_int]
         L.mla_prolog_timing_enable.restype = ctypes.c_int
         L.mla_prolog_timing_read.argtypes = [ctypes.POINTER(MlaKernelTime), ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
@@ -205,6 +207,21 @@ def mla_prolog_device_status(workspace, workspace_bytes: Optional[int] = None, s
     if rc != 0:
         raise MlaError(rc, "mla_prolog_device_status")
     return int(bits.value)
+
+
+def mla_prolog_debug_wait_probe(workspace, which: int, workspace_bytes: Optional[int] = None, stream=None) -> None:
+    """Enqueue the failure-detection probe (a wait nothing satisfies; see mla_prolog.h)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().mla_prolog_debug_wait_probe(ctypes.c_void_p(_ptr(workspace)), ctypes.c_uint64(workspace_bytes),
+                                           int(which), ctypes.c_void_p(stream))
+    if rc != 0:
+        raise MlaError(rc, "mla_prolog_debug_wait_probe")
 
 
 def mla_prolog_timing_enable(enable: bool) -> None:

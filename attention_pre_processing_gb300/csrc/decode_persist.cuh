@@ -180,6 +180,30 @@ __device__ __forceinline__ bool wait_tiles(const unsigned long long* zf, const u
     return !bad;
 }
 
+// Diagnostic: two waits that nothing can satisfy, so that the time limit, the status bit and the
+// clean return can be tested without a fault.  which == 0: the persistent kernel's flag wait
+// (wait_tiles, limit kWaitLimitNs) on a flag that never holds the tag ~0; which == 1: an
+// mbarrier wait (limit 10 ms) on a barrier nothing arrives on.  One CTA of 128 threads.
+__global__ void __launch_bounds__(128) wait_probe_kernel(const unsigned long long* flag, uint32_t* status, int which) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_abort_v;
+    const int etid = threadIdx.x;
+    if (etid == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        s_abort_v = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    bool ok = true;
+    if (which == 0) {
+        ok = wait_tiles(flag, nullptr, 0, 1, 0u, ~0ull, &s_abort_v, etid);
+    } else {
+        if (etid == 0) ok = mbar_wait(smem_u32(&bar), 0, &s_abort_v, 10000000ull);
+        ok = !epi_any(!ok);
+    }
+    if (!ok && etid == 0) atomicOr(status, kStatusWaitTimeout);
+}
+
 // ------------------------------------------------------------------ helpers
 
 // 32 values of row `row` (columns col0..col0+31 of a head's q^C) -> bf16 into the K-major,

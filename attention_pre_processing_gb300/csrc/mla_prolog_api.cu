@@ -1173,6 +1173,19 @@ extern "C" mla_status mla_prolog_device_status(const void* workspace, uint64_t w
     return MLA_OK;
 }
 
+extern "C" mla_status mla_prolog_debug_wait_probe(void* workspace, uint64_t workspaceSize, int which, void* stream) {
+    if (workspace == nullptr) return MLA_ERR_PARAM_NULLPTR;
+    if (workspaceSize < kStatusBytes || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0 || (which != 0 && which != 1))
+        return MLA_ERR_PARAM_INVALID;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the status word cleared, and the flag (bytes 8..15) zero: it never holds the probe's tag
+    if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess) return MLA_ERR_RUNTIME;
+    wait_probe_kernel<<<1, 128, 0, st>>>(reinterpret_cast<const unsigned long long*>(ws + 8),
+                                         reinterpret_cast<uint32_t*>(ws), which);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_RUNTIME;
+}
+
 extern "C" mla_status mla_prolog_timing_enable(int enable) {
     std::lock_guard<std::mutex> lk(g_timing_mu);
     g_timing.enabled = enable != 0;

@@ -186,6 +186,18 @@ MLA_API mla_status mla_prolog_device_status(const void* workspace, uint64_t work
                                     uint32_t* bits);
 
 /*
+ * Diagnostic for failure detection, no counterpart on the pages: enqueues on `stream` one small
+ * kernel whose wait nothing can satisfy -- which = 0: the flag wait of the persistent decode
+ * kernel on a flag that never holds its tag (limit 2 s); which = 1: an mbarrier wait that
+ * nothing arrives on (limit 10 ms).  The wait gives up at its limit, the kernel sets
+ * MLA_DEV_WAIT_TIMEOUT in the workspace's status word (cleared first) and returns, so the
+ * context stays usable; mla_prolog_device_status() then reads the bit.  Needs a workspace of at
+ * least 1 KB (16-byte aligned).  Returns 161001 for a NULL workspace, 161002 for a short or
+ * misaligned workspace or another `which`, 361001 if the launch fails.
+ */
+MLA_API mla_status mla_prolog_debug_wait_probe(void* workspace, uint64_t workspaceSize, int which, void* stream);
+
+/*
  * Per-kernel timing, a diagnostic with no counterpart on the pages.  While enabled
  * (process-wide, from the next mla_prolog() call on), each call records a CUDA event on
  * its stream before its first kernel and after every kernel, and launches the kernels
