@@ -243,3 +243,13 @@ def test_preprocess_tiling_rules(lib):
     t = pp()
     t["input"].data = t["input"].data + 2
     assert pp_code(t) == 161002
+
+
+def test_wait_probe_argument_checks(lib):
+    import ctypes
+    L = lib
+    addr = ctypes.c_void_p(0x200000)   # never dereferenced: every case is rejected first
+    assert L.mla_prolog_debug_wait_probe(None, 1024, 0, None) == 161001
+    assert L.mla_prolog_debug_wait_probe(addr, 512, 0, None) == 161002      # shorter than the status word
+    assert L.mla_prolog_debug_wait_probe(addr, 1024, 2, None) == 161002     # no such probe
+    assert L.mla_prolog_debug_wait_probe(ctypes.c_void_p(0x200008), 1024, 0, None) == 161002   # misaligned
