@@ -43,6 +43,7 @@ constexpr int kW8Threads = 64 + 128 + kW8Conv;
 // k-blocks of 64 per int8 stage: one TMA box of 64 * kW8Kb bytes per weight row.  The TMA
 // engine moves a box row by row, at a per-SM rate of rows, so longer rows move more bytes.
 constexpr int kW8Kb = 2;
+static_assert(kW8Kb >= 1 && kW8Kb <= 4, "a TMA box row holds at most 256 elements");
 
 template <int BN, int MSUB, int MAXST>
 struct W8Cfg {
