@@ -335,3 +335,107 @@ def test_kv_int8_cache_quantiser():
     kv = res["kv_cache"].reshape(-1, s.Hckv)
     for t, slot in enumerate(oracle._np(inp["cache_index"]).tolist()):
         assert np.array_equal(kv[slot], oracle.round_i8(res["c_kv"][t] * qs))
+
+
+# ------------------------------------------- partial quantisation: smoothScalesCq
+
+class _HandDims:
+    T, He, Hcq, N, D, Dr, Hckv, block_num, block_size = 1, 4, 6, 1, 2, 4, 2, 1, 4
+
+
+def _hand_inputs(y_q, gamma_cq, y_kvkr, gamma_ckv, cos, sin, kv_int8=False, kr_int8=False):
+    """One token whose down-projections are row 0 of the weights: x = (1, 0, 0, 0).
+
+    The other weight rows hold a non-zero filler, so a slip that reads them shows.
+    """
+    d = _HandDims
+    w_dq = np.full((d.He, d.Hcq), 7.0)
+    w_dq[0] = y_q
+    w_dkvkr = np.full((d.He, d.Hckv + d.Dr), -5.0)
+    w_dkvkr[0] = y_kvkr
+    bf = lambda a: torch.tensor(np.asarray(a, dtype=np.float64)).to(torch.bfloat16)
+    kv_dt = torch.int8 if kv_int8 else torch.bfloat16
+    kr_dt = torch.int8 if kr_int8 else torch.bfloat16
+    return {
+        "x": bf([[1.0, 0.0, 0.0, 0.0]]),
+        "w_dq": bf(w_dq),
+        "w_uqqr": torch.eye(d.Hcq, d.N * (d.D + d.Dr), dtype=torch.int8),
+        "w_uk": bf(np.ones((d.N, d.D, d.Hckv))),
+        "w_dkvkr": bf(w_dkvkr),
+        "gamma_cq": bf(gamma_cq),
+        "gamma_ckv": bf(gamma_ckv),
+        "rope_cos": bf([cos]),
+        "rope_sin": bf([sin]),
+        "cache_index": torch.tensor([2], dtype=torch.int64),
+        "kv_cache": torch.zeros((d.block_num, d.block_size, 1, d.Hckv), dtype=kv_dt),
+        "kr_cache": torch.zeros((d.block_num, d.block_size, 1, d.Dr), dtype=kr_dt),
+        "dequant_scale_w_uqqr": torch.ones((1, d.N * (d.D + d.Dr)), dtype=torch.float32),
+    }
+
+
+def test_smooth_scales_golden_row():
+    g = read_golden("smooth_quant_row.txt")
+    inp = _hand_inputs(g["y"], g["gamma"], [1, -1, 1, 2, 3, 4], [1, 1], [1, 1, 1, 1], [0, 0, 0, 0])
+    inp["smooth_scales_cq"] = torch.tensor([g["smooth"]], dtype=torch.float32)
+    res = oracle.prolog(inp, dims=_HandDims, eps_cq=0.0, eps_ckv=0.0, uqqr_int8=True)
+    assert res["c_q"][0].tolist() == g["c_q"]
+    assert res["c_q_scale"][0] == g["scale"][0]
+    assert res["c_q_i8"][0].tolist() == [int(c) for c in g["codes"]]
+    assert res["q_c"][0, 0].tolist() == g["q_c"]
+
+
+def _tiny_partial():
+    cfg = workloads.config("tiny", uqqr_int8=True)
+    return cfg, dict(workloads.make_inputs(cfg))
+
+
+def test_smooth_scales_uniform_power_of_two():
+    """A uniform smooth of 2^k scales u by 2^k exactly: the codes stay, the per-token scale
+    and the dequantised up-projection are multiplied by 2^k exactly."""
+    cfg, inp = _tiny_partial()
+    base = oracle_for(cfg, inp)
+    for k in (3, -2):
+        inp["smooth_scales_cq"] = torch.full((1, cfg.shape.Hcq), 2.0 ** k, dtype=torch.float32)
+        res = oracle_for(cfg, inp)
+        assert np.array_equal(res["c_q_i8"], base["c_q_i8"])
+        assert np.array_equal(res["c_q_scale"], base["c_q_scale"] * 2.0 ** k)
+        assert np.array_equal(res["q_c"], base["q_c"] * 2.0 ** k)
+        assert np.array_equal(res["c_q"], base["c_q"])
+
+
+def test_smooth_scales_one_hot_moves_the_argmax():
+    """smooth = e_j keeps only element j of c^Q: its code is +-127, every other code is 0 and
+    the scale is |c^Q_j| / 127, whatever element of c^Q is the largest."""
+    cfg, inp = _tiny_partial()
+    base = oracle_for(cfg, inp)
+    Hcq = cfg.shape.Hcq
+    for j in (5, Hcq - 1):
+        # j is not the largest element of c^Q in these tokens, so the smooth moves the argmax
+        assert sum(int(np.argmax(np.abs(base["c_q"][t]))) != j for t in range(cfg.shape.T)) >= cfg.shape.T - 1
+        e = torch.zeros((1, Hcq), dtype=torch.float32)
+        e[0, j] = 1.0
+        inp["smooth_scales_cq"] = e
+        res = oracle_for(cfg, inp)
+        for t in range(cfg.shape.T):
+            want = np.zeros(Hcq, dtype=np.int8)
+            want[j] = 127 if base["c_q"][t, j] > 0 else -127
+            assert np.array_equal(res["c_q_i8"][t], want)
+            assert res["c_q_scale"][t] == abs(base["c_q"][t, j]) / 127.0
+
+
+# ----------------------------------------------------- int8 kv and kr caches
+
+def test_int8_cache_rows_golden():
+    g = read_golden("int8_cache_rows.txt")
+    inp = _hand_inputs([3, -3, 3, -3, 3, -3], [1] * 6, g["ykv"] + g["ykr"], g["gamma_ckv"],
+                       g["cos"], g["sin"], kv_int8=True, kr_int8=True)
+    inp["quant_scale_ckv"] = torch.tensor([g["qs_ckv"]], dtype=torch.float32)
+    inp["quant_scale_ckr"] = torch.tensor([g["qs_ckr"]], dtype=torch.float32)
+    res = oracle.prolog(inp, dims=_HandDims, eps_cq=0.0, eps_ckv=0.0, uqqr_int8=True,
+                        kv_int8=True, kr_int8=True)
+    kv = res["kv_cache"].reshape(-1, _HandDims.Hckv)
+    kr = res["kr_cache"].reshape(-1, _HandDims.Dr)
+    assert kv[2].tolist() == [int(c) for c in g["kv_codes"]]
+    assert kr[2].tolist() == [int(c) for c in g["kr_codes"]]
+    # every other slot keeps its (zero) contents
+    assert not kv[[0, 1, 3]].any() and not kr[[0, 1, 3]].any()
