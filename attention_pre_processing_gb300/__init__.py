@@ -17,7 +17,7 @@ __all__ = [
     "MlaError", "TENSOR_ARGS", "lib", "mla_prolog_workspace_size", "mla_prolog",
     "mla_prolog_device_status", "mla_prolog_status_string", "STATUS", "DEV_CACHE_INDEX_RANGE",
     "DEV_WAIT_TIMEOUT", "library_path", "mla_prolog_timing_enable", "mla_prolog_timing_read",
-    "mla_prolog_no_alloc", "NO_ALLOC_SCRATCH_BYTES", "PP_TENSOR_ARGS", "PP_OUTPUT_ARGS",
+    "mla_prolog_no_alloc", "mla_prolog_no_alloc_status", "NO_ALLOC_SCRATCH_BYTES", "PP_TENSOR_ARGS", "PP_OUTPUT_ARGS",
     "mla_preprocess_workspace_size", "mla_preprocess", "mla_prolog_debug_wait_probe",
 ]
 
@@ -82,6 +82,8 @@ def lib():
         L.mla_prolog_no_alloc.restype = ctypes.c_int
         L.mla_prolog_device_status.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
                                                ctypes.POINTER(ctypes.c_uint32)]
+        L.mla_prolog_no_alloc_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+        L.mla_prolog_no_alloc_status.restype = ctypes.c_int
         L.mla_prolog_device_status.restype = ctypes.c_int
         L.mla_prolog_debug_wait_probe.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p]
         L.mla_prolog_debug_wait_probe.restype = ctypes.c_int
@@ -190,6 +192,21 @@ def mla_prolog_no_alloc(tensors: Dict, eps_cq: float, eps_ckv: float, stream=Non
     if check and rc != 0:
         raise MlaError(rc, "mla_prolog_no_alloc")
     return rc
+
+
+def mla_prolog_no_alloc_status(stream=None) -> int:
+    """Wait for the stream and return the device status bits of the last mla_prolog_no_alloc
+    call on the current device (read from the library's scratch buffer)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    bits = ctypes.c_uint32(0)
+    rc = lib().mla_prolog_no_alloc_status(ctypes.c_void_p(stream), ctypes.byref(bits))
+    if rc != 0:
+        raise MlaError(rc, "mla_prolog_no_alloc_status")
+    return int(bits.value)
 
 
 def mla_prolog_device_status(workspace, workspace_bytes: Optional[int] = None, stream=None) -> int:

@@ -1126,16 +1126,52 @@ static __device__ __align__(256) uint8_t g_no_alloc_scratch[MLA_NO_ALLOC_SCRATCH
 static constexpr int kMaxDevices = 64;
 static std::mutex g_scratch_mu;
 static void* g_scratch_addr[kMaxDevices] = {};
+static unsigned long long g_scratch_ctx[kMaxDevices] = {};   // id of the context the address belongs to
 
-// Device address of the scratch buffer on the current device (looked up on first use).
+// The unique id of the calling thread's current CUDA context (driver entry points, looked up
+// once); false when there is no current context or the driver does not offer the calls.
+typedef CUresult (*PFN_ctx_current)(CUcontext*);
+typedef CUresult (*PFN_ctx_id)(CUcontext, unsigned long long*);
+static PFN_ctx_current g_ctx_current = nullptr;
+static PFN_ctx_id g_ctx_id = nullptr;
+static std::once_flag g_ctx_once;
+
+static bool current_context_id(unsigned long long* id) {
+    std::call_once(g_ctx_once, [] {
+        void* f1 = nullptr;
+        void* f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+            q2 == cudaDriverEntryPointSuccess) {
+            g_ctx_current = reinterpret_cast<PFN_ctx_current>(f1);
+            g_ctx_id = reinterpret_cast<PFN_ctx_id>(f2);
+        }
+    });
+    if (g_ctx_current == nullptr || g_ctx_id == nullptr) return false;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch buffer on the current device.  Looked up on the first call on
+// a device, and again whenever the current context is not the one the address was found in
+// (after cudaDeviceReset the module is loaded anew and the buffer may move).  Without the
+// context-id calls the address is looked up on every call.
 static mla_status no_alloc_scratch(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_RUNTIME;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    if (g_scratch_addr[dev] == nullptr || !have_id || g_scratch_ctx[dev] != id) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_RUNTIME;
         g_scratch_addr[dev] = p;
+        // the lookup made the device's primary context current if no context was
+        unsigned long long id2 = 0;
+        g_scratch_ctx[dev] = current_context_id(&id2) ? id2 : 0;
     }
     *out = g_scratch_addr[dev];
     return MLA_OK;
@@ -1161,6 +1197,16 @@ extern "C" mla_status mla_prolog_no_alloc(MLA_TENSOR_PARAMS, void* stream) {
     Launched L{&a, d, sc, plan, static_cast<uint8_t*>(ws), st, sms};
     timing_begin(L.st);
     return run(L);
+}
+
+extern "C" mla_status mla_prolog_no_alloc_status(void* stream, uint32_t* bits) {
+    if (bits == nullptr) return MLA_ERR_PARAM_NULLPTR;
+    void* ws = nullptr;
+    const mla_status ss = no_alloc_scratch(&ws);
+    if (ss != MLA_OK) return ss;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_RUNTIME;
+    if (cudaMemcpy(bits, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_RUNTIME;
+    return MLA_OK;
 }
 
 extern "C" mla_status mla_prolog_device_status(const void* workspace, uint64_t workspaceSize, void* stream,

@@ -59,7 +59,10 @@ struct Half16<true> {
     }
 };
 
-// Error-free float transformations: s + e == a + b and p + e == a * b exactly.
+// Error-free float transformations: s + e == a + b and p + e == a * b exactly.  two_sum is
+// Knuth's branch-free TwoSum (The Art of Computer Programming, vol. 2, section 4.2.2); two_prod
+// forms the product's rounding error with one fused multiply-add (the FMA form of Dekker's
+// exact product).
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     s = __fadd_rn(a, b);
     const float bb = __fsub_rn(s, a);
@@ -69,7 +72,9 @@ __device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
     p = __fmul_rn(a, b);
     e = fmaf(a, b, -p);
 }
-// Float pairs (hi + lo, |lo| <= ulp(hi) / 2) carry ~48 significant bits.
+// Float pairs (hi + lo, |lo| <= ulp(hi) / 2) carry ~48 significant bits: the double-length
+// arithmetic of Dekker ("A floating-point technique for extending the available precision",
+// Numerische Mathematik 18, 1971), with quotient and square root corrected by one residual step.
 __device__ __forceinline__ void ff_norm(float& hi, float& lo) {
     const float s = __fadd_rn(hi, lo);
     lo = __fsub_rn(lo, __fsub_rn(s, hi));

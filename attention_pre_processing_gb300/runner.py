@@ -19,18 +19,33 @@ INPUT_KEYS = ("x", "w_dq", "w_uqqr", "w_uk", "w_dkvkr", "gamma_cq", "gamma_ckv",
 
 
 class PrologCall:
-    """One configured call: device tensors, outputs and workspace, reusable across launches."""
+    """One configured call: device tensors, outputs and workspace, reusable across launches.
 
-    def __init__(self, cfg: MlaConfig, inputs: Dict[str, Optional[torch.Tensor]], device="cuda"):
+    With ``bs = (B, S)`` (B * S = T) the per-token tensors are passed in the page's
+    non-concatenated layout: tokenX (B, S, He), ropeSin / ropeCos (B, S, Dr), cacheIndex (B, S),
+    queryOut (B, S, N, Hckv), queryRopeOut (B, S, N, Dr) and dequantScaleQNopeOut (B*S, N, 1).
+    """
+
+    def __init__(self, cfg: MlaConfig, inputs: Dict[str, Optional[torch.Tensor]], device="cuda", bs=None):
         s = cfg.shape
         self.cfg = cfg
         self.t: Dict[str, Optional[torch.Tensor]] = {}
         for k in INPUT_KEYS:
             v = inputs.get(k)
             self.t[k] = None if v is None else v.to(device).contiguous()
+        lead = (s.T,)
+        if bs is not None:
+            B, S = bs
+            if B * S != s.T:
+                raise ValueError(f"B * S = {B * S} != T = {s.T}")
+            lead = (B, S)
+            self.t["x"] = self.t["x"].view(B, S, s.He)
+            self.t["rope_sin"] = self.t["rope_sin"].view(B, S, s.Dr)
+            self.t["rope_cos"] = self.t["rope_cos"].view(B, S, s.Dr)
+            self.t["cache_index"] = self.t["cache_index"].view(B, S)
         q_dtype = torch.int8 if cfg.q_int8 else torch.bfloat16
-        self.t["q_out"] = torch.empty((s.T, s.N, s.Hckv), dtype=q_dtype, device=device)
-        self.t["q_rope_out"] = torch.empty((s.T, s.N, s.Dr), dtype=torch.bfloat16, device=device)
+        self.t["q_out"] = torch.empty(lead + (s.N, s.Hckv), dtype=q_dtype, device=device)
+        self.t["q_rope_out"] = torch.empty(lead + (s.N, s.Dr), dtype=torch.bfloat16, device=device)
         self.t["dequant_scale_q_nope_out"] = (torch.empty((s.T, s.N, 1), dtype=torch.float32, device=device)
                                               if cfg.q_int8 else None)
         self.ws_bytes = mla_prolog_workspace_size(self.t, cfg.eps_cq, cfg.eps_ckv)

@@ -52,6 +52,16 @@ def step_bytes(s, q_int8=False):
     return W * 2 + (s.Hcq + s.Hckv) * 2 + s.T * per_tok
 
 
+def int8_step_bytes(s, kv_int8=True):
+    """Algorithmic bytes of one int8-input call (int8 tokenX and weights W^DQ, W^UqQr, W^DkvKr at
+    one byte, W^UK bf16, fp32 scales, int8 queryOut with its (T, N, 1) scales, int8 kv rows)."""
+    w8 = s.He * (s.Hcq + s.Hckv + s.Dr) + s.Hcq * s.N * (s.D + s.Dr)
+    vectors = (s.Hcq + s.N * (s.D + s.Dr) + s.Hckv + s.Dr + s.Hckv) * 4 + (s.Hcq + s.Hckv) * 2
+    per_tok = (s.He + 4 + 2 * s.Dr * 2 + 8 + s.N * s.Hckv + s.N * 4 + s.N * s.Dr * 2
+               + s.Hckv * (1 if kv_int8 else 2) + s.Dr * 2)
+    return w8 + s.N * s.D * s.Hckv * 2 + vectors + s.T * per_tok
+
+
 def k2_bytes(s):
     """Up-projection c^Q . W^UqQr: the weight, c^Q in, q^C and q^R out (bf16)."""
     return s.Hcq * s.N * (s.D + s.Dr) * 2 + s.T * s.Hcq * 2 + s.T * s.N * (s.D + s.Dr) * 2
@@ -211,6 +221,10 @@ def run_cuda(args, rank, world):
         raise RuntimeError("device status bits set during the timed region")
     total_ms, value = job_rate(sum(step_ms), s.T * K, world, dist, dev)
     ms_per_step = total_ms / K
+    # the distribution over more calls: cold L2 (flushed before each call) and hot L2 (back to
+    # back: the 128 MB of weights mostly stay in the 129 MB L2 between calls)
+    dist_cold = _call_stats(call, stream, dev, 200, flush_l2)
+    dist_hot = _call_stats(call, stream, dev, 200, None)
 
     # per-kernel durations (each kernel alone, events between kernels) for the roofline
     mla_prolog_timing_enable(True)
@@ -253,9 +267,22 @@ def run_cuda(args, rank, world):
     if not args.skip_preprocess:
         pre = _preprocess(dev, stream, flush_l2, peaks, max(3, min(K, 20)))
 
+    # the other two DeepSeek-V3-shaped configurations: T = 256 with the int8 q^N output, and
+    # int8 inputs at T = 64
+    others = {}
+    if not args.skip_others:
+        for name, nbytes in (("decode_t256_qint8", lambda c: step_bytes(c.shape, q_int8=True)),
+                             ("int8_t64", lambda c: int8_step_bytes(c.shape))):
+            others[name] = _other(name, nbytes, dev, stream, flush_l2, peaks, max(3, min(K, 50)))
+
     cpu = None
+    cpu_1t = None
     if rank == 0 and not args.skip_cpu:
         cpu = cpu_baseline(cfg, inp, budget_s=args.cpu_budget)
+        cpu_1t = {}
+        for name in ("tiny", "decode_t32", "decode_t256_qint8", "int8_t64"):
+            c = workloads.config(name)
+            cpu_1t[name] = cpu_baseline(c, workloads.make_inputs(c), budget_s=2.0, threads=1)
 
     if rank == 0:
         line = {
@@ -271,12 +298,71 @@ def run_cuda(args, rank, world):
                        "timing": "CUDA events around each mla_prolog call on its stream"},
             "roofline": roofline, "step_roofline": step_roof, "kernels_ms": kern_ms,
             "gpu_launches": kernels_per_step * K,
+            "us_per_call_mean": statistics.mean(step_ms) * 1e3,
+            "us_per_call_median": statistics.median(step_ms) * 1e3,
+            "calls_200_cold_l2": dist_cold, "calls_200_hot_l2": dist_hot,
             "clocks": clk.summary(), "e2e": e2e, "wall_s_timed": t_wall,
-            "cpu_baseline": cpu, "prefill": prefill, "preprocess": pre,
+            "cpu_baseline": cpu, "cpu_oracle_1_thread": cpu_1t, "prefill": prefill, "preprocess": pre,
+            "other_configs": others,
         }
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
+
+
+def _call_stats(call, stream, dev, n, flush_l2):
+    """µs per call over n event-timed calls: median, mean, 10th and 90th percentile.  With
+    flush_l2 the L2 is flushed before each call (outside the events); without it the calls run
+    back to back with whatever the previous call left in L2 (labelled hot L2)."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        if flush_l2 is not None:
+            flush_l2()
+        starts[i].record(stream)
+        call(stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in zip(starts, ends))
+    return {"calls": n, "l2": "flushed before each call" if flush_l2 is not None else "hot (no flush)",
+            "us_median": statistics.median(us), "us_mean": statistics.mean(us),
+            "us_p10": us[n // 10], "us_p90": us[(9 * n) // 10],
+            "tokens_per_s_median": call.cfg.shape.T / (statistics.median(us) / 1e6)}
+
+
+def _other(name, nbytes, dev, stream, flush_l2, peaks, K):
+    """One more configuration beside the headline: µs per call (cold L2), tokens/s, algorithmic
+    bytes against the measured HBM bandwidth, and each kernel's own duration."""
+    import torch
+    from attention_pre_processing_gb300 import workloads, mla_prolog_timing_enable, mla_prolog_timing_read
+    from attention_pre_processing_gb300.runner import PrologCall
+    cfg = workloads.config(name)
+    call = PrologCall(cfg, workloads.make_inputs(cfg), device=dev)
+    for _ in range(3):
+        flush_l2()
+        call(stream)
+    st = _call_stats(call, stream, dev, K, flush_l2)
+    mla_prolog_timing_enable(True)
+    per = {}
+    for _ in range(min(K, 10)):
+        flush_l2()
+        call(stream)
+        for kname, t in mla_prolog_timing_read():
+            per.setdefault(kname, []).append(t)
+    mla_prolog_timing_enable(False)
+    kern = {k: statistics.mean(v) for k, v in per.items()}
+    b = nbytes(cfg)
+    ok = call.status(stream) == 0
+    del call
+    torch.cuda.empty_cache()
+    ms = st["us_median"] / 1e3
+    return {"workload": cfg.workload, "us_per_call_median": st["us_median"], "us_per_call_mean": st["us_mean"],
+            "tokens_per_s": cfg.shape.T / (ms / 1e3), "algorithmic_bytes": b,
+            "achieved_gbs": b / (ms / 1e3) / 1e9, "frac_of_measured_hbm": b / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "kernels_ms": kern, "launches_per_call": len(kern), "status_clean": ok,
+            "traffic": _read_traffic(max(kern, key=kern.get), name) if kern else None,
+            "dominant_kernel": max(kern, key=kern.get) if kern else None}
 
 
 def _read_traffic(kernel, workload):
@@ -419,8 +505,9 @@ def _preprocess(dev, stream, flush_l2, peaks, K):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def cpu_baseline(cfg, inp, budget_s=12.0, steps=None):
-    """Times the oracle on growing token samples until ~budget_s of CPU work."""
+def cpu_baseline(cfg, inp, budget_s=12.0, steps=None, threads=None):
+    """Times the oracle on growing token samples until ~budget_s of CPU work, on all host
+    cores (or on `threads` threads)."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
     from attention_pre_processing_gb300 import workloads
@@ -432,14 +519,16 @@ def cpu_baseline(cfg, inp, budget_s=12.0, steps=None):
     for k in ("T", "He", "Hcq", "N", "D", "Dr", "Hckv", "block_num", "block_size"):
         setattr(d, k, getattr(cfg.shape, k))
     oracle.build()
-    threads = oracle.max_threads()
+    if threads is None:
+        threads = os.cpu_count() or oracle.max_threads()
     done, elapsed, n = 0, 0.0, max(1, threads)
     while elapsed < budget_s:
         tok = (workloads.sample_tokens(cfg.shape.T, n, seed=done + 1) if n < cfg.shape.T
                else list(range(cfg.shape.T)))
         t0 = time.perf_counter()
         oracle.prolog(inp, dims=d, eps_cq=cfg.eps_cq, eps_ckv=cfg.eps_ckv, x_int8=cfg.x_int8,
-                      kv_int8=cfg.kv_int8, q_int8=cfg.q_int8, tokens=tok, with_intermediates=False)
+                      uqqr_int8=cfg.x_int8 or cfg.uqqr_int8, kv_int8=cfg.kv_int8, kr_int8=cfg.kr_int8,
+                      q_int8=cfg.q_int8, tokens=tok, with_intermediates=False, num_threads=threads)
         elapsed += time.perf_counter() - t0
         done += len(tok)
         n = min(n * 2, cfg.shape.T)
@@ -505,6 +594,7 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-preprocess", action="store_true", help="skip the aclnnMlaPreprocess variant's line")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-others", action="store_true", help="skip the T=256 int8-q^N and int8-input lines")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--kernels-only", action="store_true", help="only warmup+steps calls of --workload")
     ap.add_argument("--workload", default=HEADLINE)

@@ -235,14 +235,16 @@ MLA_API mla_status mla_prolog_timing_read(mla_kernel_time* out, int capacity, in
  * - No allocation: the call makes no cudaMalloc / cudaFree and no allocating library call.
  *   The first call on each device looks up the scratch buffer's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call before any
- *   stream capture on the device.
+ *   stream capture on the device.  The address is tied to the CUDA context it was found in:
+ *   after cudaDeviceReset (or when another context is current) the next call looks it up
+ *   again, so that call too belongs before any capture.
  * - Sharing: every call on a device uses the same scratch buffer, which keeps the previous
  *   call's contents.  The call clears the part that must start at zero (the status word)
  *   on `stream` before its kernels run.  Calls whose kernels overlap on the GPU (other
  *   streams, or other host threads) race on the scratch buffer and give wrong results:
  *   order them on one stream or with events.
- * - The device status word lives in the scratch buffer and is not exposed; out-of-range
- *   cacheIndex rows are still skipped.
+ * - The device status word (out-of-range cacheIndex rows, which are skipped, and pipeline
+ *   waits that gave up) lives in the scratch buffer; mla_prolog_no_alloc_status() reads it.
  *
  * Returns the codes of mla_prolog(), plus MLA_ERR_SCRATCH_LIMIT, and 361001 if the scratch
  * buffer's address cannot be obtained.
@@ -262,6 +264,15 @@ MLA_API mla_status mla_prolog_no_alloc(
     double rmsnormEpsilonCq, double rmsnormEpsilonCkv, const char* cacheMode,
     const mla_tensor* queryOut, const mla_tensor* queryRopeOut,
     const mla_tensor* dequantScaleQNopeOut, void* stream);
+
+/*
+ * The device status bits (MLA_DEV_* flags) of the last mla_prolog_no_alloc() call on the
+ * current device: waits for `stream`, then copies the status word out of the library's
+ * scratch buffer into *bits.  No allocation.  Like the buffer itself, the word belongs to
+ * whichever call ran last; read it before the next call.  Returns 161001 for a NULL `bits`,
+ * 361001 if a CUDA call fails.
+ */
+MLA_API mla_status mla_prolog_no_alloc_status(void* stream, uint32_t* bits);
 
 /* A constant, human-readable name for a return code. */
 MLA_API const char* mla_prolog_status_string(mla_status status);

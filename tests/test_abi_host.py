@@ -253,3 +253,34 @@ def test_wait_probe_argument_checks(lib):
     assert L.mla_prolog_debug_wait_probe(addr, 512, 0, None) == 161002      # shorter than the status word
     assert L.mla_prolog_debug_wait_probe(addr, 1024, 2, None) == 161002     # no such probe
     assert L.mla_prolog_debug_wait_probe(ctypes.c_void_p(0x200008), 1024, 0, None) == 161002   # misaligned
+
+
+# ------------------------------------------------ the no-allocation entry point
+
+def no_alloc_code(tensors, eps=1e-5, mode="PA_BSND"):
+    return mla.mla_prolog_no_alloc(tensors, eps, eps, stream=0, cache_mode=mode, check=False)
+
+
+def test_no_alloc_argument_checks(lib):
+    """mla_prolog_no_alloc validates exactly like mla_prolog, before any CUDA call."""
+    t = dsv3()
+    t["w_uk"] = None
+    assert no_alloc_code(t) == 161001
+    t = dsv3()
+    t["x"].data = None
+    assert no_alloc_code(t) == 161001
+    assert no_alloc_code(dsv3(w_dkvkr=T(BF16, 7168, 512))) == 161002
+    assert no_alloc_code(dsv3(cache_index=T(F32, 32))) == 161002
+    assert no_alloc_code(dsv3(q_out=T(I8, 32, 128, 512))) == 161001
+    assert no_alloc_code(dsv3(), mode="PA_NZ") == 161002
+
+
+def test_no_alloc_empty_tokens_returns_ok_without_the_device(lib):
+    # T = 0: MLA_OK, and the call returns before it asks the runtime for anything
+    t = dsv3(Tk=0, x=T(BF16, 0, 7168), rope_sin=T(BF16, 0, 64), rope_cos=T(BF16, 0, 64),
+             cache_index=T(I64, 0), q_out=T(BF16, 0, 128, 512), q_rope_out=T(BF16, 0, 128, 64))
+    assert no_alloc_code(t) == 0
+
+
+def test_no_alloc_status_null_pointer(lib):
+    assert lib.mla_prolog_no_alloc_status(None, None) == 161001
