@@ -103,6 +103,8 @@ struct GemmArgs {
 template <int BN, int MSUB, int MAXST, int OUTB = 0, int KPS = 1, int EPW = 1>
 struct GemmCfg {
     static constexpr int kOutBytes = 4 * EPW * OUTB * 4096;
+    // split epilogues that need a whole row (EPI_QN int8): two 128-row x EPW partial maxima
+    static constexpr int kXBytes = EPW > 1 ? 2 * 128 * EPW * 4 : 0;
     static constexpr int kBStage = BN * kBK * 2 * KPS;      // BN/64 boxes of 64 cols x 64*KPS rows
     static constexpr int kAcc = MSUB * BN;                  // TMEM columns per accumulator set
     static constexpr int kNBuf = (2 * kAcc <= 512) ? 2 : 1;
@@ -121,10 +123,10 @@ struct GemmCfg {
     // A region first: a 128-row MMA operand read from the last A stage with a short box runs
     // at most 16 KB past it, into the B ring (>= 2 stages of >= 8 KB), inside the block.
     static __host__ __device__ size_t smem_bytes(int stages, int a_box_rows) {
-        return 1024 + kBarBytes + (size_t)stages * stage_bytes(a_box_rows) + kOutBytes;
+        return 1024 + kBarBytes + (size_t)stages * stage_bytes(a_box_rows) + kOutBytes + kXBytes;
     }
     static __host__ int max_stages(int a_box_rows) {
-        int s = (int)((kSmemLimit - 1024 - kBarBytes - kOutBytes) / stage_bytes(a_box_rows));
+        int s = (int)((kSmemLimit - 1024 - kBarBytes - kOutBytes - kXBytes) / stage_bytes(a_box_rows));
         return s < MAXST ? s : MAXST;
     }
     static_assert(2 * kBStage >= 16384, "B ring must cover the A over-read");
@@ -730,6 +732,90 @@ __device__ __forceinline__ void epilogue_qn_tma(const GemmArgs& a, const Unit& u
     if (row < a.T) a.q_scale[(size_t)row * a.N + head] = scale;
 }
 
+// q^N of one whole-row tile (one head, BN >= Hckv) with EPW warps per TMEM lane quarter: the
+// warp of share `part` owns 128-column chunks part, part + EPW, ...  For the int8 output each
+// warp takes the absolute maximum over its columns of every row, the EPW partial maxima of a
+// row meet in shared memory (`xbuf`, one of two buffers by tile parity, so that a fast warp's
+// next tile never overwrites what a slow warp still reads), and every warp then quantises its
+// own columns with the row's scale.  Rows at or past T take part in the exchange with a
+// maximum of zero and store nothing.  Called by all 128 * EPW epilogue threads together.
+template <int BN, int OUTB, int EPW>
+__device__ __forceinline__ void epilogue_qn_split(const GemmArgs& a, const Unit& u, const TmemSrc& src, int q,
+                                                  OutStage<OUTB>& out, int part, float* xbuf) {
+    static_assert(BN % (128 * EPW) == 0 || BN == 128 * EPW, "whole 128-column chunks per warp");
+    const int head = u.n_tile / a.tiles_per_head;
+    const int c0 = (u.n_tile % a.tiles_per_head) * BN;
+    const int row0 = u.m_tile * 128 + q * 32;   // this warp's first row
+    const int row = row0 + out.lane;
+    const bool any = row0 < a.T;                // warp-uniform
+    const size_t ld = a.q_ld > 0 ? a.q_ld : a.Hckv;
+    if (a.q_out_i8 == nullptr) {
+        // 16-bit output: no row-wide step, each warp stores its own chunks
+#pragma unroll 1
+        for (int j = 2 * part; any && j < BN / 64; j += 2 * EPW) {
+#pragma unroll 1
+            for (int jj = j; jj < j + 2; ++jj) {
+                const int col = c0 + 64 * jj;
+                if (col >= a.Hckv) break;
+                uint32_t w[32];
+                float v[32];
+                src.load(0, BN, 64 * jj, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = a.f16 ? pack_f16(v[2 * i], v[2 * i + 1]) : pack_bf16(v[2 * i], v[2 * i + 1]);
+                src.load(0, BN, 64 * jj + 32, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[16 + i] = a.f16 ? pack_f16(v[2 * i], v[2 * i + 1]) : pack_bf16(v[2 * i], v[2 * i + 1]);
+                out.put(w, head * (int)ld + col, row0);
+            }
+        }
+        return;
+    }
+    // int8: this warp's share of the row maximum
+    float m = 0.f;
+#pragma unroll 1
+    for (int j = part; any && j < BN / 128; j += EPW) {
+        if (c0 + 128 * j >= a.Hckv) break;
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+            float v[32];
+            src.load(0, BN, 128 * j + 32 * h, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+        }
+    }
+    const int rin = q * 32 + out.lane;
+    xbuf[part * 128 + rin] = m;
+    epi_bar_n<128 * EPW>();
+#pragma unroll
+    for (int p = 0; p < EPW; ++p) m = fmaxf(m, xbuf[p * 128 + rin]);
+    if (!any) return;
+    const float scale = m / 127.f;
+    // The codes round(v / scale) are taken as round(v * (127 / m)): the two differ only for
+    // quotients within a few ulp of a half-integer, by one code at most.
+    const float inv = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;
+#pragma unroll 1
+    for (int j = part; j < BN / 128; j += EPW) {
+        const int col = 128 * j;
+        if (c0 + col >= a.Hckv) break;
+        uint32_t w[32];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float v[32];
+            src.load(0, BN, col + 32 * h, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint32_t packed = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) packed |= ((uint32_t)(quant_i8(v[4 * i + e] * inv) & 0xFF)) << (8 * e);
+                w[8 * h + i] = packed;
+            }
+        }
+        out.put(w, head * (int)ld + c0 + col, row0);
+    }
+    if (part == 0 && row < a.T) a.q_scale[(size_t)row * a.N + head] = scale;
+}
+
 // ---------------------------------------------------------------------- loads
 
 // Weight tile of the stage starting at k-block kb: BN/64 boxes of 64 columns x (64 * KPS) rows
@@ -794,8 +880,8 @@ __global__ void __launch_bounds__(gemm_threads(EPW), 1)
                    const __grid_constant__ CUtensorMap map_o2, const GemmArgs args) {
     using C = GemmCfg<BN, MSUB, MAXST, OUTB, KPS, EPW>;
     constexpr int kEpiThreads = 128 * EPW;
-    static_assert(EPW == 1 || (OUTB > 0 && (EPI == EPI_F32 || (EPI == EPI_QROPE && BN != 192))),
-                  "split epilogues exist for TMA-stored fp32 rows and head-unaligned RoPE tiles");
+    static_assert(EPW == 1 || (OUTB > 0 && (EPI == EPI_F32 || EPI == EPI_QN || (EPI == EPI_QROPE && BN != 192))),
+                  "split epilogues exist for TMA-stored fp32 rows, q^N tiles and head-unaligned RoPE tiles");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -812,6 +898,7 @@ __global__ void __launch_bounds__(gemm_threads(EPW), 1)
     uint8_t* sA = smem + C::kBarBytes;
     uint8_t* sB = sA + (size_t)stages * a_stage;
     uint8_t* sOut = sB + (size_t)stages * C::kBStage;   // OUTB x 4 KB per epilogue warp
+    float* sX = reinterpret_cast<float*>(sOut + C::kOutBytes);   // C::kXBytes: split-epilogue exchange
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1038,7 +1125,9 @@ __global__ void __launch_bounds__(gemm_threads(EPW), 1)
                     epilogue_qrope<MSUB>(args, row0, u.n_tile, tsrc);
                 }
             } else {
-                if constexpr (OUTB > 0) {
+                if constexpr (EPW > 1) {
+                    epilogue_qn_split<BN, OUTB, EPW>(args, u, tsrc, q, ostage, part, sX + (ai & 1) * 128 * EPW);
+                } else if constexpr (OUTB > 0) {
                     if (args.tma_out)
                         epilogue_qn_tma<BN, OUTB>(args, u, tsrc, q, ostage);
                     else

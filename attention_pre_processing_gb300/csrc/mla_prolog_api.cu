@@ -1017,7 +1017,9 @@ mla_status run(const Launched& L) {
     if (sc.q_i8) {
         g3.q_out_i8 = static_cast<int8_t*>(a.qout->data);
         g3.q_scale = static_cast<float*>(a.qscale->data);
-        e = launch_gemm<512, 1, 4, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr);
+        // two warps per TMEM lane quarter, each with 256 of the 512 columns (TMA-stored boxes)
+        e = g3.tma_out ? launch_gemm<512, 1, 4, EPI_QN, 1, 1, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, &mO3)
+                       : launch_gemm<512, 1, 4, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, nullptr);
     } else {
         g3.q_out_bf16 = static_cast<__nv_bfloat16*>(a.qout->data);
         e = kps3 ? launch_gemm<256, 1, 8, EPI_QN, 2, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr)
