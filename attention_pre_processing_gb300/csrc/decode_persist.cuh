@@ -8,7 +8,8 @@
 //        counter.  Once a c^Q tile's count is complete, its CTAs add the tile's slots in k-range
 //        order, one 16-column chunk each, and write bf16(gamma * y) (P3's activation) and each
 //        token's sum of y^2 over the chunk
-//   P3   head n = CTA index, once every c^Q chunk is written: c^Q by TMA;
+//   P3   head n = CTA index: c^Q by TMA, each 64-column k-block as soon as its four chunks are
+//        written;
 //        (gamma * y) . W^UqQr[:, head n]; the epilogue multiplies by the token's 1 / RMS,
 //        applies RoPE to the rope columns (queryRopeOut) and writes q^C straight into shared
 //        memory as P4's A operand
@@ -19,15 +20,22 @@
 // RmsNorm(y) . W = (1 / RMS(y)) * ((gamma * y) . W): the per-token scale moves behind the
 // contraction, so no row pass sits between the reduction and P3.
 //
+// The MMAs are M = 64 (T <= 64 token rows) by N = the weight columns: an MMA costs the same for
+// M = 64 and M = 128 (its time grows with N only), reads half the token rows from shared memory,
+// and puts rows 16 q .. 16 q + 15 in TMEM lanes 32 q .. 32 q + 15, so that the epilogue warp of
+// lane quarter q holds tokens 16 q ..: two warps share the P1 and P3 epilogues at T = 32.  P4's
+// token rows are written by the P3 epilogue itself, spread so that all four warps share P4's
+// epilogue: token t sits in row 16 (t / tpq) + t % tpq, tpq = ceil(T / 4) tokens per quarter.
+//
 // Every sum is taken in a fixed order, so calls are bit-reproducible.  Each tile's counter is
 // reset at the start of the call by the tile's first k-range CTA, which then stores the call's
 // tag in the tile's flag; readers wait for the flag and a complete counter.  Flags of another
 // call hold another tag, so the workspace needs no initialisation.
 //
 // Roles (256 threads): warp 0 streams weight stages with TMA (one 3D box of three 64-column
-// blocks per stage); warp 1 allocates tensor memory and issues tcgen05.mma; warp 2 loads P1's
-// activation tiles (x) with TMA; warp 3 is idle; warps 4..7 run the zeroing, the epilogues, P3's
-// activation tiles and the cache rows.  Every wait is bounded: a wait that gives up sets
+// blocks per stage); warp 1 allocates tensor memory and issues tcgen05.mma; warp 2 loads the
+// activation tiles with TMA (x for P1, then each c^Q k-block once its chunk flags hold the call's
+// tag); warp 3 is idle; warps 4..7 run the zeroing, the epilogues and the cache rows.  Every wait is bounded: a wait that gives up sets
 // MLA_DEV_WAIT_TIMEOUT, the other roles stop at their next wait, tensor memory is freed and the
 // kernel returns.
 
@@ -46,7 +54,7 @@ constexpr int kPBox = 8192;                  // one 64 x 64 bf16 weight box
 constexpr int kPStage = 3 * kPBox;           // one weight stage: up to 192 columns
 constexpr int kPMaxW = 12;                   // weight stages at most
 constexpr int kPA = 4;                       // P1 activation slots (TMA)
-constexpr int kPA3 = 8;                      // P3 activation slots (written by the epilogue warps)
+constexpr int kPA3 = 24;                     // P3 activation (c^Q) slots at most
 constexpr int kPTile = 192;                  // P1 columns per tile
 constexpr int kPChunk = 16;                  // columns per c^Q reduction chunk
 constexpr int kPMaxT = 64;                   // tokens at most
@@ -54,6 +62,8 @@ constexpr int kPMaxS = 16;                   // k ranges at most
 
 struct PersistArgs {
     int T, a_rows, a_bytes, wst;        // tokens, A box rows, A slot bytes, weight stages
+    int na3;                            // P3 activation (c^Q) slots, <= kPA3
+    int pf;                             // P3 weight stages requested into L2 beyond the ring
     // P1
     int hcq, hckv, dr, ncols1, n1, s1, kb1;
     float* y;                           // s1 k-range slots of T x ncols1 fp32 products
@@ -221,13 +231,49 @@ __device__ __forceinline__ void chain_store(uint32_t base, int slot_bytes, int r
     }
 }
 
-// Alignment slack, barriers and a 1 KB scratch, the activation region (P1's TMA ring, later
-// P3's ring, later P4's A operand) and the weight ring.
-__host__ __device__ inline size_t persist_smem_bytes(int a_bytes, int wst) {
-    return 1024 + 2048 + (size_t)kPA3 * a_bytes + (size_t)wst * kPStage;
+// The activation region: P1's TMA ring, later P3's ring of na3 c^Q slots, later P4's A operand
+// (two k-blocks of 64 rows x 128 bytes, so at least 16 KB).
+__host__ __device__ inline size_t persist_act_bytes(int a_bytes, int na3) {
+    const size_t r = (size_t)na3 * a_bytes;
+    return r < 16384 ? 16384 : r;
+}
+constexpr int kP4Blk = 64 * 128;   // one k-block of P4's A operand (64 rows)
+
+// Shared memory split of the persistent kernel for a given activation slot size (T token rows
+// of 128 bytes): the c^Q slots first, as many of the kb2 k-blocks as leave kPMinW weight stages
+// (with every k-block resident, c^Q requests never wait for the MMAs to free a slot), then the
+// weight ring with the rest, and kPPre P3 stages in flight before P3 starts (ring + L2).
+constexpr int kPMinW = 6;    // weight stages at least (P4's six stages in distinct slots)
+constexpr int kPPre = 16;    // P3 weight stages requested before the reduction completes
+struct PersistSlots {
+    int na3, wst, pf;
+};
+__host__ __device__ inline PersistSlots persist_slots(int a_bytes, int kb2, size_t smem_limit);
+
+// Alignment slack, barriers and a 1 KB scratch, the activation region and the weight ring.
+__host__ __device__ inline size_t persist_smem_bytes(int a_bytes, int na3, int wst) {
+    return 1024 + 2048 + persist_act_bytes(a_bytes, na3) + (size_t)wst * kPStage;
+}
+
+__host__ __device__ inline PersistSlots persist_slots(int a_bytes, int kb2, size_t smem_limit) {
+    PersistSlots r{0, 0, 0};
+    const size_t fixed = 1024 + 2048 + (size_t)kPMinW * kPStage;
+    if (smem_limit <= fixed) return r;
+    int na3 = (int)((smem_limit - fixed) / (size_t)a_bytes);
+    if (na3 > kb2) na3 = kb2;
+    if (na3 > kPA3) na3 = kPA3;
+    if (na3 < 2) return r;
+    int wst = (int)((smem_limit - persist_smem_bytes(a_bytes, na3, 0)) / kPStage);
+    if (wst > kPMaxW) wst = kPMaxW;
+    r.na3 = na3;
+    r.wst = wst;
+    r.pf = kPPre > wst ? kPPre - wst : 0;
+    return r;
 }
 
 // ------------------------------------------------------------------ kernel
+
+static_assert(8 * (2 * kPMaxW + 2 * kPA + 2 * kPA3 + 3 + 3 + 4) + 16 <= 1024, "barrier area");
 
 __global__ void __launch_bounds__(kPThreads, 1)
     decode_persist_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wdq,
@@ -246,14 +292,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint64_t* tfull = aempty3 + kPA3;             // [3]: P1, P3 accumulators ([2] unused)
     uint64_t* tfull4 = tfull + 3;                 // [3]: P4 column groups
     uint64_t* chain_full = tfull4 + 3;
-    uint64_t* cq_ready = chain_full + 1;         // the epilogue saw every c^Q tile written
-    uint64_t* done = cq_ready + 1;
+    uint64_t* p1_done = chain_full + 1;          // this CTA's P1 product and chunk reductions are stored
+    uint64_t* cq_all = p1_done + 1;              // warp 2 saw every c^Q chunk flag hold the tag
+    uint64_t* done = cq_all + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     volatile int* s_last = s_abort + 1;   // this CTA stored the last k range of its P1 tile
     float* scratch = reinterpret_cast<float*>(smem + 1024);   // 1 KB: the KV rows' warp sums
     uint8_t* aring = smem + 2048;
-    uint8_t* wring = aring + (size_t)kPA3 * args.a_bytes;
+    uint8_t* wring = aring + persist_act_bytes(args.a_bytes, args.na3);
+    const int na3 = args.na3;
     const int wst = args.wst;
 
     const int warp = threadIdx.x >> 5;
@@ -278,7 +326,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(smem_u32(&afull[s]), 1);
             mbar_init(smem_u32(&aempty[s]), 1);
         }
-        for (int s = 0; s < kPA3; ++s) {
+        for (int s = 0; s < na3; ++s) {
             mbar_init(smem_u32(&afull3[s]), 1);
             mbar_init(smem_u32(&aempty3[s]), 1);
         }
@@ -287,7 +335,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(smem_u32(&tfull4[p]), 1);
         }
         mbar_init(smem_u32(chain_full), 128);
-        mbar_init(smem_u32(cq_ready), 1);
+        mbar_init(smem_u32(p1_done), 1);
+        mbar_init(smem_u32(cq_all), 1);
         mbar_init(smem_u32(done), 1);
         *s_abort = 0;
         fence_barrier_init();
@@ -340,12 +389,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     ph ^= 1;
                 }
                 // The ring now holds the first P3 stages, which wait for the reduction: while HBM
-                // idles, the next eight P3 stages are requested into L2 (all of P3 / P4 would
-                // load L2 enough to stretch the reduction's dependency chain).
+                // idles, the next pf P3 stages are requested into L2 (all of P3 / P4 would load L2
+                // enough to stretch the reduction's dependency chain).
                 if (head && i == n1s + wst - 1) {
                     const uint64_t keep = policy_evict_last();
                     PStep pf;
-                    for (int k = i + 1; k <= i + 8 && p_step(args, k, n1s, pf); ++k)
+                    for (int k = i + 1; k <= i + args.pf && p_step(args, k, n1s, pf); ++k)
                         if (pf.phase == 3) tma_prefetch_l2_3d(&map_wuqqr, 0, pf.kb * 64, (int)blockIdx.x * 3, keep);
                 }
             }
@@ -356,8 +405,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // constant offsets (their start-address field counts 16-byte units), so that a stage
         // costs little more than its four MMAs.
         if (lane == 0) {
-            constexpr uint32_t id192 = idesc_bf16_f32(128, 192, false, true);
-            constexpr uint32_t id128 = idesc_bf16_f32(128, 128, false, true);
+            constexpr uint32_t id192 = idesc_bf16_f32(64, 192, false, true);
+            constexpr uint32_t id128 = idesc_bf16_f32(64, 128, false, true);
             const uint64_t adesc0 = smem_desc_sw128(smem_u32(aring), 16, 1024);
             const uint64_t bdesc0 = smem_desc_sw128(smem_u32(wring), kPBox, 1024);
             const uint64_t a_unit = (uint64_t)(args.a_bytes >> 4);   // one activation slot
@@ -410,8 +459,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 int sa = 0;
                 uint32_t pha = 0;
                 for (int kb = 0; ok && kb < args.kb2; kb += 2) {
-                    const int sa1 = sa + 1 == kPA3 ? 0 : sa + 1;
-                    const uint32_t pha1 = sa + 1 == kPA3 ? pha ^ 1 : pha;
+                    const int sa1 = sa + 1 == na3 ? 0 : sa + 1;
+                    const uint32_t pha1 = sa + 1 == na3 ? pha ^ 1 : pha;
                     const int sw1 = sw + 1 == wst ? 0 : sw + 1;
                     const uint32_t phw1 = sw + 1 == wst ? phw ^ 1 : phw;
                     ok = mbar_wait(smem_u32(&afull3[sa]), pha, s_abort, kWaitLimitNs) && wait_w() &&
@@ -424,20 +473,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     umma_commit(smem_u32(&aempty3[sa]));
                     umma_commit(smem_u32(&wempty[uw1]));
                     umma_commit(smem_u32(&aempty3[sa1]));
-                    sa = sa1 + 1 == kPA3 ? 0 : sa1 + 1;
-                    pha = sa1 + 1 == kPA3 ? pha1 ^ 1 : pha1;
+                    sa = sa1 + 1 == na3 ? 0 : sa1 + 1;
+                    pha = sa1 + 1 == na3 ? pha1 ^ 1 : pha1;
                 }
                 if (ok) umma_commit(smem_u32(&tfull[1]));
-                // P4: A = q^C in activation slots 0 and 1; column group by column group (both
-                // k-blocks), each group's accumulator committed on its own so that its epilogue
-                // overlaps the next groups' MMAs
+                // P4: A = q^C, two 64-row k-blocks at the start of the activation region; column
+                // group by column group (both k-blocks), each group's accumulator committed on
+                // its own so that its epilogue overlaps the next groups' MMAs
                 ok = ok && mbar_wait(smem_u32(chain_full), 0, s_abort, kWaitLimitNs) && wait_w();
                 for (int g = 0; ok && g < 3; ++g) {
                     const uint32_t id = g == 2 ? id128 : id192;
                     const int u0 = mma4(adesc0, tmem_base + 192 * g, id, true);
                     ok = wait_w();
                     int u1 = -1;
-                    if (ok) u1 = mma4(adesc0 + a_unit, tmem_base + 192 * g, id, false);
+                    if (ok) u1 = mma4(adesc0 + (kP4Blk >> 4), tmem_base + 192 * g, id, false);
                     if (ok && g < 2) ok = wait_w();
                     umma_commit(smem_u32(&wempty[u0]));
                     if (u1 >= 0) umma_commit(smem_u32(&wempty[u1]));
@@ -450,52 +499,101 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ activation tiles
+        const uint64_t pol = policy_evict_last();
+        bool ok = true;
         if (lane == 0) {
-            const uint64_t pol = policy_evict_last();
             int sa = 0;
             uint32_t ph = 0;
-            bool ok = true;
-            auto put = [&](const CUtensorMap* map, int kb) -> bool {
-                if (!mbar_wait_sleep(smem_u32(&aempty[sa]), ph ^ 1, s_abort, kWaitLimitNs)) return false;
+            for (int i = 0; ok && i < n1s; ++i) {
+                if (!mbar_wait_sleep(smem_u32(&aempty[sa]), ph ^ 1, s_abort, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t fb = smem_u32(&afull[sa]);
                 mbar_arrive_expect_tx(fb, (uint32_t)args.a_bytes);
-                tma_load_2d(smem_u32(aring + (size_t)sa * args.a_bytes), map, fb, kb * 64, 0, pol);
+                tma_load_2d(smem_u32(aring + (size_t)sa * args.a_bytes), &map_x, fb, (kb0 + i) * 64, 0, pol);
                 if (++sa == kPA) {
                     sa = 0;
                     ph ^= 1;
                 }
-                return true;
-            };
-            for (int i = 0; ok && i < n1s; ++i) ok = put(&map_x, kb0 + i);
-            if (ok && head) {
-                // P3's activation tiles (c^Q k-blocks), once the epilogue warps have seen every
-                // c^Q tile written.  c^Q was written by other CTAs' ordinary stores and is read
-                // here by the TMA engine, into slots this CTA's epilogue used for staging: the
-                // proxy fence orders both.
-                ok = mbar_wait_sleep(smem_u32(cq_ready), 0, s_abort, kWaitLimitNs);
-                asm volatile("fence.proxy.async;" ::: "memory");
-                for (int kb = 0; ok && kb < args.kb2; ++kb) {
-                    const int s3 = kb % kPA3;
-                    if (kb >= kPA3 &&
-                        !mbar_wait_sleep(smem_u32(&aempty3[s3]), ((kb / kPA3) & 1) ^ 1, s_abort, kWaitLimitNs)) {
-                        ok = false;
-                        break;
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (ok && head) {
+            // P3's activation tiles: c^Q k-block kb is requested as soon as its four 16-column
+            // chunk flags hold the call's tag (the chunks are reduced in parallel by other CTAs,
+            // so early k-blocks need not wait for the last chunk).  Polling starts once this
+            // CTA's own P1 work is stored (the other CTAs finish theirs at about the same time;
+            // earlier polling only loads L2 while the reductions run).  One round loads every chunk
+            // flag not yet seen (four per lane): one trip to L2; the longest prefix of set flags
+            // gives the k-blocks that may be requested, in order.  c^Q was written by
+            // other CTAs' ordinary stores and is read here by the TMA engine: a relaxed read that
+            // saw the release, an acquire fence, then the proxy fence.  Once every flag is seen,
+            // cq_all tells the epilogue warps (their 1 / RMS needs every chunk's sum of squares).
+            if (lane == 0) ok = mbar_wait_sleep(smem_u32(p1_done), 0, s_abort, kWaitLimitNs);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            const int nchunks = args.hcq / kPChunk;   // <= 128
+            int seen = 0;     // chunk flags seen, in order
+            int issued = 0;   // k-blocks requested
+            const uint64_t t0 = global_timer_ns();
+            while (ok && issued < args.kb2) {
+                if (seen < nchunks) {
+                    bool set[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = seen + lane + 32 * k;
+                        set[k] = c >= nchunks || ld_relaxed_u64(args.cqflags + c) == args.tag;
                     }
-                    const uint32_t fb = smem_u32(&afull3[s3]);
-                    mbar_arrive_expect_tx(fb, (uint32_t)args.a_bytes);
-                    tma_load_2d(smem_u32(aring + (size_t)s3 * args.a_bytes), &map_cq, fb, kb * 64, 0, pol);
+                    int run = 0;   // consecutive set flags from `seen` on
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const unsigned m = __ballot_sync(0xffffffffu, set[k]);
+                        if (run == 32 * k) run += m == 0xffffffffu ? 32 : __ffs(~m) - 1;
+                    }
+                    if (run > 0) {
+                        seen = min(nchunks, seen + run);
+                        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                        if (seen == nchunks && lane == 0) mbar_arrive(smem_u32(cq_all));
+                    }
+                }
+                const int ready = seen / 4;   // k-blocks whose four chunks are written
+                if (ready > issued) {
+                    if (lane == 0) {
+                        asm volatile("fence.proxy.async;" ::: "memory");
+                        for (; ok && issued < ready; ++issued) {
+                            const int s3 = issued % na3;
+                            if (issued >= na3 && !mbar_wait_sleep(smem_u32(&aempty3[s3]), ((issued / na3) & 1) ^ 1,
+                                                                   s_abort, kWaitLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t fb = smem_u32(&afull3[s3]);
+                            mbar_arrive_expect_tx(fb, (uint32_t)args.a_bytes);
+                            tma_load_2d(smem_u32(aring + (size_t)s3 * args.a_bytes), &map_cq, fb, issued * 64, 0, pol);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    issued = __shfl_sync(0xffffffffu, issued, 0);
+                } else {
+                    // nothing new: give up at the limit (lane 0 decides for the warp)
+                    int stop = 0;
+                    if (lane == 0) stop = (*s_abort || global_timer_ns() - t0 > kWaitLimitNs) ? 1 : 0;
+                    if (__shfl_sync(0xffffffffu, stop, 0)) ok = false;
+                    else __nanosleep(128);
                 }
             }
-            if (!ok) fail();
         }
+        if (!ok && lane == 0) fail();
     } else if (warp == 3) {
         // idle
     } else {
         // ------------------------------------------------------------ epilogue warps
         const int etid = threadIdx.x - 128;   // 0..127
         const int q = warp & 3;               // TMEM lane quarter
-        const int row = q * 32 + lane;
+        const int row = q * 16 + lane;        // the token of this lane in P1 / P3 (M = 64 layout)
         const int T = args.T;
+        const bool rowok = lane < 16 && row < T;
+        const int tpq = (T + 3) / 4;          // P4: tokens per lane quarter
         bool ok = true;
         auto acc_ready = [&](int p) -> bool {
             int r = 1;
@@ -531,13 +629,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // 16 bytes).  The staging row stride (196 floats) spreads the row writes over banks.
             constexpr int kStg = kPTile + 4;
             float* stg = reinterpret_cast<float*>(aring);
-            if (ok && q * 32 < T) {
+            if (ok && q * 16 < T) {
 #pragma unroll 1
                 for (int ch = 0; ch < kPTile / 32; ++ch) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + 256 + ch * 32, r);
                     tmem_ld_wait();
-                    if (row < T) {
+                    if (rowok) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             *reinterpret_cast<uint4*>(stg + row * kStg + ch * 32 + 4 * i) =
@@ -614,42 +712,57 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         if (!ok) fail();
         ok = !epi_any(!ok);   // uniform over the 128 threads: the waits below are collective
+        if (etid == 0) mbar_arrive(smem_u32(p1_done));   // warp 2 may start polling the chunk flags
 
         if (ok && head) {
-            // Every c^Q chunk is written ...
-            ok = wait_tiles(args.cqflags, nullptr, 0, args.hcq / kPChunk, 0u, args.tag, s_abort, etid);
-            // ... then P3's activation tiles come by TMA (warp 2) ...
-            if (etid == 0) mbar_arrive(smem_u32(cq_ready));
-            // ... and each row's 1 / RMS from the chunks' sums of y^2 (in chunk order).
+            // Every c^Q chunk is written (warp 2 saw every flag; P3's MMAs wait for their own
+            // k-blocks only), so each row's 1 / RMS from the chunks' sums of y^2 (in chunk order)
+            {
+                int r = 1;
+                if (lane == 0) r = mbar_wait_sleep(smem_u32(cq_all), 0, s_abort, kWaitLimitNs) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, r, 0) != 0;
+                ok = !epi_any(!ok);
+            }
+            // This row's RoPE tables, loaded before P3's product is ready
+            uint4 rcs[16];
+            if (ok && rowok) {
+                const uint4* cp = reinterpret_cast<const uint4*>(args.rope_cos + (size_t)row * 64);
+                const uint4* sp = reinterpret_cast<const uint4*>(args.rope_sin + (size_t)row * 64);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    rcs[i] = cp[i];
+                    rcs[8 + i] = sp[i];
+                }
+            }
             float inv = 0.f;
-            if (ok && row < T) {
+            if (ok && rowok) {
                 float s2 = 0.f;
                 for (int c = 0; c < args.hcq / kPChunk; ++c) s2 += __ldcg(args.ss + (size_t)c * T + row);
                 inv = 1.f / sqrtf(s2 / (float)args.hcq + args.eps_cq);
             }
             // ---- P3 epilogue: 1 / RMS per token, RoPE -> queryRopeOut, q^C -> P4's A operand
+            // (token `row` in P4 row 16 (row / tpq) + row % tpq)
             ok = acc_ready(1);
-            if (ok && q * 32 < T) {
+            if (ok && q * 16 < T) {
                 const TmemSrc src{tmem_base + ((uint32_t)(q * 32) << 16)};
                 const uint32_t chain = smem_u32(aring);
+                const int prow = 16 * (row / tpq) + row % tpq;
 #pragma unroll 1
                 for (int ch = 0; ch < 4; ++ch) {
                     float v[32];
                     src.load(0, 0, ch * 32, v);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= inv;
-                    if (row < T) chain_store(chain, args.a_bytes, row, ch * 32, v);
+                    if (rowok) chain_store(chain, kP4Blk, prow, ch * 32, v);
                 }
                 float x0[32], x1[32];
                 src.load(0, 0, 128, x0);
                 src.load(0, 0, 160, x1);
-                if (row < T) {
-                    const uint4* cp = reinterpret_cast<const uint4*>(args.rope_cos + (size_t)row * 64);
-                    const uint4* sp = reinterpret_cast<const uint4*>(args.rope_sin + (size_t)row * 64);
+                if (rowok) {
                     float o0[32], o1[32];
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
-                        const uint4 c0 = cp[qq], c1 = cp[qq + 4], s0 = sp[qq], s1 = sp[qq + 4];
+                        const uint4 c0 = rcs[qq], c1 = rcs[qq + 4], s0 = rcs[8 + qq], s1 = rcs[8 + qq + 4];
                         const uint32_t cw0[4] = {c0.x, c0.y, c0.z, c0.w}, cw1[4] = {c1.x, c1.y, c1.z, c1.w};
                         const uint32_t sw0[4] = {s0.x, s0.y, s0.z, s0.w}, sw1[4] = {s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
@@ -673,12 +786,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(chain_full));
 
-            // ---- P4 epilogue: queryOut through shared memory and TMA stores, group by group.
-            // Staging: the ring slot of P4's first weight stage (the last phase: once group 0 is
-            // complete that slot is never loaded again); 8 KB per warp, at most two warps.
+            // ---- P4 epilogue: queryOut through shared memory and TMA stores (boxes of the warp's
+            // tpq tokens x 64 columns), group by group.  Staging: the ring slots of P4's first two
+            // weight stages (the last phase: once group 0 is complete they are never loaded
+            // again); 8 KB per warp, two warps per slot.
             {
-                const int slot0 = (n1s + args.kb2) % wst;
-                OutStage<2> out{wring + (size_t)slot0 * kPStage + (size_t)(warp - 4) * 2 * 4096, 0, &map_o, lane};
+                const int slot = (n1s + args.kb2 + (q >> 1)) % wst;
+                OutStage<2> out{wring + (size_t)slot * kPStage + (size_t)(q & 1) * 2 * 4096, 0, &map_o, lane};
                 const TmemSrc src{tmem_base + ((uint32_t)(q * 32) << 16)};
                 for (int g = 0; ok && g < 3; ++g) {
                     int r = 1;
@@ -686,7 +800,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     ok = __shfl_sync(0xffffffffu, r, 0) != 0;
                     __syncwarp();
                     tc_fence_after();
-                    if (!ok || q * 32 >= T) continue;
+                    if (!ok || q * tpq >= T) continue;
 #pragma unroll 1
                     for (int j = 3 * g; j < (g == 2 ? 8 : 3 * g + 3); ++j) {
                         uint32_t w[32];
@@ -697,10 +811,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         src.load(0, 0, 64 * j + 32, v);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-                        out.put(w, (int)blockIdx.x * 512 + 64 * j, q * 32);
+                        out.put(w, (int)blockIdx.x * 512 + 64 * j, q * tpq);
                     }
                 }
-                if (q * 32 < T) out.drain();
+                if (q * tpq < T) out.drain();
             }
         }
 

@@ -235,7 +235,7 @@ struct Plan {
     bool fold_cq = false;    // K1 writes bf16(gamma_cq * y) and row sums of squares, K2 applies 1 / RMS
     size_t off_ss = 0;       // fold_cq: T x kFoldSums row sums of squares
     bool persist = false;    // decode-sized bf16 call: the one persistent kernel of decode_persist.cuh
-    int p_n1 = 0, p_s1 = 0, p_wst = 0, p_arows = 0;
+    int p_n1 = 0, p_s1 = 0, p_wst = 0, p_arows = 0, p_na3 = 0, p_pf = 0;
     size_t p_smem = 0, off_pbar = 0;
     int64_t ncols1 = 0, ncols2 = 0;
     size_t off_cq = 0, off_cqs = 0, off_qc = 0, off_y1 = 0, off_y2 = 0, off_xb = 0, off_wdq = 0, off_wdkvkr = 0,
@@ -337,21 +337,23 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
         const int kb1 = (int)(d.He / 64);
         const int arows = (int)((T + 7) / 8 * 8);
         const size_t a_bytes = (size_t)arows * 128;
-        const int wst_fit = (int)((kSmemLimit - persist_smem_bytes((int)a_bytes, 0)) / kPStage);
-        const int wst = wst_fit < kPMaxW ? wst_fit : kPMaxW;
+        const PersistSlots ps = persist_slots((int)a_bytes, (int)(d.Hcq / 64), kSmemLimit);
+        const int wst = ps.wst;
         int s1 = n1 > 0 ? sms / n1 : 0;
         if (s1 > kb1) s1 = kb1;
         if (s1 > kPMaxS) s1 = kPMaxS;
         if (!sc.x_i8 && !sc.uqqr_i8 && !sc.kv_i8 && !sc.kr_i8 && !sc.q_i8 && T >= 1 && T <= kPMaxT &&
             d.D == 128 && d.Dr == 64 && d.Hckv == 512 && d.Hcq % 384 == 0 && d.He % 64 == 0 && ncols1 % 192 == 0 &&
             d.Hcq / kPChunk <= 128 && d.N >= 1 && d.N <= sms && s1 >= 1 &&
-            wst >= 6) {   // P4 staging needs its six stages in distinct slots
+            ps.na3 >= 2 && wst >= kPMinW) {   // P4 staging needs its six stages in distinct slots
             p.persist = true;
             p.p_n1 = n1;
             p.p_s1 = s1;
             p.p_wst = wst;
+            p.p_na3 = ps.na3;
+            p.p_pf = ps.pf;
             p.p_arows = arows;
-            p.p_smem = persist_smem_bytes((int)a_bytes, wst);
+            p.p_smem = persist_smem_bytes((int)a_bytes, ps.na3, wst);
         }
     }
 
@@ -756,7 +758,7 @@ mla_status run(const Launched& L) {
         const uint64_t ocols = (uint64_t)d.N * (uint64_t)d.Hckv;
         const uint64_t odims[2] = {ocols, (uint64_t)d.T};
         const uint64_t ostrides[1] = {ocols * 2};
-        const uint32_t obox[2] = {64, 32};
+        const uint32_t obox[2] = {64, (uint32_t)((d.T + 3) / 4)};   // one lane quarter's tokens
         if (!map_2d(&mx, x_bf, d.T, d.He, rows) || !map_colblocks(&mwdq, wdq_bf, d.He, d.Hcq, 64, 3) ||
             !map_colblocks(&mwdkvkr, wdkvkr_bf, d.He, d.Hckv + d.Dr, 64, 3) ||
             !map_2d(&mcq, ws + p.off_cq, d.T, d.Hcq, rows) || !map_colblocks(&mwuqqr, wuqqr_bf, d.Hcq, p.ncols2, 64, 3) ||
@@ -768,6 +770,8 @@ mla_status run(const Launched& L) {
         pa.a_rows = (int)rows;
         pa.a_bytes = (int)rows * 128;
         pa.wst = p.p_wst;
+        pa.na3 = p.p_na3;
+        pa.pf = p.p_pf;
         pa.hcq = (int)d.Hcq;
         pa.hckv = (int)d.Hckv;
         pa.dr = (int)d.Dr;
