@@ -54,7 +54,7 @@ struct DownArgs {
     int kr_int8;
     const float* quant_scale_ckr;       // (Dr)
     __nv_bfloat16* c_q;                 // (T, Hcq): bf16 c^Q, or int8 codes held as bf16
-    int cq_quant;                       // dynamic per-token int8 codes of c^Q
+    int cq_quant;                       // dynamic per-token int8 codes of c^Q, written as fp16
     const float* smooth_cq;             // (Hcq) or null
     float* c_q_scale;                   // (T)
     int cq_done;                        // c^Q was written by the down-projection (rows only need c^KV | k^R)
@@ -182,7 +182,7 @@ __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, floa
             float u = __bfloat162float(gcq[j]) * ys[j] * inv_q;
             if (a.smooth_cq) u *= a.smooth_cq[j];
             const int q = scale > 0.f ? quant_i8(__fdiv_rn(u, scale)) : 0;
-            cq[j] = __int2bfloat16_rn(q);
+            reinterpret_cast<__half*>(cq)[j] = __int2half_rn(q);   // exact: the fp16 A operand of the int8 GEMM
         }
         if (tid == 0) a.c_q_scale[t] = scale;
     }
@@ -380,7 +380,8 @@ __global__ void __launch_bounds__(kWarpRowThreads) finalize_down_warp_kernel(con
                 const int c = 2 * lane + 64 * k;
                 const int q0 = scale > 0.f ? quant_i8(__fdiv_rn(yq[k].x, scale)) : 0;
                 const int q1 = scale > 0.f ? quant_i8(__fdiv_rn(yq[k].y, scale)) : 0;
-                *reinterpret_cast<__nv_bfloat162*>(cq + c) = __halves2bfloat162(__int2bfloat16_rn(q0), __int2bfloat16_rn(q1));
+                // exact fp16 codes: the A operand of the int8-weight GEMM
+                *reinterpret_cast<__half2*>(cq + c) = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
             }
         if (lane == 0) a.c_q_scale[t] = scale;
     }
@@ -471,9 +472,10 @@ __global__ void __launch_bounds__(kRowThreads) finalize_up_kernel(const UpArgs a
     }
 }
 
-// Exact int8 -> bf16 widening (|v| <= 128 has at most 8 significant bits).
-__global__ void __launch_bounds__(256) convert_i8_to_bf16_kernel(const int8_t* __restrict__ src,
-                                                                 __nv_bfloat16* __restrict__ dst, long long n) {
+// Exact int8 -> fp16 widening (|v| <= 128 has at most 8 significant bits), for the fp16 A operand
+// of the int8-weight GEMM.
+__global__ void __launch_bounds__(256) convert_i8_to_f16_kernel(const int8_t* __restrict__ src,
+                                                                __half* __restrict__ dst, long long n) {
     pdl_launch_dependents();
     pdl_wait();
     const long long n16 = n / 16;
@@ -489,14 +491,15 @@ __global__ void __launch_bounds__(256) convert_i8_to_bf16_kernel(const int8_t* _
             for (int e = 0; e < 2; ++e) {
                 const int b0 = (int)(int8_t)((w[k] >> (16 * e)) & 0xFF);
                 const int b1 = (int)(int8_t)((w[k] >> (16 * e + 8)) & 0xFF);
-                ow[2 * k + e] = pack_bf16((float)b0, (float)b1);
+                const __half2 h = __halves2half2(__int2half_rn(b0), __int2half_rn(b1));
+                ow[2 * k + e] = *reinterpret_cast<const uint32_t*>(&h);
             }
         }
         reinterpret_cast<uint4*>(dst)[2 * i] = o[0];
         reinterpret_cast<uint4*>(dst)[2 * i + 1] = o[1];
     }
     for (long long i = n16 * 16 + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-        dst[i] = __int2bfloat16_rn((int)src[i]);
+        dst[i] = __int2half_rn((int)src[i]);
 }
 
 }  // namespace mla

@@ -1,7 +1,11 @@
-// GEMM with int8 weights streamed as int8 and widened in shared memory (decode-sized calls of the
-// aclnnMlaPreprocess variant): out = A . W^T with A fp16 (T, K) row-major (int8 codes held as
-// fp16, exact) and W int8 (ncols, K) row-major, one row per output column ("transposeWdq/Wuq"
-// true).
+// GEMM with int8 weights streamed as int8 and widened in shared memory: out = A . W with A fp16
+// (T, K) row-major (int8 codes held as fp16, exact) and W int8 in one of two orientations:
+//   MN = false: (ncols, K) row-major, one row per output column (the aclnnMlaPreprocess variant,
+//               "transposeWdq/Wuq" true), widened into K-major B tiles;
+//   MN = true:  (K, ncols) row-major, the (k, n) orientation of aclnnMlaPrologV2WeightNz's int8
+//               weights, widened into MN-major B tiles (64-column blocks of 64 k rows); the
+//               columns below b_split_col come from map_b8, the rest from map_b8b (two weights
+//               side by side, as W^DQ | W^DkvKr).
 //
 // GB300's int8 tensor rate is far below its fp16 rate, so the contraction runs as fp16 MMAs with
 // fp32 accumulation (exact for these integer products while the sums stay below 2^24).  fp16
@@ -12,12 +16,14 @@
 // would move three bytes per weight through HBM more than needed; here the int8 tile crosses HBM
 // once:
 //   warp 0      TMA producer: per stage, kW8Kb k-blocks of A tiles (128-byte swizzle) and one
-//               int8 weight box of BN rows x 64 * kW8Kb k (plain rows)
-//   warp 1      TMEM allocation and the tcgen05.mma issuer (B K-major, 128-byte swizzle)
-//   warps 2-5   epilogue: TMEM -> fp32 k-range slots (split-K), as gemm_tc's EPI_F32
-//   warps 6-13  converters: per k-block, each 16-byte int8 chunk of a weight row -> two 16-byte
-//               fp16 chunks of the K-major swizzled B slot (chunk c of row r at (c ^ (r % 8)) * 16),
-//               then a proxy fence and an arrival on the slot's "B full" barrier
+//               int8 weight box (plain rows): BN rows x 64 * kW8Kb k, or 64 * kW8Kb k rows x BN
+//   warp 1      TMEM allocation and the tcgen05.mma issuer (B 128-byte swizzle)
+//   warps 2-5   epilogue: TMEM -> fp32 k-range slots (split-K), as gemm_tc's EPI_F32, or (EPI_QROPE,
+//               one 192-column head per tile) dequant scales, RoPE and q^C, as gemm_tc's
+//   warps 6-13  converters: per k-block, each 16-byte int8 chunk -> two 16-byte fp16 chunks of the
+//               swizzled B slot (chunk c of 128-byte row r at (c ^ (r % 8)) * 16; rows are output
+//               columns (K-major) or k (MN-major, one 8 KB block per 64 columns)), then a proxy
+//               fence and an arrival on the slot's "B full" barrier
 // The int8 and A tiles run in a deep ring of stages (the weight stream's latency hiding); the
 // fp16 B tiles in a ring of two slots only (the converters stay at most one k-block ahead of the
 // tensor core), so that the shared memory goes to int8 stages in flight.  Stage s is reused only
@@ -45,11 +51,11 @@ constexpr int kW8Threads = 64 + 128 + kW8Conv;
 constexpr int kW8Kb = 2;
 static_assert(kW8Kb >= 1 && kW8Kb <= 4, "a TMA box row holds at most 256 elements");
 
-template <int BN, int MSUB, int MAXST>
+template <int BN, int MSUB, int MAXST, bool MN = false>
 struct W8Cfg {
     static constexpr int kKb = kW8Kb;
-    static constexpr int kB8Row = kBK * kKb;         // bytes per weight row per stage
-    static constexpr int kB8Stage = BN * kB8Row;     // int8: BN rows x 64 * kKb k
+    static constexpr int kB8Row = MN ? BN : kBK * kKb;   // bytes per int8 box row
+    static constexpr int kB8Stage = BN * kBK * kKb;  // int8: BN columns x 64 * kKb k
     static constexpr int kBStage = BN * kBK * 2;     // fp16: BN rows x 128 bytes
     static constexpr int kBSlots = 2;
     static constexpr int kAcc = MSUB * BN;
@@ -59,6 +65,7 @@ struct W8Cfg {
     static constexpr int kBarBytes = 1024;
     static_assert(8 * (3 * MAXST + 9) + 16 <= kBarBytes, "barrier area");
     static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
+    static_assert(!MN || BN % 64 == 0, "MN-major tiles are whole 64-column blocks");
     static_assert(kAcc <= 512, "accumulator exceeds TMEM");
     static __host__ __device__ int a_stage_bytes(int a_box_rows) { return kKb * MSUB * a_box_rows * 128; }
     static __host__ __device__ int stage_bytes(int a_box_rows) { return a_stage_bytes(a_box_rows) + kB8Stage; }
@@ -74,11 +81,12 @@ struct W8Cfg {
     static_assert(kBSlots * kBStage >= 16384, "the B slots must cover the A over-read");
 };
 
-template <int BN, int MSUB, int MAXST>
+template <int BN, int MSUB, int MAXST, bool MN = false, int EPI = EPI_F32>
 __global__ void __launch_bounds__(kW8Threads, 1)
     gemm_w8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b8,
-                   const GemmArgs args) {
-    using C = W8Cfg<BN, MSUB, MAXST>;
+                   const __grid_constant__ CUtensorMap map_b8b, const GemmArgs args) {
+    using C = W8Cfg<BN, MSUB, MAXST, MN>;
+    static_assert(EPI == EPI_F32 || (EPI == EPI_QROPE && BN == 192), "epilogues: fp32 slots, or one head per tile");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -105,6 +113,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b8);
+        if (MN) tma_prefetch_map(&map_b8b);
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
@@ -156,7 +165,16 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                     const int nkb = min(C::kKb, u.kb1 - kb);   // the unit's last stage may be short
                     const uint32_t fa = smem_u32(&full[s]), f8 = smem_u32(&full8[s]);
                     mbar_arrive_expect_tx(f8, (uint32_t)C::kB8Stage);   // the whole box lands (zeros past K)
-                    tma_load_2d(smem_u32(sB8 + (size_t)s * C::kB8Stage), &map_b8, f8, kb * kBK, u.n_tile * BN, pol_w);
+                    if constexpr (MN) {
+                        const int c0 = u.n_tile * BN;   // a tile never straddles b_split_col
+                        if (c0 < args.b_split_col)
+                            tma_load_2d(smem_u32(sB8 + (size_t)s * C::kB8Stage), &map_b8, f8, c0, kb * kBK, pol_w);
+                        else
+                            tma_load_2d(smem_u32(sB8 + (size_t)s * C::kB8Stage), &map_b8b, f8, c0 - args.b_split_col,
+                                        kb * kBK, pol_w);
+                    } else {
+                        tma_load_2d(smem_u32(sB8 + (size_t)s * C::kB8Stage), &map_b8, f8, kb * kBK, u.n_tile * BN, pol_w);
+                    }
                     mbar_arrive_expect_tx(fa, (uint32_t)(nkb * MSUB * a_box));
                     for (int i = 0; i < nkb; ++i)
                         load_a<MSUB>(args, u, kb + i, smem_u32(sA + (size_t)s * a_stage + i * MSUB * a_box), a_box, fa,
@@ -172,9 +190,11 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(128, BN, false, false);   // fp16, A and B K-major
+            // fp16, A K-major; B K-major or MN-major (64-column blocks 8 KB apart)
+            constexpr uint32_t idesc = idesc_f16_f32(128, BN, false, MN);
+            constexpr uint64_t b_step = MN ? 128 : 2;   // one K = 16 step: 16 rows, or 32 bytes of a row
             const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
-            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), MN ? 64 * 128 : 16, 1024);
             int s = 0;
             uint32_t ph = 0, ai = 0, gi = 0;   // gi: k-blocks so far (fp16 slot gi & 1, use gi >> 1)
             Unit u;
@@ -209,7 +229,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
 #pragma unroll
                             for (int ms = 0; ms < MSUB; ++ms)
                                 umma_bf16(d_base + ms * BN, a_desc + (uint64_t)(((ms * a_box) >> 4) + 2 * kk),
-                                          b_desc + (uint64_t)(2 * kk), idesc, (kb + i > u.kb0 || kk > 0) ? 1u : 0u);
+                                          b_desc + b_step * kk, idesc, (kb + i > u.kb0 || kk > 0) ? 1u : 0u);
                         umma_commit(smem_u32(&bempty[j]));
                     }
                     if (!ok) break;
@@ -243,7 +263,10 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             __syncwarp();
             tc_fence_after();
             const TmemSrc tsrc{tmem_base + ((uint32_t)(q * 32) << 16) + b * C::kAcc};
-            epilogue_f32<BN, MSUB>(args, u.m_tile * MSUB * 128 + row_in, u.n_tile, u.ks, tsrc);
+            if constexpr (EPI == EPI_QROPE)
+                epilogue_qrope<MSUB>(args, u.m_tile * MSUB * 128 + row_in, u.n_tile, tsrc);
+            else
+                epilogue_f32<BN, MSUB>(args, u.m_tile * MSUB * 128 + row_in, u.n_tile, u.ks, tsrc);
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[b]));
         }
@@ -267,11 +290,16 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                         ok = false;
                         break;
                     }
-                    const uint8_t* src = sB8 + (size_t)s * C::kB8Stage + i * kBK;
+                    // k-block i of the stage: 16 bytes of the int8 box's rows at i * kBK (K-major), or
+                    // its 64 rows from 64 i on (MN-major)
+                    const uint8_t* src = sB8 + (size_t)s * C::kB8Stage + (MN ? (size_t)i * kBK * BN : (size_t)i * kBK);
                     const uint32_t dst = smem_u32(sB + (size_t)j * C::kBStage);
 #pragma unroll 2
                     for (int task = ct; task < BN * 4; task += kW8Conv) {
-                        const int r = task >> 2, c = task & 3;   // row r, 16-byte int8 chunk c (k 16c .. 16c+15)
+                        // K-major: row r = output column, chunk c = k 16c .. 16c+15 (4 per row);
+                        // MN-major: row r = k, chunk c = columns 16c .. 16c+15 (BN / 16 per row)
+                        const int r = MN ? task / (BN / 16) : task >> 2;
+                        const int c = MN ? task % (BN / 16) : task & 3;
                         const int4 v = *reinterpret_cast<const int4*>(src + r * C::kB8Row + c * 16);
                         const uint32_t w[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
                         uint32_t o[8];
@@ -286,12 +314,14 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                             o[2 * e] = *reinterpret_cast<uint32_t*>(&hl);
                             o[2 * e + 1] = *reinterpret_cast<uint32_t*>(&hh);
                         }
-                        const uint32_t row = dst + (uint32_t)(r * 128);
+                        // the fp16 row (128 bytes) and its 16-byte chunk pair
+                        const uint32_t row = MN ? dst + (uint32_t)((c >> 2) * (64 * 128) + r * 128) : dst + (uint32_t)(r * 128);
+                        const uint32_t cc = MN ? 2u * (uint32_t)(c & 3) : 2u * (uint32_t)c;
                         const uint32_t sw = (uint32_t)(r & 7);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((2u * c) ^ sw) << 4)),
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((cc ^ sw) << 4)),
                                      "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
                                      : "memory");
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((2u * c + 1) ^ sw) << 4)),
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((cc + 1) ^ sw) << 4)),
                                      "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
                                      : "memory");
                     }

@@ -3,10 +3,12 @@
 //
 // Pipeline of one call (all kernels on the caller's stream, chained with programmatic
 // dependent launch so each grid's prologue overlaps the previous grid's tail):
-//   [int8 operands only] widen int8 tokenX / weights to bf16 in the workspace
-//   K1  x . [W^DQ | W^DKV | W^KR]        -> fp32 partials (decode) or fp32 rows (prefill)
-//   F1  sum partials, RmsNorm, RoPE(k^R), kv/kr cache writes, c^Q (bf16 or int8 codes)
-//   K2  c^Q . W^UqQr                      -> fp32 partials + F2 (decode), or fused RoPE epilogue
+//   [int8 tokenX only] widen the int8 codes of tokenX to fp16 in the workspace
+//   K1  x . [W^DQ | W^DKV | W^KR]        -> fp32 partials (decode) or fp32 rows (prefill); int8
+//                                           weights stream as int8 and are widened in shared memory
+//   F1  sum partials, RmsNorm, RoPE(k^R), kv/kr cache writes, c^Q (bf16, or int8 codes as fp16)
+//   K2  c^Q . W^UqQr                      -> fused RoPE epilogue, or (int8 W^UqQr, widened in
+//                                           shared memory) fp32 rows + F2
 //   K3  q^C[:, n, :] . W^UK[n] per head   -> queryOut bf16, or int8 + dequantScaleQNope
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -238,8 +240,7 @@ struct Plan {
     int p_n1 = 0, p_s1 = 0, p_wst = 0, p_arows = 0, p_na3 = 0, p_pf = 0;
     size_t p_smem = 0, off_pbar = 0;
     int64_t ncols1 = 0, ncols2 = 0;
-    size_t off_cq = 0, off_cqs = 0, off_qc = 0, off_y1 = 0, off_y2 = 0, off_xb = 0, off_wdq = 0, off_wdkvkr = 0,
-           off_wuqqr = 0, bytes = 0;
+    size_t off_cq = 0, off_cqs = 0, off_qc = 0, off_y1 = 0, off_y2 = 0, off_xb = 0, bytes = 0;
 };
 
 constexpr size_t kStatusBytes = 1024;
@@ -290,9 +291,12 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     // Down-projection: at decode, 64-column tiles x k ranges; two 128-row sub-tiles use
     // 192-column tiles; prefill 256-column tiles (2112 columns: nine tiles per 256 rows, so that
     // 8192 tokens make two waves on 152 SMs instead of three).
-    plan_gemm(p.g1, T, p.ncols1, d.He, sms, T <= 128 ? 64 : (T <= kDecodeRows ? 192 : 256), true);
+    // int8 weights (widened in shared memory, MN-major int8 boxes of one BN-byte row per k): 192
+    // columns per tile (a tile must not straddle W^DQ | W^DkvKr)
+    const int bn1_i8 = d.Hcq % 192 == 0 ? 192 : 64;
+    plan_gemm(p.g1, T, p.ncols1, d.He, sms, sc.x_i8 ? bn1_i8 : (T <= 128 ? 64 : (T <= kDecodeRows ? 192 : 256)), true);
     // prefill: 256 x 256 tiles on SM pairs (W^DQ's columns split into whole 128-column halves)
-    p.g1_pair = p.g1.bn == 256 && p.g1.ksplit == 1 && d.Hcq % 128 == 0 && (d.Hckv + d.Dr) % 64 == 0 &&
+    p.g1_pair = !sc.x_i8 && p.g1.bn == 256 && p.g1.ksplit == 1 && d.Hcq % 128 == 0 && (d.Hckv + d.Dr) % 64 == 0 &&
                 (d.He / 64) % kPairKps == 0 && p.ncols1 % 4 == 0;
     if (p.g1_pair) {
         p.g1.msub = 2;
@@ -373,12 +377,7 @@ Plan make_plan(const Dims& d, const Scenario& sc, int sms) {
     // per P1 tile: a flag and a counter; per 16-column c^Q chunk: a flag and T sums of squares
     if (p.persist) p.off_pbar = take((size_t)p.p_n1 * (8 + 4) + 8 + (size_t)(d.Hcq / kPChunk) * (8 + 4 * T));
     if (!p.g2_fused) p.off_y2 = take((size_t)T * p.ncols2 * 4);
-    if (sc.x_i8) {
-        p.off_xb = take((size_t)T * d.He * 2);
-        p.off_wdq = take((size_t)d.He * d.Hcq * 2);
-        p.off_wdkvkr = take((size_t)d.He * (d.Hckv + d.Dr) * 2);
-    }
-    if (sc.uqqr_i8) p.off_wuqqr = take((size_t)d.Hcq * p.ncols2 * 2);
+    if (sc.x_i8) p.off_xb = take((size_t)T * d.He * 2);   // tokenX's int8 codes as fp16
     p.bytes = off;
     return p;
 }
@@ -556,6 +555,37 @@ cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const C
     return launch(k, grid, gemm_threads(EPW), smem, st, a, b0, b1, mo, mo2, args);
 }
 
+// Launches one int8-weight GEMM instantiation (gemm_w8.cuh); b8b holds the columns from
+// args.b_split_col on (MN-major only).
+template <int BN, int MSUB, int MAXST, bool MN = false, int EPI = EPI_F32>
+cudaError_t launch_gemm_w8(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b8,
+                           const CUtensorMap& b8b, GemmArgs args) {
+    using C = W8Cfg<BN, MSUB, MAXST, MN>;
+    auto k = gemm_w8_kernel<BN, MSUB, MAXST, MN, EPI>;
+    args.stages = C::max_stages(args.a_box_rows);
+    if (args.stages < 2) return cudaErrorInvalidConfiguration;
+    cudaError_t e = set_attr(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+    if (e != cudaSuccess) return e;
+    return launch(k, grid, kW8Threads, C::smem_bytes(args.stages, args.a_box_rows), st, a, b8, b8b, args);
+}
+template <int BN, int MSUB, int MAXST>
+cudaError_t launch_gemm_w8(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b8, GemmArgs args) {
+    return launch_gemm_w8<BN, MSUB, MAXST, false>(grid, st, a, b8, b8, args);
+}
+
+// int8 (K, cols) row-major weight in the (k, n) orientation: boxes of box_cols columns (one
+// box_cols-byte row per k, no swizzle) x 64 * kW8Kb k rows; rows and columns past the end read
+// as zero.
+bool map_w8_cols(CUtensorMap* m, const void* base, uint64_t K, uint64_t cols, uint32_t box_cols) {
+    const cuuint64_t gd[2] = {cols, K};
+    const cuuint64_t gs[1] = {cols};
+    const cuuint32_t bx[2] = {box_cols, (cuuint32_t)(64 * kW8Kb)};
+    const cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gd, gs, bx, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Launches one pair-CTA GEMM instantiation (clusters of two CTAs): as many pairs as the GPU
 // holds at once, at most one per 256-row tile.
 template <int BN, int MAXST, int EPI, int OUTB, int EPW, int KPS>
@@ -668,33 +698,21 @@ mla_status run(const Launched& L) {
     SideStream* side = nullptr;   // set once work is forked onto the side stream
     std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
 
-    // int8 operands are widened to bf16 (exact) for the bf16 tensor-core path.
+    // int8 tokenX: its codes widened to fp16 (exact), the A operand of the int8-weight GEMM; the
+    // int8 weights stay int8 in HBM and are widened in shared memory.
     const void* x_bf = a.x->data;
     const void* wdq_bf = a.wdq->data;
     const void* wdkvkr_bf = a.wdkvkr->data;
     const void* wuqqr_bf = a.wuqqr->data;
-    auto widen = [&](const void* src, size_t off, long long n) -> cudaError_t {
+    if (sc.x_i8) {
+        const long long n = (long long)d.T * d.He;
         const long long blocks = (n / 16 + 255) / 256;
         const int grid = (int)(blocks < 4096 ? (blocks > 0 ? blocks : 1) : 4096);
-        return launch(convert_i8_to_bf16_kernel, grid, 256, 0, st, reinterpret_cast<const int8_t*>(src),
-                      reinterpret_cast<__nv_bfloat16*>(ws + off), n);
-    };
-    if (sc.x_i8) {
-        if (widen(a.x->data, p.off_xb, (long long)d.T * d.He) != cudaSuccess) return MLA_ERR_RUNTIME;
-        timing_mark(st, "widen_x");
-        if (widen(a.wdq->data, p.off_wdq, (long long)d.He * d.Hcq) != cudaSuccess) return MLA_ERR_RUNTIME;
-        timing_mark(st, "widen_w_dq");
-        if (widen(a.wdkvkr->data, p.off_wdkvkr, (long long)d.He * (d.Hckv + d.Dr)) != cudaSuccess)
+        if (launch(convert_i8_to_f16_kernel, grid, 256, 0, st, static_cast<const int8_t*>(a.x->data),
+                   reinterpret_cast<__half*>(ws + p.off_xb), n) != cudaSuccess)
             return MLA_ERR_RUNTIME;
-        timing_mark(st, "widen_w_dkvkr");
+        timing_mark(st, "widen_x");
         x_bf = ws + p.off_xb;
-        wdq_bf = ws + p.off_wdq;
-        wdkvkr_bf = ws + p.off_wdkvkr;
-    }
-    if (sc.uqqr_i8) {
-        if (widen(a.wuqqr->data, p.off_wuqqr, (long long)d.Hcq * p.ncols2) != cudaSuccess) return MLA_ERR_RUNTIME;
-        timing_mark(st, "widen_w_uqqr");
-        wuqqr_bf = ws + p.off_wuqqr;
     }
 
     DownArgs f1 = {};
@@ -826,6 +844,26 @@ mla_status run(const Launched& L) {
 
     // ---- K1: down-projection x . [W^DQ | W^DKV | W^KR] -> fp32 rows Y1
     CUtensorMap mA1, mB1a, mB1b;
+    if (sc.x_i8) {
+        // int8 weights streamed as int8 and widened in shared memory (fp16 x fp16 -> fp32, exact
+        // integer sums); F1 applies tokenX's and the weights' dequant scales
+        constexpr int BN = 192;
+        if (p.g1.bn != BN && p.g1.bn != 64) return MLA_ERR_TILING;
+        if (!map_2d(&mA1, x_bf, d.T, d.He, (uint32_t)p.g1.a_box_rows) ||
+            !map_w8_cols(&mB1a, a.wdq->data, d.He, d.Hcq, (uint32_t)p.g1.bn) ||
+            !map_w8_cols(&mB1b, a.wdkvkr->data, d.He, d.Hckv + d.Dr, (uint32_t)p.g1.bn))
+            return MLA_ERR_RUNTIME;
+        GemmArgs g1 = gemm_args(p.g1, T, p.ncols1, status);
+        g1.b_split_col = (int)d.Hcq;
+        g1.clear_status = 1;
+        g1.out_f32 = y1;
+        if (p.g1.bn == BN)
+            e = p.g1.msub == 1 ? launch_gemm_w8<BN, 1, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
+                               : launch_gemm_w8<BN, 2, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+        else
+            e = p.g1.msub == 1 ? launch_gemm_w8<64, 1, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
+                               : launch_gemm_w8<64, 2, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+    } else {
     // Whole-K 256-row tiles store their fp32 rows through shared memory with TMA (32 x 32
     // boxes of the T x ncols1 matrix); k ranges (decode) use plain stores into their slots.
     const bool tma1 = p.g1.ksplit == 1 && p.g1.msub == 2 && p.ncols1 % 4 == 0;
@@ -847,8 +885,7 @@ mla_status run(const Launched& L) {
     GemmArgs g1 = gemm_args(p.g1, T, p.ncols1, status);
     g1.b_split_col = (int)d.Hcq;
     g1.clear_status = 1;
-    g1.a_ready = sc.x_i8 ? 0 : 1;   // bf16 tokenX is read as passed; int8 is widened first
-    g1.b_late = sc.x_i8 ? 1 : 0;    // so are int8 weights
+    g1.a_ready = 1;   // bf16 tokenX is read as passed
     g1.a_one_box = big1 ? 1 : 0;
     g1.b_blocks = big1 ? 1 : 0;
     CUtensorMap mO1;
@@ -882,6 +919,7 @@ mla_status run(const Launched& L) {
                                   : launch_gemm<256, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1))
                            : (g1.tma_out ? launch_gemm<192, 2, 4, EPI_F32, 2>(p.g1.grid, st, mA1, mB1a, mB1b, g1, &mO1)
                                          : launch_gemm<192, 2, 4, EPI_F32>(p.g1.grid, st, mA1, mB1a, mB1b, g1));
+    }
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "k1_down_proj");
 
@@ -929,12 +967,16 @@ mla_status run(const Launched& L) {
         if (!map_colblocks(&mA2, ws + p.off_cq, d.T, d.Hcq, 128, kPairKps) ||
             !map_colblocks(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64 * kPairKps, 2))
             return MLA_ERR_RUNTIME;
+    } else if (sc.uqqr_i8) {
+        // int8 W^UqQr streamed as int8 and widened in shared memory; c^Q's int8 codes as fp16
+        if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
+            !map_w8_cols(&mB2, a.wuqqr->data, d.Hcq, p.ncols2, 192))
+            return MLA_ERR_RUNTIME;
     } else if (!map_2d(&mA2, ws + p.off_cq, d.T, d.Hcq, (uint32_t)p.g2.a_box_rows) ||
                !map_2d(&mB2, wuqqr_bf, d.Hcq, p.ncols2, 64)) {
         return MLA_ERR_RUNTIME;
     }
     GemmArgs g2 = gemm_args(p.g2, T, p.ncols2, status);
-    g2.b_late = sc.uqqr_i8 ? 1 : 0;   // a widened int8 W^UqQr is written by this call
     g2.a_one_box = p.g2_wide ? 1 : 0;
     g2.b_blocks = p.g2_wide ? 1 : 0;
     CUtensorMap mO2c, mO2r;
@@ -961,7 +1003,17 @@ mla_status run(const Launched& L) {
     g2.row_scale = row_scale;
     g2.col_scale = col_scale;
     g2.out_f32 = reinterpret_cast<float*>(ws + p.off_y2);
-    if (p.g2_fused) {
+    if (sc.uqqr_i8) {
+        if (p.g2.bn != 192) return MLA_ERR_TILING;
+        g2.b_split_col = (int)p.ncols2;   // every column from the one map
+        if (p.g2_fused)
+            e = (p.g2.msub == 1)
+                    ? launch_gemm_w8<192, 1, 16, true, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2)
+                    : launch_gemm_w8<192, 2, 16, true, EPI_QROPE>(p.g2.grid, st, mA2, mB2, mB2, g2);
+        else
+            e = (p.g2.msub == 1) ? launch_gemm_w8<192, 1, 16, true>(p.g2.grid, st, mA2, mB2, mB2, g2)
+                                 : launch_gemm_w8<192, 2, 16, true>(p.g2.grid, st, mA2, mB2, mB2, g2);
+    } else if (p.g2_fused) {
         if (p.g2_wide)
             e = launch_gemm_pair<256, 8, EPI_QROPE, 1, 2, kPairKps>(st, mA2, mB2, mB2, g2, mO2c, mO2r);
         else if (p.g2.msub == 1)

@@ -56,17 +56,6 @@ bool map_w8_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, ui
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MSUB, int MAXST>
-cudaError_t launch_gemm_w8(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b8, GemmArgs args) {
-    using C = W8Cfg<BN, MSUB, MAXST>;
-    auto k = gemm_w8_kernel<BN, MSUB, MAXST>;
-    args.stages = C::max_stages(args.a_box_rows);
-    if (args.stages < 2) return cudaErrorInvalidConfiguration;
-    cudaError_t e = set_attr(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
-    if (e != cudaSuccess) return e;
-    return launch(k, grid, kW8Threads, C::smem_bytes(args.stages, args.a_box_rows), st, a, b8, args);
-}
-
 mla_status pp_validate(const PpArgs& a, PpDims& d) {
     const mla_tensor* req[] = {a.x,  a.g0,  a.b0, a.qs0, a.qo0, a.w1,  a.de0,   a.g1,   a.b1,    a.qs1,
                                a.qo1, a.w2, a.de1, a.g2,  a.cos, a.sin, a.wuk, a.kv, a.slots, a.qout, a.kv_out};

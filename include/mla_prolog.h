@@ -230,8 +230,8 @@ MLA_API mla_status mla_prolog_timing_read(mla_kernel_time* out, int capacity, in
  *
  * - Size limit: calls whose workspace (as mla_prolog_workspace_size reports it) exceeds
  *   MLA_NO_ALLOC_SCRATCH_BYTES return MLA_ERR_SCRATCH_LIMIT and launch nothing.  16 MiB
- *   covers bf16 decode batches of up to 128 tokens with DeepSeek-V3 shapes; int8-input
- *   calls (which widen the int8 weights into the workspace) do not fit.
+ *   covers bf16 decode batches of up to 128 tokens with DeepSeek-V3 shapes; prefill-sized
+ *   calls (hundreds of tokens and more) do not fit.
  * - No allocation: the call makes no cudaMalloc / cudaFree and no allocating library call.
  *   The first call on each device looks up the scratch buffer's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call before any
