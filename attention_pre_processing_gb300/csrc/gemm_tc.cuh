@@ -453,9 +453,10 @@ struct OutStage {
     }
 };
 
-// fp32 product rows (EPI_F32, ksplit = 1) through shared memory and TMA stores: 32-row x
-// 32-column (128-byte) boxes of the T x ncols matrix; rows and columns past its extent are not
-// written.
+// fp32 product rows (EPI_F32) through shared memory and TMA stores: 32-row x 32-column (128-byte)
+// boxes of the T x ncols matrix; rows and columns past its extent are not written.  With k ranges
+// the map spans the ksplit slots (ksplit * T rows) and slot ks starts at row ks * T: T must then be
+// a multiple of 32, so that no box crosses into the next slot.
 template <int BN, int MSUB, int OUTB, int EPW = 1>
 __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const Unit& u, const TmemSrc& src, int q,
                                                  OutStage<OUTB>& out, int part = 0) {
@@ -470,7 +471,7 @@ __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const Unit& 
             uint32_t w[32];
             tmem_ld_32x32b_x32(src.tacc + ms * BN + ch * 32, w);
             tmem_ld_wait();
-            out.put(w, col, row0);
+            out.put(w, col, u.ks * a.T + row0);
         }
     }
 }

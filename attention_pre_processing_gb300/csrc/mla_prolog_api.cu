@@ -864,9 +864,10 @@ mla_status run(const Launched& L) {
             e = p.g1.msub == 1 ? launch_gemm_w8<64, 1, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
                                : launch_gemm_w8<64, 2, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
     } else {
-    // Whole-K 256-row tiles store their fp32 rows through shared memory with TMA (32 x 32
-    // boxes of the T x ncols1 matrix); k ranges (decode) use plain stores into their slots.
-    const bool tma1 = p.g1.ksplit == 1 && p.g1.msub == 2 && p.ncols1 % 4 == 0;
+    // 256-row tiles store their fp32 rows through shared memory with TMA (32 x 32 boxes of the
+    // T x ncols1 matrix, or of the ksplit slots stacked when T is a multiple of 32); other k
+    // ranges use plain stores into their slots.
+    const bool tma1 = p.g1.msub == 2 && p.ncols1 % 4 == 0 && (p.g1.ksplit == 1 || d.T % 32 == 0);
     // 256-column tiles: one 256-row activation box and one column-blocked weight box per k-block
     const bool big1 = !p.g1_pair && p.g1.bn == 256 && d.Hcq % 256 == 0 && (d.Hckv + d.Dr) % 64 == 0;
     if (p.g1_pair) {
@@ -890,7 +891,7 @@ mla_status run(const Launched& L) {
     g1.b_blocks = big1 ? 1 : 0;
     CUtensorMap mO1;
     if (tma1) {
-        const uint64_t dims[2] = {(uint64_t)p.ncols1, (uint64_t)d.T};
+        const uint64_t dims[2] = {(uint64_t)p.ncols1, (uint64_t)d.T * (uint64_t)p.g1.ksplit};
         const uint64_t strides[1] = {(uint64_t)p.ncols1 * 4};
         const uint32_t box[2] = {32, 32};
         g1.tma_out = encode_map(&mO1, y1, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ? 1 : 0;
