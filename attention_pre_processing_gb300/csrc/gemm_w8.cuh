@@ -139,7 +139,11 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     const uint32_t tmem_base = *s_tmem;
 
     pdl_launch_dependents();
-    pdl_wait();   // A and W are both written by earlier kernels of the call
+    // The weights are inputs of the call: the producer requests its first ring of int8 weight
+    // tiles before waiting for the previous kernel (its activation tiles after), and the
+    // converters, which touch shared memory only, widen them meanwhile.  The MMA and epilogue
+    // warps wait here.
+    if (warp >= 1 && warp < 6) pdl_wait();
     if (args.clear_status && blockIdx.x == 0 && threadIdx.x == 64) *args.status = 0u;
 
     auto fail = [&]() {
@@ -156,29 +160,50 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             uint32_t ph = 0;
             Unit u;
             bool ok = true;
+            // one stage: the int8 weight box (the whole box lands, zeros past K) ...
+            auto issue_w = [&](int st, const Unit& uu, int kb) {
+                const uint32_t f8 = smem_u32(&full8[st]);
+                const uint32_t dst = smem_u32(sB8 + (size_t)st * C::kB8Stage);
+                mbar_arrive_expect_tx(f8, (uint32_t)C::kB8Stage);
+                if constexpr (MN) {
+                    const int c0 = uu.n_tile * BN;   // a tile never straddles b_split_col
+                    if (c0 < args.b_split_col)
+                        tma_load_2d(dst, &map_b8, f8, c0, kb * kBK, pol_w);
+                    else
+                        tma_load_2d(dst, &map_b8b, f8, c0 - args.b_split_col, kb * kBK, pol_w);
+                } else {
+                    tma_load_2d(dst, &map_b8, f8, kb * kBK, uu.n_tile * BN, pol_w);
+                }
+            };
+            // ... and its activation tiles (the unit's last stage may be short)
+            auto issue_a = [&](int st, const Unit& uu, int kb) {
+                const int nkb = min(C::kKb, uu.kb1 - kb);
+                const uint32_t fa = smem_u32(&full[st]);
+                mbar_arrive_expect_tx(fa, (uint32_t)(nkb * MSUB * a_box));
+                for (int i = 0; i < nkb; ++i)
+                    load_a<MSUB>(args, uu, kb + i, smem_u32(sA + (size_t)st * a_stage + i * MSUB * a_box), a_box, fa,
+                                 &map_a, pol_a);
+            };
+            if (args.b_late) pdl_wait();   // the weights come from an earlier kernel of the call
+            int pre = 0;
+            Unit u0;
+            if (get_unit(args, 0, u0)) {
+                const int n0 = (u0.kb1 - u0.kb0 + C::kKb - 1) / C::kKb;
+                pre = n0 < stages ? n0 : stages;
+                for (int i = 0; i < pre; ++i) issue_w(i, u0, u0.kb0 + i * C::kKb);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i) issue_a(i, u0, u0.kb0 + i * C::kKb);
+            s = pre % stages;
+            ph = (pre == stages) ? 1u : 0u;
             for (int idx = 0; ok && get_unit(args, idx, u); ++idx) {
-                for (int kb = u.kb0; kb < u.kb1; kb += C::kKb) {
+                for (int kb = u.kb0 + (idx == 0 ? pre * C::kKb : 0); kb < u.kb1; kb += C::kKb) {
                     if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, s_abort, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
-                    const int nkb = min(C::kKb, u.kb1 - kb);   // the unit's last stage may be short
-                    const uint32_t fa = smem_u32(&full[s]), f8 = smem_u32(&full8[s]);
-                    mbar_arrive_expect_tx(f8, (uint32_t)C::kB8Stage);   // the whole box lands (zeros past K)
-                    if constexpr (MN) {
-                        const int c0 = u.n_tile * BN;   // a tile never straddles b_split_col
-                        if (c0 < args.b_split_col)
-                            tma_load_2d(smem_u32(sB8 + (size_t)s * C::kB8Stage), &map_b8, f8, c0, kb * kBK, pol_w);
-                        else
-                            tma_load_2d(smem_u32(sB8 + (size_t)s * C::kB8Stage), &map_b8b, f8, c0 - args.b_split_col,
-                                        kb * kBK, pol_w);
-                    } else {
-                        tma_load_2d(smem_u32(sB8 + (size_t)s * C::kB8Stage), &map_b8, f8, kb * kBK, u.n_tile * BN, pol_w);
-                    }
-                    mbar_arrive_expect_tx(fa, (uint32_t)(nkb * MSUB * a_box));
-                    for (int i = 0; i < nkb; ++i)
-                        load_a<MSUB>(args, u, kb + i, smem_u32(sA + (size_t)s * a_stage + i * MSUB * a_box), a_box, fa,
-                                     &map_a, pol_a);
+                    issue_w(s, u, kb);
+                    issue_a(s, u, kb);
                     if (++s == stages) {
                         s = 0;
                         ph ^= 1;
