@@ -79,7 +79,9 @@ struct GemmArgs {
     int tma_out;                   // store the output through shared memory with TMA (map_o, map_o2)
     int a_one_box;                 // one A box spans all MSUB x 128 rows (map_a box height MSUB*128)
     int b_blocks;                  // the B maps are 3D (64 columns, k, 64-column blocks): one box
-                                   // brings all BN/64 column blocks of a k-block
+                                   // brings all BN/64 column blocks of a k-block; in head_mode the
+                                   // k rows of head n start at n * head_rows
+    int head_rows;                 // head_mode with b_blocks: weight rows per head (D)
     int n_fastest;                 // pair tiles: column tile fastest (the row tiles of A then come
                                    // from HBM once, shared by the pairs of all column tiles)
     // EPI_DOWN (prefill down-projection): columns below cq_cols leave as bf16(gamma_cq * y)
@@ -211,6 +213,12 @@ struct TmemSrc {
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = bits_f(r[i]);
+    }
+    // 128 consecutive columns: four loads in flight, one wait
+    __device__ __forceinline__ void load128(int col, uint32_t (&r)[4][32]) const {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) tmem_ld_32x32b_x32(tacc + col + 32 * h, r[h]);
+        tmem_ld_wait();
     }
 };
 
@@ -777,13 +785,12 @@ __device__ __forceinline__ void epilogue_qn_split(const GemmArgs& a, const Unit&
 #pragma unroll 1
     for (int j = part; any && j < BN / 128; j += EPW) {
         if (c0 + 128 * j >= a.Hckv) break;
-#pragma unroll 1
-        for (int h = 0; h < 4; ++h) {
-            float v[32];
-            src.load(0, BN, 128 * j + 32 * h, v);
+        uint32_t r[4][32];
+        src.load128(128 * j, r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
-        }
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(bits_f(r[h][i])));
     }
     const int rin = q * 32 + out.lane;
     xbuf[part * 128 + rin] = m;
@@ -800,15 +807,16 @@ __device__ __forceinline__ void epilogue_qn_split(const GemmArgs& a, const Unit&
         const int col = 128 * j;
         if (c0 + col >= a.Hckv) break;
         uint32_t w[32];
+        uint32_t r[4][32];
+        src.load128(col, r);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-            float v[32];
-            src.load(0, BN, col + 32 * h, v);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 uint32_t packed = 0;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) packed |= ((uint32_t)(quant_i8(v[4 * i + e] * inv) & 0xFF)) << (8 * e);
+                for (int e = 0; e < 4; ++e)
+                    packed |= ((uint32_t)(quant_i8(bits_f(r[h][4 * i + e]) * inv) & 0xFF)) << (8 * e);
                 w[8 * h + i] = packed;
             }
         }
@@ -830,6 +838,11 @@ __device__ __forceinline__ void load_b(const GemmArgs& a, const Unit& u, int kb,
         c0 = (u.n_tile % a.tiles_per_head) * BN;
     } else {
         c0 = u.n_tile * BN;
+    }
+    if (a.head_mode && a.b_blocks) {
+        // one box: BN/64 column blocks of 64 x (64 * KPS) rows of head `head`
+        tma_load_3d(dst, b0, bar, 0, head * a.head_rows + kb * kBK, c0 / 64, pol);
+        return;
     }
     if (!a.head_mode && a.b_blocks) {
         // one box: BN/64 column blocks of 64 x (64 * KPS), laid out block after block (a tile

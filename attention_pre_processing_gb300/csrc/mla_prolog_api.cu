@@ -756,16 +756,25 @@ mla_status run(const Launched& L) {
     // Row tiles of 128 tokens take both k-blocks of D = 128 in one stage.
     CUtensorMap mA3, mB3;
     const bool kps3 = !sc.q_i8 && p.g3.m_tiles > 1 && p.g3.kblocks % 2 == 0;   // 512-column int8 tiles: no room
+    const bool blocks3 = d.D % 64 == 0 && d.Hckv % 64 == 0;   // whole-k-block boxes of all column blocks
     const uint32_t a3_rows = (uint32_t)p.g3.a_box_rows;
     {
         const uint64_t dims[3] = {(uint64_t)d.D, (uint64_t)d.N, (uint64_t)d.T};
         const uint64_t strides[2] = {(uint64_t)d.D * 2, (uint64_t)d.N * d.D * 2};
         const uint32_t box[3] = {64, 1, a3_rows};
         if (!encode_map(&mA3, qc, 3, dims, strides, box)) return MLA_ERR_RUNTIME;
-        const uint64_t dimsb[3] = {(uint64_t)d.Hckv, (uint64_t)d.D, (uint64_t)d.N};
-        const uint64_t stridesb[2] = {(uint64_t)d.Hckv * 2, (uint64_t)d.D * d.Hckv * 2};
-        const uint32_t boxb[3] = {64, kps3 ? 128u : 64u, 1};
-        if (!encode_map(&mB3, a.wuk->data, 3, dimsb, stridesb, boxb)) return MLA_ERR_RUNTIME;
+        if (blocks3) {
+            // W^UK as (64 columns, N * D rows, Hckv / 64 blocks): one box per stage brings every
+            // column block of the tile (8 KB boxes move far fewer bytes per SM per second)
+            if (!map_colblocks(&mB3, a.wuk->data, (uint64_t)d.N * d.D, d.Hckv, kps3 ? 128u : 64u,
+                               (uint32_t)(p.g3.bn / 64)))
+                return MLA_ERR_RUNTIME;
+        } else {
+            const uint64_t dimsb[3] = {(uint64_t)d.Hckv, (uint64_t)d.D, (uint64_t)d.N};
+            const uint64_t stridesb[2] = {(uint64_t)d.Hckv * 2, (uint64_t)d.D * d.Hckv * 2};
+            const uint32_t boxb[3] = {64, kps3 ? 128u : 64u, 1};
+            if (!encode_map(&mB3, a.wuk->data, 3, dimsb, stridesb, boxb)) return MLA_ERR_RUNTIME;
+        }
     }
 
     if (p.persist) {
@@ -1050,6 +1059,8 @@ mla_status run(const Launched& L) {
     // ---- K3: per-head W^UK contraction
     GemmArgs g3 = gemm_args(p.g3, T, d.Hckv, status);
     g3.head_mode = 1;
+    g3.b_blocks = blocks3 ? 1 : 0;
+    g3.head_rows = (int)d.D;
     g3.tiles_per_head = p.g3.n_tiles / (int)d.N;
     g3.N = (int)d.N;
     g3.Hckv = (int)d.Hckv;
