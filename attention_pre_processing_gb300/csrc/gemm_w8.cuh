@@ -25,8 +25,10 @@
 //               columns (K-major) or k (MN-major, one 8 KB block per 64 columns)), then a proxy
 //               fence and an arrival on the slot's "B full" barrier
 // The int8 and A tiles run in a deep ring of stages (the weight stream's latency hiding); the
-// fp16 B tiles in a ring of two slots only (the converters stay at most one k-block ahead of the
-// tensor core), so that the shared memory goes to int8 stages in flight.  Stage s is reused only
+// fp16 B tiles in a ring of kBSlots slots: with two, each k-block paid its conversion and the
+// MMAs' completion one after the other (~0.39 us per k-block at BN = 64, measured with
+// globaltimer stamps), so the ring is as deep as the shared memory allows (8 slots of 8 KB at
+// BN = 64, 4 of 24 KB at BN = 192; 2 with 256-row tiles, whose activation stages are large).  Stage s is reused only
 // after the MMAs that read it commit (empty[s]), which follows its conversion; slot j only after
 // the MMAs that read it commit (bempty[j]).  Every wait is bounded and sets kStatusWaitTimeout.
 #pragma once
@@ -57,13 +59,13 @@ struct W8Cfg {
     static constexpr int kB8Row = MN ? BN : kBK * kKb;   // bytes per int8 box row
     static constexpr int kB8Stage = BN * kBK * kKb;  // int8: BN columns x 64 * kKb k
     static constexpr int kBStage = BN * kBK * 2;     // fp16: BN rows x 128 bytes
-    static constexpr int kBSlots = 2;
+    static constexpr int kBSlots = MSUB == 1 ? (BN <= 64 ? 8 : 4) : 2;   // fp16 B slots
     static constexpr int kAcc = MSUB * BN;
     static constexpr int kNBuf = (2 * kAcc <= 512) ? 2 : 1;
     static constexpr int kTmemCols = (kNBuf * kAcc <= 32) ? 32 : (kNBuf * kAcc <= 64) ? 64
                                      : (kNBuf * kAcc <= 128) ? 128 : (kNBuf * kAcc <= 256) ? 256 : 512;
     static constexpr int kBarBytes = 1024;
-    static_assert(8 * (3 * MAXST + 9) + 16 <= kBarBytes, "barrier area");
+    static_assert(8 * (3 * MAXST + 2 * kBSlots + 5) + 16 <= kBarBytes, "barrier area");
     static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
     static_assert(!MN || BN % 64 == 0, "MN-major tiles are whole 64-column blocks");
     static_assert(kAcc <= 512, "accumulator exceeds TMEM");
@@ -93,9 +95,9 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     uint64_t* full = bars;                 // A tile landed (TMA)
     uint64_t* empty = bars + MAXST;        // the stage's MMAs completed
     uint64_t* full8 = bars + 2 * MAXST;    // int8 weight tile landed (TMA)
-    uint64_t* bfull = bars + 3 * MAXST;    // fp16 slot written by the converters (2)
-    uint64_t* bempty = bfull + 2;          // fp16 slot's MMAs completed (2)
-    uint64_t* tfull = bempty + 2;
+    uint64_t* bfull = bars + 3 * MAXST;    // fp16 slot written by the converters [kBSlots]
+    uint64_t* bempty = bfull + C::kBSlots; // fp16 slot's MMAs completed [kBSlots]
+    uint64_t* tfull = bempty + C::kBSlots;
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tempty + 2;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
@@ -119,9 +121,11 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             mbar_init(smem_u32(&empty[s]), 1);
             mbar_init(smem_u32(&full8[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kBSlots; ++b) {
             mbar_init(smem_u32(&bfull[b]), kW8Conv);
             mbar_init(smem_u32(&bempty[b]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
             mbar_init(smem_u32(&tempty[b]), 128);
         }
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
             const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), MN ? 64 * 128 : 16, 1024);
             int s = 0;
-            uint32_t ph = 0, ai = 0, gi = 0;   // gi: k-blocks so far (fp16 slot gi & 1, use gi >> 1)
+            uint32_t ph = 0, ai = 0, gi = 0;   // gi: k-blocks so far (fp16 slot gi % kBSlots)
             Unit u;
             bool ok = true;
             for (int idx = 0; ok && get_unit(args, idx, u); ++idx, ++ai) {
@@ -240,8 +244,8 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                         break;
                     }
                     for (int i = 0; i < nkb; ++i, ++gi) {
-                        const int j = (int)(gi & 1u);
-                        if (!mbar_wait(smem_u32(&bfull[j]), (gi >> 1) & 1u, s_abort, kWaitLimitNs)) {
+                        const int j = (int)(gi % C::kBSlots);
+                        if (!mbar_wait(smem_u32(&bfull[j]), (gi / C::kBSlots) & 1u, s_abort, kWaitLimitNs)) {
                             ok = false;
                             break;
                         }
@@ -310,8 +314,8 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                     break;
                 }
                 for (int i = 0; i < nkb; ++i, ++gi) {
-                    const int j = (int)(gi & 1u);
-                    if (!mbar_wait(smem_u32(&bempty[j]), ((gi >> 1) & 1u) ^ 1u, s_abort, kWaitLimitNs)) {
+                    const int j = (int)(gi % C::kBSlots);
+                    if (!mbar_wait(smem_u32(&bempty[j]), ((gi / C::kBSlots) & 1u) ^ 1u, s_abort, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
