@@ -139,8 +139,11 @@ PpPlan pp_plan(const PpDims& d, int sms) {
     const int64_t T = d.T;
     p.n1 = d.Hcq + d.Hckv + d.Dr;
     p.n2 = d.N * (d.D + d.Dr);
-    // the down-projection: 64-column tiles x k ranges up to 128 tokens, 192-column tiles above
-    plan_gemm(p.g1, T, p.n1, d.He, sms, T <= 128 ? 64 : 192, true);
+    // the down-projection: 128-column tiles x k ranges up to 128 tokens (17 x 8 at 2112 columns:
+    // 14 k-blocks per CTA; with 64-column tiles each CTA walked 28, and the pipeline's per-k-block
+    // latency, not the bytes, set the time: 21.5 -> 17.4 us per launch at T = 32), 192-column
+    // tiles above
+    plan_gemm(p.g1, T, p.n1, d.He, sms, T <= 128 ? 128 : 192, true);
     // the up-projection: 192-column tiles, whole K
     plan_gemm(p.g2, T, p.n2, d.Hcq, sms, 192, false);
     // W^UK: up to 128 tokens one 512-column tile per head (N tiles: one wave on the SMs for
@@ -205,7 +208,7 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
     GemmArgs g1 = gemm_args(p.g1, T, p.n1, status);
     g1.clear_status = 1;
     g1.out_f32 = y1;
-    e = p.g1.bn == 64 ? launch_gemm_w8<64, 1, 16>(p.g1.grid, st, mA1, mB1, g1)
+    e = p.g1.bn == 128 ? launch_gemm_w8<128, 1, 16>(p.g1.grid, st, mA1, mB1, g1)
                       : launch_gemm_w8<192, 2, 16>(p.g1.grid, st, mA1, mB1, g1);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
     timing_mark(st, "pp_down_proj");

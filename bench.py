@@ -569,8 +569,17 @@ def run_kernels_only(args):
     import torch
     from attention_pre_processing_gb300 import build as cuda_build
     from attention_pre_processing_gb300 import workloads
-    from attention_pre_processing_gb300.runner import PrologCall
+    from attention_pre_processing_gb300.runner import PrologCall, PreprocessCall
     cuda_build.build()
+    if args.workload.startswith("pp_"):   # the aclnnMlaPreprocess variant
+        cfg = workloads.pp_config(args.workload, **({"T": args.T} if args.T else {}))
+        call = PreprocessCall(cfg, workloads.make_pp_inputs(cfg))
+        for _ in range(args.warmup + args.steps):
+            call()
+        torch.cuda.synchronize()
+        if call.status() != 0:
+            raise SystemExit("device status bits set")
+        return
     cfg = workloads.config(args.workload)
     if args.T:
         over = {"T": args.T}
