@@ -24,9 +24,18 @@ class PrologCall:
     With ``bs = (B, S)`` (B * S = T) the per-token tensors are passed in the page's
     non-concatenated layout: tokenX (B, S, He), ropeSin / ropeCos (B, S, Dr), cacheIndex (B, S),
     queryOut (B, S, N, Hckv), queryRopeOut (B, S, N, Dr) and dequantScaleQNopeOut (B*S, N, 1).
+
+    With ``packed_io`` the per-token inputs (tokenX, ropeSin, ropeCos, cacheIndex) are views of one
+    device buffer ``io_in`` and the outputs (queryOut, queryRopeOut and, for int8 q^N, its scales)
+    views of one buffer ``io_out`` (each piece 256-byte aligned), so that a step's inputs and
+    results cross the host link in one copy each way.
     """
 
-    def __init__(self, cfg: MlaConfig, inputs: Dict[str, Optional[torch.Tensor]], device="cuda", bs=None):
+    IO_IN = ("x", "rope_sin", "rope_cos", "cache_index")
+    IO_OUT = ("q_out", "q_rope_out", "dequant_scale_q_nope_out")
+
+    def __init__(self, cfg: MlaConfig, inputs: Dict[str, Optional[torch.Tensor]], device="cuda", bs=None,
+                 packed_io: bool = False):
         s = cfg.shape
         self.cfg = cfg
         self.t: Dict[str, Optional[torch.Tensor]] = {}
@@ -48,12 +57,33 @@ class PrologCall:
         self.t["q_rope_out"] = torch.empty(lead + (s.N, s.Dr), dtype=torch.bfloat16, device=device)
         self.t["dequant_scale_q_nope_out"] = (torch.empty((s.T, s.N, 1), dtype=torch.float32, device=device)
                                               if cfg.q_int8 else None)
+        self.io_in = self.io_out = None
+        if packed_io:
+            self.io_in = self._pack(self.IO_IN, device, copy=True)
+            self.io_out = self._pack(self.IO_OUT, device, copy=False)
         self.ws_bytes = mla_prolog_workspace_size(self.t, cfg.eps_cq, cfg.eps_ckv)
         self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
         # The tensors stay put between calls: their descriptors are marshalled once.
         args, self._keep = _marshal(self.t, cfg.eps_cq, cfg.eps_ckv, "PA_BSND")
         self._args = tuple(args) + (ctypes.c_void_p(self.workspace.data_ptr()), ctypes.c_uint64(self.ws_bytes))
         self._fn = lib().mla_prolog
+
+    def _pack(self, keys, device, copy: bool) -> torch.Tensor:
+        """One byte buffer holding the tensors ``keys`` (the present ones) as aligned views."""
+        present = [k for k in keys if self.t.get(k) is not None]
+        offs, off = [], 0
+        for k in present:
+            offs.append(off)
+            off += (self.t[k].numel() * self.t[k].element_size() + 255) // 256 * 256
+        buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+        for k, o in zip(present, offs):
+            old = self.t[k]
+            n = old.numel() * old.element_size()
+            view = buf[o:o + n].view(old.dtype).view(old.shape)
+            if copy:
+                view.copy_(old)
+            self.t[k] = view
+        return buf
 
     def __call__(self, stream=None) -> None:
         if stream is None:

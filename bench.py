@@ -377,35 +377,41 @@ def _read_traffic(kernel, workload):
 
 
 def _e2e(call, cfg, stream, dev, K, flush_l2):
+    """The headline call end to end: each step copies its inputs (tokenX, rope tables,
+    cacheIndex) from pinned host memory, runs mla_prolog through the C ABI and reads queryOut and
+    queryRopeOut back into pinned host memory, all on the call's stream, inside the step's events.
+    The per-token tensors are views of one device buffer each way (PrologCall packed_io), so a
+    step makes one copy in each direction."""
     import torch
+    from attention_pre_processing_gb300.runner import PrologCall
+    from attention_pre_processing_gb300 import workloads
     s = cfg.shape
-    host_in = {k: call.t[k].cpu().pin_memory() for k in ("x", "rope_sin", "rope_cos", "cache_index")}
-    host_out = {k: torch.empty(call.t[k].shape, dtype=call.t[k].dtype, pin_memory=True) for k in ("q_out", "q_rope_out")}
-    bi = sum(v.numel() * v.element_size() for v in host_in.values())
-    bo = sum(v.numel() * v.element_size() for v in host_out.values())
-    for _ in range(3):
-        for k, v in host_in.items():
-            call.t[k].copy_(v, non_blocking=True)
-        call(stream)
-        for k, v in host_out.items():
-            v.copy_(call.t[k], non_blocking=True)
-    torch.cuda.synchronize(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for i in range(K):
-        flush_l2()
-        starts[i].record(stream)
-        for k, v in host_in.items():
-            call.t[k].copy_(v, non_blocking=True)
-        call(stream)
-        for k, v in host_out.items():
-            v.copy_(call.t[k], non_blocking=True)
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
+    pc = PrologCall(cfg, workloads.make_inputs(cfg), device=dev, packed_io=True)
+    host_in = pc.io_in.cpu().pin_memory()
+    host_out = torch.empty(pc.io_out.shape, dtype=torch.uint8, pin_memory=True)
+    bi = host_in.numel()
+    bo = host_out.numel()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            pc.io_in.copy_(host_in, non_blocking=True)
+            pc(stream)
+            host_out.copy_(pc.io_out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for i in range(K):
+            flush_l2()
+            starts[i].record(stream)
+            pc.io_in.copy_(host_in, non_blocking=True)
+            pc(stream)
+            host_out.copy_(pc.io_out, non_blocking=True)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
     ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / K
     return {"value": s.T / (ms / 1e3), "unit": "tokens/s", "us_per_call": ms * 1e3,
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "path": "pinned host -> device copies, mla_prolog (C ABI), device -> pinned host copies"}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "copies_per_step": 2,
+            "path": "pinned host -> device copy of the per-token inputs, mla_prolog (C ABI), "
+                    "device -> pinned host copy of queryOut | queryRopeOut"}
 
 
 def _prefill(dev, stream, flush_l2, peaks, K):

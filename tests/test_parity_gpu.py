@@ -322,6 +322,25 @@ def test_batch_seq_layout(name, B, S):
         assert torch.equal(_bits(c.call.t[k]).reshape(-1), _bits(flat.call.t[k]).reshape(-1)), k
 
 
+@pytest.mark.parametrize("name", ["decode_t32", "decode_t256_qint8"])
+def test_packed_io_matches_separate_tensors(name):
+    """PrologCall(packed_io=True) (the per-token inputs and the outputs as views of one buffer
+    each way, as the end-to-end bench copies them) gives the same bits as separate tensors."""
+    cfg = workloads.config(name)
+    inp = workloads.make_inputs(cfg)
+    PrologCall = _runner()
+    a, b = PrologCall(cfg, inp), PrologCall(cfg, inp, packed_io=True)
+    assert b.io_in is not None and b.io_out is not None
+    assert b.t["x"].data_ptr() == b.io_in.data_ptr() and b.t["q_out"].data_ptr() == b.io_out.data_ptr()
+    a()
+    b()
+    torch.cuda.synchronize()
+    assert a.status() == 0 and b.status() == 0
+    for k in ("q_out", "q_rope_out", "dequant_scale_q_nope_out", "kv_cache", "kr_cache"):
+        if a.t[k] is not None:
+            assert torch.equal(_bits(a.t[k]), _bits(b.t[k])), k
+
+
 def test_empty_tokens_is_a_no_op():
     cfg = workloads.config("tiny", T=0)
     inp = workloads.make_inputs(cfg)
