@@ -20,17 +20,20 @@
 //   warp 1      TMEM allocation and the tcgen05.mma issuer (B 128-byte swizzle)
 //   warps 2-5   epilogue: TMEM -> fp32 k-range slots (split-K), as gemm_tc's EPI_F32, or (EPI_QROPE,
 //               one 192-column head per tile) dequant scales, RoPE and q^C, as gemm_tc's
-//   warps 6-13  converters: per k-block, each 16-byte int8 chunk -> two 16-byte fp16 chunks of the
-//               swizzled B slot (chunk c of 128-byte row r at (c ^ (r % 8)) * 16; rows are output
-//               columns (K-major) or k (MN-major, one 8 KB block per 64 columns)), then a proxy
-//               fence and an arrival on the slot's "B full" barrier
+//   warps 6-13  converters: per stage, each 16-byte int8 chunk of its k-blocks -> two 16-byte fp16
+//               chunks of the swizzled B slots (chunk c of 128-byte row r at (c ^ (r % 8)) * 16;
+//               rows are output columns (K-major) or k (MN-major, one 8 KB block per 64 columns)),
+//               then a proxy fence and one arrival on the slots' "B full" barrier
 // The int8 and A tiles run in a deep ring of stages (the weight stream's latency hiding); the
-// fp16 B tiles in a ring of kBSlots slots: with two, each k-block paid its conversion and the
-// MMAs' completion one after the other (~0.39 us per k-block at BN = 64, measured with
-// globaltimer stamps), so the ring is as deep as the shared memory allows (8 slots of 8 KB at
-// BN = 64, 4 of 24 KB at BN = 192; 2 with 256-row tiles, whose activation stages are large).  Stage s is reused only
-// after the MMAs that read it commit (empty[s]), which follows its conversion; slot j only after
-// the MMAs that read it commit (bempty[j]).  Every wait is bounded and sets kStatusWaitTimeout.
+// fp16 B tiles in a ring of kBSlots slots, as deep as the shared memory allows (8 slots of 8 KB at
+// BN = 64, 4 at BN = 128 and 192, 2 with 256-row tiles), so that the converters run ahead of the
+// MMAs.  The slots change hands a stage (kKb k-blocks) at a time: one "B full" wait and one
+// "B empty" commit per stage, not per k-block.  At decode sizes each hand-over between the
+// single-thread roles costs ~0.1 us (measured with cycle-counter stamps), so a CTA's time follows
+// its number of hand-overs: per-stage hand-over took the variant's call 59.4 -> 57.3 us.
+// Stage s is reused only after the MMAs that read it commit (empty[s]), which follows its
+// conversion; a slot pair only after the MMAs that read it commit (bempty).  Every wait is
+// bounded and sets kStatusWaitTimeout.
 #pragma once
 
 #include <cuda.h>
@@ -60,6 +63,8 @@ struct W8Cfg {
     static constexpr int kB8Stage = BN * kBK * kKb;  // int8: BN columns x 64 * kKb k
     static constexpr int kBStage = BN * kBK * 2;     // fp16: BN rows x 128 bytes
     static constexpr int kBSlots = MSUB == 1 ? (BN <= 64 ? 8 : 4) : 2;   // fp16 B slots
+    static constexpr int kBPairs = kBSlots / kKb;   // handed over per stage: kKb slots per barrier
+    static_assert(kBSlots % kKb == 0, "whole stages of slots");
     static constexpr int kAcc = MSUB * BN;
     static constexpr int kNBuf = (2 * kAcc <= 512) ? 2 : 1;
     static constexpr int kTmemCols = (kNBuf * kAcc <= 32) ? 32 : (kNBuf * kAcc <= 64) ? 64
@@ -121,7 +126,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             mbar_init(smem_u32(&empty[s]), 1);
             mbar_init(smem_u32(&full8[s]), 1);
         }
-        for (int b = 0; b < C::kBSlots; ++b) {
+        for (int b = 0; b < C::kBPairs; ++b) {
             mbar_init(smem_u32(&bfull[b]), kW8Conv);
             mbar_init(smem_u32(&bempty[b]), 1);
         }
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
             const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), MN ? 64 * 128 : 16, 1024);
             int s = 0;
-            uint32_t ph = 0, ai = 0, gi = 0;   // gi: k-blocks so far (fp16 slot gi % kBSlots)
+            uint32_t ph = 0, ai = 0, gs = 0;   // gs: stages so far (fp16 slot pair gs % kBPairs)
             Unit u;
             bool ok = true;
             for (int idx = 0; ok && get_unit(args, idx, u); ++idx, ++ai) {
@@ -243,13 +248,15 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                         ok = false;
                         break;
                     }
-                    for (int i = 0; i < nkb; ++i, ++gi) {
-                        const int j = (int)(gi % C::kBSlots);
-                        if (!mbar_wait(smem_u32(&bfull[j]), (gi / C::kBSlots) & 1u, s_abort, kWaitLimitNs)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
+                    // the stage's fp16 slots: pair gp (kKb slots from kKb * gp)
+                    const int gp = (int)(gs % C::kBPairs);
+                    if (!mbar_wait(smem_u32(&bfull[gp]), (gs / C::kBPairs) & 1u, s_abort, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int i = 0; i < nkb; ++i) {
+                        const int j = gp * C::kKb + i;
                         const uint64_t a_desc =
                             a_desc0 + (uint64_t)(((size_t)s * a_stage + (size_t)i * MSUB * a_box) >> 4);
                         const uint64_t b_desc = b_desc0 + (uint64_t)j * (uint64_t)(C::kBStage >> 4);
@@ -259,8 +266,9 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                             for (int ms = 0; ms < MSUB; ++ms)
                                 umma_bf16(d_base + ms * BN, a_desc + (uint64_t)(((ms * a_box) >> 4) + 2 * kk),
                                           b_desc + b_step * kk, idesc, (kb + i > u.kb0 || kk > 0) ? 1u : 0u);
-                        umma_commit(smem_u32(&bempty[j]));
                     }
+                    umma_commit(smem_u32(&bempty[gp]));
+                    ++gs;
                     if (!ok) break;
                     umma_commit(smem_u32(&empty[s]));
                     if (++s == stages) {
@@ -303,7 +311,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
         // ------------------------------------------------------------ converters
         const int ct = threadIdx.x - 192;   // 0 .. kW8Conv - 1
         int s = 0;
-        uint32_t ph = 0, gi = 0;
+        uint32_t ph = 0, gs = 0;
         Unit u;
         bool ok = true;
         for (int idx = 0; ok && get_unit(args, idx, u); ++idx) {
@@ -313,12 +321,13 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                     ok = false;
                     break;
                 }
-                for (int i = 0; i < nkb; ++i, ++gi) {
-                    const int j = (int)(gi % C::kBSlots);
-                    if (!mbar_wait(smem_u32(&bempty[j]), ((gi / C::kBSlots) & 1u) ^ 1u, s_abort, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
+                const int gp = (int)(gs % C::kBPairs);
+                if (!mbar_wait(smem_u32(&bempty[gp]), ((gs / C::kBPairs) & 1u) ^ 1u, s_abort, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                for (int i = 0; i < nkb; ++i) {
+                    const int j = gp * C::kKb + i;
                     // k-block i of the stage: 16 bytes of the int8 box's rows at i * kBK (K-major), or
                     // its 64 rows from 64 i on (MN-major)
                     const uint8_t* src = sB8 + (size_t)s * C::kB8Stage + (MN ? (size_t)i * kBK * BN : (size_t)i * kBK);
@@ -354,9 +363,10 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                                      "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
                                      : "memory");
                     }
-                    fence_proxy_async_smem();   // the tensor core reads what these threads wrote
-                    mbar_arrive(smem_u32(&bfull[j]));
                 }
+                fence_proxy_async_smem();   // the tensor core reads what these threads wrote
+                mbar_arrive(smem_u32(&bfull[gp]));
+                ++gs;
                 if (!ok) break;
                 if (++s == stages) {
                     s = 0;
