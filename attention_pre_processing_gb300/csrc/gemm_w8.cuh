@@ -23,14 +23,16 @@
 //   warps 6-13  converters: per stage, each 16-byte int8 chunk of its k-blocks -> two 16-byte fp16
 //               chunks of the swizzled B slots (chunk c of 128-byte row r at (c ^ (r % 8)) * 16;
 //               rows are output columns (K-major) or k (MN-major, one 8 KB block per 64 columns)),
-//               then a proxy fence and one arrival on the slots' "B full" barrier
+//               then a proxy fence, a wait for the stage's A tiles and one arrival on the slots'
+//               "B full" barrier (so the MMA thread waits once per stage)
 // The int8 and A tiles run in a deep ring of stages (the weight stream's latency hiding); the
 // fp16 B tiles in a ring of kBSlots slots, as deep as the shared memory allows (8 slots of 8 KB at
 // BN = 64, 4 at BN = 128 and 192, 2 with 256-row tiles), so that the converters run ahead of the
 // MMAs.  The slots change hands a stage (kKb k-blocks) at a time: one "B full" wait and one
 // "B empty" commit per stage, not per k-block.  At decode sizes each hand-over between the
 // single-thread roles costs ~0.1 us (measured with cycle-counter stamps), so a CTA's time follows
-// its number of hand-overs: per-stage hand-over took the variant's call 59.4 -> 57.3 us.
+// its number of hand-overs: per-stage hand-over took the variant's call 59.4 -> 57.3 us, and
+// folding the A tiles' wait into "B full" a further ~1.5 us.
 // Stage s is reused only after the MMAs that read it commit (empty[s]), which follows its
 // conversion; a slot pair only after the MMAs that read it commit (bempty).  Every wait is
 // bounded and sets kStatusWaitTimeout.
@@ -244,11 +246,8 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                 const uint32_t d_base = tmem_base + b * C::kAcc;
                 for (int kb = u.kb0; ok && kb < u.kb1; kb += C::kKb) {
                     const int nkb = min(C::kKb, u.kb1 - kb);
-                    if (!mbar_wait(smem_u32(&full[s]), ph, s_abort, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    // the stage's fp16 slots: pair gp (kKb slots from kKb * gp)
+                    // the stage's fp16 slots: pair gp (kKb slots from kKb * gp); "B full" also
+                    // means the stage's A tiles have landed (the converters wait for them)
                     const int gp = (int)(gs % C::kBPairs);
                     if (!mbar_wait(smem_u32(&bfull[gp]), (gs / C::kBPairs) & 1u, s_abort, kWaitLimitNs)) {
                         ok = false;
@@ -365,6 +364,11 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                     }
                 }
                 fence_proxy_async_smem();   // the tensor core reads what these threads wrote
+                // the stage's A tiles too: one wait for the MMA thread per stage
+                if (!mbar_wait(smem_u32(&full[s]), ph, s_abort, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
                 mbar_arrive(smem_u32(&bfull[gp]));
                 ++gs;
                 if (!ok) break;
