@@ -103,8 +103,10 @@ __device__ __forceinline__ float group_reduce(float v, float* red, int tid, Sync
 // already staged in shared memory.  Every load that does not depend on the partial sums is
 // issued before them, and a thread's partial loads for up to kRowCols columns are in flight
 // together: with few rows (decode) the row then costs about one memory latency; with many rows a
-// small kRowCols keeps the registers, and so the rows in flight per SM, up.
-template <int NT, int kRowCols, class Sync>
+// small kRowCols keeps the registers, and so the rows in flight per SM, up.  kSlots > 0: every
+// k-range slot (up to kSlots) of those columns is requested at once, instead of four slots per
+// round (each round waits for the previous one's loads).
+template <int NT, int kRowCols, class Sync, int kSlots = 0>
 __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, float* ys, float* red,
                                          const __nv_bfloat16* gcq, const __nv_bfloat16* gckv, Sync sync) {
     const int ncols = a.Hcq + a.Hckv + a.Dr;
@@ -124,6 +126,22 @@ __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, floa
     float sq = 0.f, skv = 0.f;
     for (int c0 = tid; c0 < ncols; c0 += kRowCols * NT) {
         float v[kRowCols];
+        if constexpr (kSlots > 0) {
+            float w[kSlots][kRowCols];
+#pragma unroll
+            for (int k = 0; k < kSlots; ++k)
+#pragma unroll
+                for (int u = 0; u < kRowCols; ++u) {
+                    const int c = c0 + u * NT;
+                    w[k][u] = (k < a.src.slots && c < ncols) ? __ldcg(src + k * a.src.slot_stride + c) : 0.f;
+                }
+#pragma unroll
+            for (int u = 0; u < kRowCols; ++u) {
+                v[u] = w[0][u];
+#pragma unroll
+                for (int k = 1; k < kSlots; ++k) v[u] += w[k][u];   // k-range order
+            }
+        } else {
 #pragma unroll
         for (int u = 0; u < kRowCols; ++u) {
             const int c = c0 + u * NT;
@@ -142,6 +160,7 @@ __device__ __forceinline__ void down_row(const DownArgs& a, int t, int tid, floa
             for (int k = 0; k < 4; ++k)
 #pragma unroll
                 for (int u = 0; u < kRowCols; ++u) v[u] += w[k][u];
+        }
         }
 #pragma unroll
         for (int u = 0; u < kRowCols; ++u) {
@@ -250,29 +269,30 @@ __host__ __device__ inline size_t down_smem_bytes(int Hcq, int Hckv, int Dr) {
     return (((size_t)(Hcq + Hckv + Dr) * 4 + 15) & ~(size_t)15) + (size_t)(Hcq + Hckv) * 2;
 }
 
-// One CTA per token (grid-stride).  ROWCOLS: columns of partial sums a thread has in flight.
-template <int ROWCOLS>
-__global__ void __launch_bounds__(kRowThreads) finalize_down_kernel(const DownArgs a) {
+// One CTA of NT threads per token (grid-stride).  ROWCOLS: columns of partial sums a thread has
+// in flight; KS > 0: all of their k-range slots (up to KS) at once.
+template <int ROWCOLS, int NT = kRowThreads, int KS = 0>
+__global__ void __launch_bounds__(NT) finalize_down_kernel(const DownArgs a) {
     extern __shared__ __align__(16) uint8_t fsm[];
     float* ys = reinterpret_cast<float*>(fsm);
     __nv_bfloat16* gcq = reinterpret_cast<__nv_bfloat16*>(fsm + (((size_t)(a.Hcq + a.Hckv + a.Dr) * 4 + 15) & ~(size_t)15));
     __nv_bfloat16* gckv = gcq + a.Hcq;
-    __shared__ float red[kRowThreads / 32 + 1];
+    __shared__ float red[NT / 32 + 1];
     // All CTAs of this grid are resident once every one has passed here: the next kernel may
     // start its prologue (and its first weight loads) now.
     pdl_launch_dependents();
     // The gammas and the other small inputs do not depend on the previous kernel: stage and
     // prefetch them while it finishes, so that the row work does not wait on cold lines.
     // (Hcq and Hckv are multiples of 8: 16-byte copies.)
-    for (int i = threadIdx.x; i < a.Hcq / 8; i += kRowThreads)
+    for (int i = threadIdx.x; i < a.Hcq / 8; i += NT)
         reinterpret_cast<uint4*>(gcq)[i] = reinterpret_cast<const uint4*>(a.gamma_cq)[i];
-    for (int i = threadIdx.x; i < a.Hckv / 8; i += kRowThreads)
+    for (int i = threadIdx.x; i < a.Hckv / 8; i += NT)
         reinterpret_cast<uint4*>(gckv)[i] = reinterpret_cast<const uint4*>(a.gamma_ckv)[i];
-    prefetch_down_inputs(a, threadIdx.x, kRowThreads);
+    prefetch_down_inputs(a, threadIdx.x, NT);
     pdl_wait();
     __syncthreads();
     for (int t = blockIdx.x; t < a.T; t += gridDim.x)
-        down_row<kRowThreads, ROWCOLS>(a, t, threadIdx.x, ys, red, gcq, gckv, CtaSync{});
+        down_row<NT, ROWCOLS, CtaSync, KS>(a, t, threadIdx.x, ys, red, gcq, gckv, CtaSync{});
 }
 
 // Warp-per-token variant of the row work for many tokens (one k-range slot): each lane keeps

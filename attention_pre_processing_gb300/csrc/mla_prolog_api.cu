@@ -957,12 +957,14 @@ mla_status run(const Launched& L) {
     } else {
         const int grid = T < 16 * L.sms ? T : 16 * L.sms;
         const size_t fsmem = down_smem_bytes((int)d.Hcq, (int)d.Hckv, (int)d.Dr);
-        // decode-sized T: every partial load of a row in flight at once; many rows: fewer, so
-        // that more rows fit on an SM
-        auto fk = T <= kDecodeRows ? finalize_down_kernel<9> : finalize_down_kernel<3>;
+        // decode-sized T: 512 threads per token, each with all k-range partials of its five
+        // columns in flight at once (the k ranges number at most 16 there); many rows: fewer
+        // loads in flight, so that more rows fit on an SM
+        const bool wide = T <= kDecodeRows && p.g1.ksplit <= 16;
+        auto fk = wide ? finalize_down_kernel<5, 512, 16> : finalize_down_kernel<3>;
         e = set_attr(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
         if (e != cudaSuccess) return MLA_ERR_RUNTIME;
-        e = launch(fk, grid, kRowThreads, fsmem, st, f1);
+        e = launch(fk, grid, wide ? 512 : kRowThreads, fsmem, st, f1);
         if (e != cudaSuccess) return MLA_ERR_RUNTIME;
         timing_mark(st, "f1_norm_rope_cache");
     }
