@@ -296,6 +296,10 @@ struct PpMidArgs {
     uint32_t* status;
 };
 
+// k ranges of the down-projection's partials that pp_mid_kernel requests at once (a round of
+// 32 registers of loads at 1024 threads).
+constexpr int kPpSlotRound = 8;
+
 // One CTA per token; dynamic shared memory holds the token's n1 values as exact float pairs
 // (y = (acc + bias) * deScale has at most 48 significant bits: acc + bias is an integer below
 // 2^24 and deScale a float, so its product splits exactly into a float and the float error).
@@ -314,11 +318,19 @@ __global__ void __launch_bounds__(kPpRowThreads) pp_mid_kernel(const PpMidArgs a
     for (int j4 = tid; j4 < a.n1 / 4; j4 += kPpRowThreads) {
         // the k-range partials are integer-valued (int8 products), so their fp32 sum in k-range
         // order is the exact integer while it stays below 2^24; bias and scale then in double
+        // kPpSlotRound k ranges' partials in flight at once (all of them at the decode plan's 8),
+        // summed in k-range order
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int s = 0; s < a.ksplit; ++s) {   // k-range order
-            const float4 p = __ldcg(reinterpret_cast<const float4*>(y0 + (size_t)s * a.slot_stride) + j4);
-            acc.x += p.x, acc.y += p.y, acc.z += p.z, acc.w += p.w;
+        for (int s0 = 0; s0 < a.ksplit; s0 += kPpSlotRound) {
+            float4 pk[kPpSlotRound];
+#pragma unroll
+            for (int i = 0; i < kPpSlotRound; ++i)
+                pk[i] = s0 + i < a.ksplit
+                            ? __ldcg(reinterpret_cast<const float4*>(y0 + (size_t)(s0 + i) * a.slot_stride) + j4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < kPpSlotRound; ++i)
+                if (s0 + i < a.ksplit) acc.x += pk[i].x, acc.y += pk[i].y, acc.z += pk[i].z, acc.w += pk[i].w;
         }
         int4 b = make_int4(0, 0, 0, 0);
         if (a.bias0 != nullptr) b = reinterpret_cast<const int4*>(a.bias0)[j4];

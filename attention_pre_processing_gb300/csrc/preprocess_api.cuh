@@ -308,7 +308,9 @@ mla_status pp_run(const PpArgs& a, const PpDims& d, const PpPlan& p, uint8_t* ws
         const uint32_t box[2] = {64, 32};
         g3.tma_out = encode_map(&mO3, a.qout->data, 2, dims, strides, box, tdt) ? 1 : 0;
     }
-    e = p.g3.bn == 512 ? launch_gemm<512, 1, 4, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr)
+    // one 512-column tile per head: four epilogue warps per TMEM lane quarter, 128 columns each
+    // (at T = 32 every row sits in the first lane quarter, which one warp alone drained in ~1.5 us more)
+    e = p.g3.bn == 512 ? launch_gemm<512, 1, 4, EPI_QN, 1, 1, 4>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr)
         : p.kps3 ? launch_gemm<256, 1, 8, EPI_QN, 2, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr)
                : launch_gemm<256, 1, 8, EPI_QN, 2>(p.g3.grid, st, mA3, mB3, mB3, g3, g3.tma_out ? &mO3 : nullptr);
     if (e != cudaSuccess) return MLA_ERR_RUNTIME;
