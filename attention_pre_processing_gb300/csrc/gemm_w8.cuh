@@ -16,15 +16,18 @@
 // would move three bytes per weight through HBM more than needed; here the int8 tile crosses HBM
 // once:
 //   warp 0      TMA producer: per stage, kW8Kb k-blocks of A tiles (128-byte swizzle) and one
-//               int8 weight box (plain rows): BN rows x 64 * kW8Kb k, or 64 * kW8Kb k rows x BN
+//               int8 weight box (plain rows): BN rows x 64 * kW8Kb k, or 64 * kW8Kb k rows x BN;
+//               with A8 the A tiles are one int8 box (int8 tokenX, rows x 64 * kW8Kb bytes),
+//               requested with the weights before the grid dependency when A is a call input
 //   warp 1      TMEM allocation and the tcgen05.mma issuer (B 128-byte swizzle)
 //   warps 2-5   epilogue: TMEM -> fp32 k-range slots (split-K), as gemm_tc's EPI_F32, or (EPI_QROPE,
 //               one 192-column head per tile) dequant scales, RoPE and q^C, as gemm_tc's
 //   warps 6-13  converters: per stage, each 16-byte int8 chunk of its k-blocks -> two 16-byte fp16
 //               chunks of the swizzled B slots (chunk c of 128-byte row r at (c ^ (r % 8)) * 16;
 //               rows are output columns (K-major) or k (MN-major, one 8 KB block per 64 columns)),
-//               then a proxy fence, a wait for the stage's A tiles and one arrival on the slots'
-//               "B full" barrier (so the MMA thread waits once per stage)
+//               then a wait for the stage's A tiles (A8: and their widening into the pair's fp16 A
+//               slots, the same 128-byte-swizzled K-major layout), a proxy fence and one arrival
+//               on the slots' "B full" barrier (so the MMA thread waits once per stage)
 // The int8 and A tiles run in a deep ring of stages (the weight stream's latency hiding); the
 // fp16 B tiles in a ring of kBSlots slots, as deep as the shared memory allows (8 slots of 8 KB at
 // BN = 64, 4 at BN = 128 and 192, 2 with 256-row tiles), so that the converters run ahead of the
@@ -58,7 +61,7 @@ constexpr int kW8Threads = 64 + 128 + kW8Conv;
 constexpr int kW8Kb = 2;
 static_assert(kW8Kb >= 1 && kW8Kb <= 4, "a TMA box row holds at most 256 elements");
 
-template <int BN, int MSUB, int MAXST, bool MN = false>
+template <int BN, int MSUB, int MAXST, bool MN = false, bool A8 = false>
 struct W8Cfg {
     static constexpr int kKb = kW8Kb;
     static constexpr int kB8Row = MN ? BN : kBK * kKb;   // bytes per int8 box row
@@ -76,25 +79,59 @@ struct W8Cfg {
     static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
     static_assert(!MN || BN % 64 == 0, "MN-major tiles are whole 64-column blocks");
     static_assert(kAcc <= 512, "accumulator exceeds TMEM");
-    static __host__ __device__ int a_stage_bytes(int a_box_rows) { return kKb * MSUB * a_box_rows * 128; }
+    static_assert(!A8 || MSUB == 1, "int8 activations: one 128-row tile");
+    // A per stage: fp16 boxes (128-byte swizzle), or with A8 one int8 box of 64 * kKb bytes per
+    // row, widened by the converters into fp16 A slots (one per fp16 B slot, a_box_rows x 128 B)
+    static __host__ __device__ int a_stage_bytes(int a_box_rows) {
+        return A8 ? kKb * a_box_rows * 64 : kKb * MSUB * a_box_rows * 128;
+    }
+    static __host__ __device__ int a_slot_bytes(int a_box_rows) { return A8 ? a_box_rows * 128 : 0; }
     static __host__ __device__ int stage_bytes(int a_box_rows) { return a_stage_bytes(a_box_rows) + kB8Stage; }
-    // Layout: barriers | A ring | fp16 B slots | int8 ring.  A 128-row MMA read of a short A box
-    // runs at most 16 KB past its stage, into the B slots (>= 16 KB), inside the block.
+    // Layout: barriers | A ring (A8: fp16 A slots) | fp16 B slots | int8 ring | (A8) int8 A
+    // ring.  A 128-row MMA read of a short A box runs at most 16 KB past its stage or slot, into
+    // the B slots (>= 16 KB), inside the block.
     static __host__ __device__ size_t smem_bytes(int stages, int a_box_rows) {
-        return 1024 + kBarBytes + (size_t)kBSlots * kBStage + (size_t)stages * stage_bytes(a_box_rows);
+        return 1024 + kBarBytes + (size_t)kBSlots * (kBStage + a_slot_bytes(a_box_rows)) +
+               (size_t)stages * stage_bytes(a_box_rows);
     }
     static __host__ int max_stages(int a_box_rows) {
-        int s = (int)((kSmemLimit - 1024 - kBarBytes - kBSlots * kBStage) / stage_bytes(a_box_rows));
+        int s = (int)((kSmemLimit - 1024 - kBarBytes - kBSlots * (kBStage + a_slot_bytes(a_box_rows))) /
+                      stage_bytes(a_box_rows));
         return s < MAXST ? s : MAXST;
     }
     static_assert(kBSlots * kBStage >= 16384, "the B slots must cover the A over-read");
 };
 
-template <int BN, int MSUB, int MAXST, bool MN = false, int EPI = EPI_F32>
+// Sixteen int8 values (one 16-byte chunk) widened to fp16 and stored as the 16-byte chunks cc and
+// cc + 1 of the 128-byte shared-memory row at `row`, 128-byte swizzled (chunk c at (c ^ sw) * 16).
+// The biased byte b + 128 goes under the exponent of 1024 (one byte permute); subtracting 1152
+// leaves b, exactly.
+__device__ __forceinline__ void w8_widen_store(int4 v, uint32_t row, uint32_t cc, uint32_t sw) {
+    const uint32_t w[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+    uint32_t o[8];
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));   // 1152
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t ub = w[e] ^ 0x80808080u;   // bytes b + 128, in 0..255
+        uint32_t lo = __byte_perm(ub, 0x64646464u, 0x4140u), hi = __byte_perm(ub, 0x64646464u, 0x4342u);
+        __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
+        __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
+        o[2 * e] = *reinterpret_cast<uint32_t*>(&hl);
+        o[2 * e + 1] = *reinterpret_cast<uint32_t*>(&hh);
+    }
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((cc ^ sw) << 4)), "r"(o[0]), "r"(o[1]),
+                 "r"(o[2]), "r"(o[3])
+                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((cc + 1) ^ sw) << 4)), "r"(o[4]),
+                 "r"(o[5]), "r"(o[6]), "r"(o[7])
+                 : "memory");
+}
+
+template <int BN, int MSUB, int MAXST, bool MN = false, int EPI = EPI_F32, bool A8 = false>
 __global__ void __launch_bounds__(kW8Threads, 1)
     gemm_w8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b8,
                    const __grid_constant__ CUtensorMap map_b8b, const GemmArgs args) {
-    using C = W8Cfg<BN, MSUB, MAXST, MN>;
+    using C = W8Cfg<BN, MSUB, MAXST, MN, A8>;
     static_assert(EPI == EPI_F32 || (EPI == EPI_QROPE && BN == 192), "epilogues: fp32 slots, or one head per tile");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -112,9 +149,11 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     const int stages = args.stages;
     const int a_stage = C::a_stage_bytes(args.a_box_rows);
     const int a_box = args.a_box_rows * 128;
-    uint8_t* sA = smem + C::kBarBytes;
-    uint8_t* sB = sA + (size_t)stages * a_stage;
+    const int a_slot = C::a_slot_bytes(args.a_box_rows);
+    uint8_t* sA = smem + C::kBarBytes;   // fp16 A stages, or (A8) fp16 A slots
+    uint8_t* sB = sA + (A8 ? (size_t)C::kBSlots * a_slot : (size_t)stages * a_stage);
     uint8_t* sB8 = sB + (size_t)C::kBSlots * C::kBStage;
+    uint8_t* sA8 = sB8 + (size_t)stages * C::kB8Stage;   // A8: int8 activation stages
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -188,12 +227,18 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             };
             // ... and its activation tiles (the unit's last stage may be short)
             auto issue_a = [&](int st, const Unit& uu, int kb) {
-                const int nkb = min(C::kKb, uu.kb1 - kb);
                 const uint32_t fa = smem_u32(&full[st]);
-                mbar_arrive_expect_tx(fa, (uint32_t)(nkb * MSUB * a_box));
-                for (int i = 0; i < nkb; ++i)
-                    load_a<MSUB>(args, uu, kb + i, smem_u32(sA + (size_t)st * a_stage + i * MSUB * a_box), a_box, fa,
-                                 &map_a, pol_a);
+                if constexpr (A8) {
+                    // one int8 box: a_box_rows rows x 64 * kKb bytes (zeros past K and past T)
+                    mbar_arrive_expect_tx(fa, (uint32_t)a_stage);
+                    tma_load_2d(smem_u32(sA8 + (size_t)st * a_stage), &map_a, fa, kb * kBK, uu.m_tile * 128, pol_a);
+                } else {
+                    const int nkb = min(C::kKb, uu.kb1 - kb);
+                    mbar_arrive_expect_tx(fa, (uint32_t)(nkb * MSUB * a_box));
+                    for (int i = 0; i < nkb; ++i)
+                        load_a<MSUB>(args, uu, kb + i, smem_u32(sA + (size_t)st * a_stage + i * MSUB * a_box), a_box,
+                                     fa, &map_a, pol_a);
+                }
             };
             if (args.b_late) pdl_wait();   // the weights come from an earlier kernel of the call
             int pre = 0;
@@ -201,10 +246,14 @@ __global__ void __launch_bounds__(kW8Threads, 1)
             if (get_unit(args, 0, u0)) {
                 const int n0 = (u0.kb1 - u0.kb0 + C::kKb - 1) / C::kKb;
                 pre = n0 < stages ? n0 : stages;
-                for (int i = 0; i < pre; ++i) issue_w(i, u0, u0.kb0 + i * C::kKb);
+                for (int i = 0; i < pre; ++i) {
+                    issue_w(i, u0, u0.kb0 + i * C::kKb);
+                    if (args.a_ready) issue_a(i, u0, u0.kb0 + i * C::kKb);   // A is an input of the call
+                }
             }
             pdl_wait();
-            for (int i = 0; i < pre; ++i) issue_a(i, u0, u0.kb0 + i * C::kKb);
+            if (!args.a_ready)
+                for (int i = 0; i < pre; ++i) issue_a(i, u0, u0.kb0 + i * C::kKb);
             s = pre % stages;
             ph = (pre == stages) ? 1u : 0u;
             for (int idx = 0; ok && get_unit(args, idx, u); ++idx) {
@@ -257,7 +306,8 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                     for (int i = 0; i < nkb; ++i) {
                         const int j = gp * C::kKb + i;
                         const uint64_t a_desc =
-                            a_desc0 + (uint64_t)(((size_t)s * a_stage + (size_t)i * MSUB * a_box) >> 4);
+                            A8 ? a_desc0 + (uint64_t)(((size_t)j * a_slot) >> 4)
+                               : a_desc0 + (uint64_t)(((size_t)s * a_stage + (size_t)i * MSUB * a_box) >> 4);
                         const uint64_t b_desc = b_desc0 + (uint64_t)j * (uint64_t)(C::kBStage >> 4);
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
@@ -338,37 +388,30 @@ __global__ void __launch_bounds__(kW8Threads, 1)
                         const int r = MN ? task / (BN / 16) : task >> 2;
                         const int c = MN ? task % (BN / 16) : task & 3;
                         const int4 v = *reinterpret_cast<const int4*>(src + r * C::kB8Row + c * 16);
-                        const uint32_t w[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
-                        uint32_t o[8];
-                        const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint32_t ub = w[e] ^ 0x80808080u;   // bytes b + 128, in 0..255
-                            // (1024 + byte) as fp16: the byte under the exponent bits 0x64
-                            uint32_t lo = __byte_perm(ub, 0x64646464u, 0x4140u), hi = __byte_perm(ub, 0x64646464u, 0x4342u);
-                            __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
-                            __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
-                            o[2 * e] = *reinterpret_cast<uint32_t*>(&hl);
-                            o[2 * e + 1] = *reinterpret_cast<uint32_t*>(&hh);
-                        }
                         // the fp16 row (128 bytes) and its 16-byte chunk pair
                         const uint32_t row = MN ? dst + (uint32_t)((c >> 2) * (64 * 128) + r * 128) : dst + (uint32_t)(r * 128);
-                        const uint32_t cc = MN ? 2u * (uint32_t)(c & 3) : 2u * (uint32_t)c;
-                        const uint32_t sw = (uint32_t)(r & 7);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((cc ^ sw) << 4)),
-                                     "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                                     : "memory");
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((cc + 1) ^ sw) << 4)),
-                                     "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
-                                     : "memory");
+                        w8_widen_store(v, row, MN ? 2u * (uint32_t)(c & 3) : 2u * (uint32_t)c, (uint32_t)(r & 7));
                     }
                 }
-                fence_proxy_async_smem();   // the tensor core reads what these threads wrote
                 // the stage's A tiles too: one wait for the MMA thread per stage
                 if (!mbar_wait(smem_u32(&full[s]), ph, s_abort, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
+                if constexpr (A8) {
+                    // the int8 activation box (row r = token, 64 * kKb bytes) into the pair's fp16
+                    // A slots (K-major, 128-byte swizzle)
+                    const uint8_t* srcA = sA8 + (size_t)s * a_stage;
+                    for (int i = 0; i < nkb; ++i) {
+                        const uint32_t dstA = smem_u32(sA + (size_t)(gp * C::kKb + i) * a_slot);
+                        for (int task = ct; task < args.a_box_rows * 4; task += kW8Conv) {
+                            const int r = task >> 2, c = task & 3;
+                            const int4 v = *reinterpret_cast<const int4*>(srcA + r * (kBK * C::kKb) + i * kBK + c * 16);
+                            w8_widen_store(v, dstA + (uint32_t)(r * 128), 2u * (uint32_t)c, (uint32_t)(r & 7));
+                        }
+                    }
+                }
+                fence_proxy_async_smem();   // the tensor core reads what these threads wrote
                 mbar_arrive(smem_u32(&bfull[gp]));
                 ++gs;
                 if (!ok) break;

@@ -557,11 +557,11 @@ cudaError_t launch_gemm(int grid, cudaStream_t st, const CUtensorMap& a, const C
 
 // Launches one int8-weight GEMM instantiation (gemm_w8.cuh); b8b holds the columns from
 // args.b_split_col on (MN-major only).
-template <int BN, int MSUB, int MAXST, bool MN = false, int EPI = EPI_F32>
+template <int BN, int MSUB, int MAXST, bool MN = false, int EPI = EPI_F32, bool A8 = false>
 cudaError_t launch_gemm_w8(int grid, cudaStream_t st, const CUtensorMap& a, const CUtensorMap& b8,
                            const CUtensorMap& b8b, GemmArgs args) {
-    using C = W8Cfg<BN, MSUB, MAXST, MN>;
-    auto k = gemm_w8_kernel<BN, MSUB, MAXST, MN, EPI>;
+    using C = W8Cfg<BN, MSUB, MAXST, MN, A8>;
+    auto k = gemm_w8_kernel<BN, MSUB, MAXST, MN, EPI, A8>;
     args.stages = C::max_stages(args.a_box_rows);
     if (args.stages < 2) return cudaErrorInvalidConfiguration;
     cudaError_t e = set_attr(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
@@ -580,6 +580,19 @@ bool map_w8_cols(CUtensorMap* m, const void* base, uint64_t K, uint64_t cols, ui
     const cuuint64_t gd[2] = {cols, K};
     const cuuint64_t gs[1] = {cols};
     const cuuint32_t bx[2] = {box_cols, (cuuint32_t)(64 * kW8Kb)};
+    const cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gd, gs, bx, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// int8 (rows, K) row-major matrix, one row per output column (the variant's weights) or per
+// token (int8 tokenX): boxes of 64 * kW8Kb k (no swizzle) x box_rows rows; rows and columns past
+// the end read as zero.
+bool map_w8_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
+    const cuuint64_t gd[2] = {K, rows};
+    const cuuint64_t gs[1] = {K};
+    const cuuint32_t bx[2] = {(cuuint32_t)(64 * kW8Kb), box_rows};
     const cuuint32_t es[2] = {1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gd, gs, bx, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -704,7 +717,13 @@ mla_status run(const Launched& L) {
     const void* wdq_bf = a.wdq->data;
     const void* wdkvkr_bf = a.wdkvkr->data;
     const void* wuqqr_bf = a.wuqqr->data;
-    if (sc.x_i8) {
+    // When its fp16 A slots leave room for three stages (one row tile, T <= 64 at these shapes)
+    // the down-projection loads tokenX as int8 and widens it in shared memory beside the
+    // weights: no widening launch.
+    const bool x_a8 = sc.x_i8 && p.g1.msub == 1 &&
+                      (p.g1.bn == 192 ? W8Cfg<192, 1, 16, true, true>::max_stages(p.g1.a_box_rows)
+                                      : W8Cfg<64, 1, 16, true, true>::max_stages(p.g1.a_box_rows)) >= 3;
+    if (sc.x_i8 && !x_a8) {
         const long long n = (long long)d.T * d.He;
         const long long blocks = (n / 16 + 255) / 256;
         const int grid = (int)(blocks < 4096 ? (blocks > 0 ? blocks : 1) : 4096);
@@ -858,7 +877,8 @@ mla_status run(const Launched& L) {
         // integer sums); F1 applies tokenX's and the weights' dequant scales
         constexpr int BN = 192;
         if (p.g1.bn != BN && p.g1.bn != 64) return MLA_ERR_TILING;
-        if (!map_2d(&mA1, x_bf, d.T, d.He, (uint32_t)p.g1.a_box_rows) ||
+        if (!(x_a8 ? map_w8_rows(&mA1, a.x->data, d.T, d.He, (uint32_t)p.g1.a_box_rows)
+                   : map_2d(&mA1, x_bf, d.T, d.He, (uint32_t)p.g1.a_box_rows)) ||
             !map_w8_cols(&mB1a, a.wdq->data, d.He, d.Hcq, (uint32_t)p.g1.bn) ||
             !map_w8_cols(&mB1b, a.wdkvkr->data, d.He, d.Hckv + d.Dr, (uint32_t)p.g1.bn))
             return MLA_ERR_RUNTIME;
@@ -866,12 +886,15 @@ mla_status run(const Launched& L) {
         g1.b_split_col = (int)d.Hcq;
         g1.clear_status = 1;
         g1.out_f32 = y1;
+        g1.a_ready = x_a8 ? 1 : 0;   // int8 tokenX is read as passed
         if (p.g1.bn == BN)
-            e = p.g1.msub == 1 ? launch_gemm_w8<BN, 1, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
-                               : launch_gemm_w8<BN, 2, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+            e = x_a8                ? launch_gemm_w8<BN, 1, 16, true, EPI_F32, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
+                : p.g1.msub == 1 ? launch_gemm_w8<BN, 1, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
+                                 : launch_gemm_w8<BN, 2, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
         else
-            e = p.g1.msub == 1 ? launch_gemm_w8<64, 1, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
-                               : launch_gemm_w8<64, 2, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
+            e = x_a8                ? launch_gemm_w8<64, 1, 16, true, EPI_F32, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
+                : p.g1.msub == 1 ? launch_gemm_w8<64, 1, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1)
+                                 : launch_gemm_w8<64, 2, 16, true>(p.g1.grid, st, mA1, mB1a, mB1b, g1);
     } else {
     // 256-row tiles store their fp32 rows through shared memory with TMA (32 x 32 boxes of the
     // T x ncols1 matrix, or of the ksplit slots stacked when T is a multiple of 32); other k

@@ -44,18 +44,6 @@ struct PpPlan {
 
 bool pp_absent(const mla_tensor* t) { return t == nullptr || numel(t) == 0; }
 
-// int8 (rows, K) row-major weight, one row per output column: boxes of 64 * kW8Kb k (no
-// swizzle) x box_rows rows; rows and columns past the end read as zero.
-bool map_w8_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
-    const cuuint64_t gd[2] = {K, rows};
-    const cuuint64_t gs[1] = {K};
-    const cuuint32_t bx[2] = {(cuuint32_t)(64 * kW8Kb), box_rows};
-    const cuuint32_t es[2] = {1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gd, gs, bx, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 mla_status pp_validate(const PpArgs& a, PpDims& d) {
     const mla_tensor* req[] = {a.x,  a.g0,  a.b0, a.qs0, a.qo0, a.w1,  a.de0,   a.g1,   a.b1,    a.qs1,
                                a.qo1, a.w2, a.de1, a.g2,  a.cos, a.sin, a.wuk, a.kv, a.slots, a.qout, a.kv_out};
