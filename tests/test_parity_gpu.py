@@ -233,6 +233,14 @@ def test_tile_path_ragged(T):
     case("decode_t32", sample=24, T=T, block_num=8).check_all()
 
 
+@pytest.mark.parametrize("T", [1, 37, 100, 200])
+def test_int8_full_quant_ragged_token_counts(T):
+    """int8 inputs at ragged decode sizes: tokenX widened inside the down-projection (T <= 64,
+    short activation boxes), widened by its own launch with one 128-row tile (T = 100) and with
+    two sub-tiles (T = 200)."""
+    case("int8_t64", T=T).check_all()
+
+
 def test_int8_full_quant_many_tokens():
     """int8 inputs and int8 kv cache / q^N with T above the decode sizes: the warp-per-token
     row pass with its dequant scales, int8 c^Q codes and int8 cache rows."""
