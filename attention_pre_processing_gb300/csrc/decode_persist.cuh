@@ -742,8 +742,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             // ---- P3 epilogue: 1 / RMS per token, RoPE -> queryRopeOut, q^C -> P4's A operand
             // (token `row` in P4 row 16 (row / tpq) + row % tpq)
+            // Every TMEM column of P3 (q^C and the rope part) is read before P4 may start (its
+            // first group's accumulator reuses those columns); RoPE and the queryRopeOut stores
+            // then run beside P4's MMAs.
             ok = acc_ready(1);
-            if (ok && q * 16 < T) {
+            const bool act = ok && q * 16 < T;   // warp-uniform
+            float x0[32], x1[32];
+            if (act) {
                 const TmemSrc src{tmem_base + ((uint32_t)(q * 32) << 16)};
                 const uint32_t chain = smem_u32(aring);
                 const int prow = 16 * (row / tpq) + row % tpq;
@@ -755,9 +760,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     for (int i = 0; i < 32; ++i) v[i] *= inv;
                     if (rowok) chain_store(chain, kP4Blk, prow, ch * 32, v);
                 }
-                float x0[32], x1[32];
                 src.load(0, 0, 128, x0);
                 src.load(0, 0, 160, x1);
+            }
+            fence_proxy_async_smem();   // q^C written by threads, read by the tensor core
+            tc_fence_before();
+            mbar_arrive(smem_u32(chain_full));
+            if (act) {
                 if (rowok) {
                     float o0[32], o1[32];
 #pragma unroll
@@ -782,9 +791,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     store_bf16_chunk(dst + 32, o1, 32);
                 }
             }
-            fence_proxy_async_smem();   // q^C written by threads, read by the tensor core
-            tc_fence_before();
-            mbar_arrive(smem_u32(chain_full));
 
             // ---- P4 epilogue: queryOut through shared memory and TMA stores (boxes of the warp's
             // tpq tokens x 64 columns), group by group.  Staging: the ring slots of P4's first two
