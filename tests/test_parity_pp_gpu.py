@@ -137,6 +137,14 @@ def test_decode_full_oracle(name):
     PpCase(workloads.pp_config(name)).check()
 
 
+@pytest.mark.parametrize("T", [100, 200])
+def test_decode_shapes_ragged_token_counts(T):
+    """DeepSeek-V3 shapes at ragged token counts, every token: one 128-row tile with the
+    down-projection's 128-column tiles and one 512-column W^UK tile per head (T = 100), two
+    sub-tiles with 192-column tiles and two W^UK tiles per head (T = 200)."""
+    PpCase(workloads.pp_config("pp_decode_t32", T=T, block_num=8)).check()
+
+
 def test_t256_every_token():
     """The page's largest tokenNum (256), cacheMode 1, every token against the oracle."""
     PpCase(workloads.pp_config("pp_t256")).check()
