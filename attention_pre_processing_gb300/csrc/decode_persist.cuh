@@ -172,14 +172,15 @@ __device__ __forceinline__ bool poll_lanes(const T* base, int t0, int t1, Ready 
 // the counters read after it are this call's (the flag says the counter was reset); then the
 // counters.  The named barrier releases the other warps, and every thread then takes an
 // acquire fence for what the flags and counters published (a relaxed read that saw a release
-// write, followed by a fence, synchronises with it).
+// write, followed by a fence, synchronises with it).  `flags_seen`: these threads already waited
+// for the same flags in this call, so only the counters are polled (one L2 round trip fewer).
 __device__ __forceinline__ bool wait_tiles(const unsigned long long* zf, const unsigned int* cnt, int t0, int t1,
                                            unsigned int need, unsigned long long tag, const volatile int* abort,
-                                           int etid) {
+                                           int etid, bool flags_seen = false) {
     bool ok = true;
     if (etid < 32) {
         const uint64_t start = global_timer_ns();
-        ok = poll_lanes(zf, t0, t1, [tag](unsigned long long v) { return v == tag; }, start, abort);
+        if (!flags_seen) ok = poll_lanes(zf, t0, t1, [tag](unsigned long long v) { return v == tag; }, start, abort);
         if (ok && need > 0) {
             asm volatile("fence.acq_rel.gpu;" ::: "memory");
             ok = poll_lanes(cnt, t0, t1, [need](unsigned int v) { return v == need; }, start, abort);
@@ -668,7 +669,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 // wait for the counter), the chunk's slots are added in k-range order,
                 // bf16(gamma * y) goes to cq and each token's sum of y^2 over the chunk to ss;
                 // then the chunk's flag.
-                if (!*s_last) ok = wait_tiles(args.zflags, args.cnt, tile, tile + 1, (unsigned int)args.s1, args.tag, s_abort, etid);
+                // (the tile's flag was seen before the slot was stored)
+                if (!*s_last)
+                    ok = wait_tiles(args.zflags, args.cnt, tile, tile + 1, (unsigned int)args.s1, args.tag, s_abort, etid, true);
                 else asm volatile("fence.acq_rel.gpu;" ::: "memory");
                 for (int c = ks; ok && c < kChunks; c += args.s1) {
                     const int col0 = tile * kPTile + c * kPChunk;
