@@ -290,12 +290,10 @@ def run_cuda(args, rank, world):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_call": ms_per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded, DeepSeek-V3-shaped random weights)",
-            "config": {"workload": cfg.workload, "T": s.T, "He": s.He, "Hcq": s.Hcq, "N": s.N, "D": s.D,
-                       "Dr": s.Dr, "Hckv": s.Hckv, "kv_cache": f"{s.block_num}x{s.block_size}",
-                       "global_batch": s.T * world, "parallelism": f"replicas x{world}",
-                       "l2": ("flushed before every step: 2 x L2 bytes written, then another 2 x L2 bytes "
-                              "read, outside the timed events"),
-                       "timing": "CUDA events around each mla_prolog call on its stream"},
+            "config": dict(workload_config(cfg, world),
+                           l2=("flushed before every step: 2 x L2 bytes written, then another 2 x L2 bytes "
+                               "read, outside the timed events"),
+                           timing="CUDA events around each mla_prolog call on its stream"),
             "roofline": roofline, "step_roofline": step_roof, "kernels_ms": kern_ms,
             "gpu_launches": kernels_per_step * K,
             "us_per_call_mean": statistics.mean(step_ms) * 1e3,
@@ -542,6 +540,14 @@ def cpu_baseline(cfg, inp, budget_s=12.0, steps=None, threads=None):
             "sample": f"{done} tokens of {cfg.workload} in {elapsed:.1f} s (fp64 C, OpenMP over tokens)"}
 
 
+def workload_config(cfg, world):
+    """The workload keys of a bench line's config: the same on both arms."""
+    s = cfg.shape
+    return {"workload": cfg.workload, "T": s.T, "He": s.He, "Hcq": s.Hcq, "N": s.N, "D": s.D, "Dr": s.Dr,
+            "Hckv": s.Hckv, "kv_cache": f"{s.block_num}x{s.block_size}", "global_batch": s.T * world,
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -562,7 +568,8 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, DeepSeek-V3-shaped random weights)",
-            "config": {"workload": cfg.workload, "T": cfg.shape.T},
+            "config": dict(workload_config(cfg, world),
+                           timing="wall clock of the oracle's token loop on the host cores (OpenMP over tokens)"),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": vals[0]["cores"], "kind": "oracle",
                              "sample": f"{int(tok)} tokens over {args.steps} steps"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -56,3 +56,29 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
         steps, warmup = 1, 1
     bench.run_reference(A(), rank=1, world=2)   # returns at once: no oracle run, no line
     assert capsys.readouterr().out == ""
+
+
+def test_reference_line_shares_the_workload_config(capsys, monkeypatch):
+    """The reference arm's line carries the GPU arm's workload keys, metric and unit; the oracle
+    timing is stubbed (two steps of 32 tokens in 0.5 s each: 64 tokens/s)."""
+    import json
+    import bench
+    from attention_pre_processing_gb300 import workloads
+
+    def fake(cfg, inp, budget_s, threads=None):
+        return {"value": 64.0, "unit": "tokens/s", "cores": 2, "kind": "oracle",
+                "sample": f"32 tokens of {cfg.workload} in 0.5 s (fp64 C, OpenMP over tokens)"}
+    monkeypatch.setattr(bench, "cpu_baseline", fake)
+    monkeypatch.setattr(workloads, "make_inputs", lambda cfg: None)
+
+    class A:
+        steps, warmup = 2, 3
+    bench.run_reference(A(), rank=0, world=1)
+    line = json.loads(capsys.readouterr().out)
+    want = bench.workload_config(workloads.config(bench.HEADLINE), 1)
+    assert {k: line["config"][k] for k in want} == want
+    assert want["T"] == 32 and want["He"] == 7168 and want["N"] == 128
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["value"] == pytest.approx(64.0)
+    assert line["e2e"]["value"] == line["value"] and line["cpu_baseline"]["cores"] == 2
